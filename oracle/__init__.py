@@ -1,0 +1,200 @@
+"""CPU oracle for one tree-verification pass (numpy front end over oracle.c).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The product (the CUDA library and its binding) never imports it,
+and has no CPU fallback.
+
+What each function follows (page title, section):
+  * mask_build        -- "SpecInfer Guide: Tree-Based Speculative LLM Serving",
+                         "The Topology-Aware 2D Causal Mask"
+  * tree_attention    -- same page, "Generalizing Attention to Tree Topologies"
+                         and "Depth-First Flattening and KV Cache Reuse"
+  * verify_greedy     -- same page, "Greedy Verification Algorithm"
+  * verify_stochastic -- same page, "Stochastic Verification Algorithm", with
+                         the accept / residual rule of "Inference Optimization
+                         Techniques: Speed and Efficiency" (the
+                         "Misconception" section and its traced example)
+  * kv_commit         -- SpecInfer guide, "Depth-First Flattening and KV Cache
+                         Reuse" and "PagedKV Allocation with Zero-Copy Pruning"
+  * philox_uniforms   -- Philox4x32-10 (Salmon et al., SC'11)
+
+Pins (in tests/test_oracle_pins.py, all ``-m "not gpu"``):
+  * mask: the 6-node matrix printed on the SpecInfer guide (tests/golden),
+    chain tree == lower-triangular causal mask, brute-force ancestor sets;
+  * attention: every node equals plain causal attention over the gathered
+    sequence prefix + root path (independent fp64 routine, 1e-12); chain tree
+    with an empty prefix == torch scaled_dot_product_attention(is_causal);
+    q = 0 gives the mean of the visible values; bf16 rounding vs exact
+    rational rounding;
+  * greedy: brute force over all root paths; the adapted harness example of
+    the SpecInfer guide (tests/golden);
+  * stochastic: the two per-token examples of the "Inference Optimization
+    Techniques" page (tests/golden), a Monte-Carlo chi-square test that the
+    emitted tokens follow p, and the closed form E[T] = (1-a^(g+1))/(1-a) of
+    the same page on chains;
+  * canonical exp: <= 2 ulp from libm's fp64 exp;
+  * FX sums: equal to exact integer sums;
+  * commit: invariants against a snapshot gather;
+  * Philox: equal to the Philox4x32-10 engine shipped in PyTorch's headers.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+F32, BF16 = 0, 1
+ST_BAD_TREE, ST_BAD_TOKEN, ST_CAPACITY, ST_BAD_BLOCK, ST_BAD_PATH = 1, 2, 4, 16, 32
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i32, i64, u32, u64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_double
+        L.oracle_tree_mask_build.argtypes = [P, P, i32, i32, P, P, P]
+        L.oracle_tree_attention.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, i32, i32, i32, i32, i32, i32,
+                                            f64, P, i64, P, P, P]
+        L.oracle_verify_greedy.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P]
+        L.oracle_verify_stochastic.argtypes = [P, P, P, P, P, P, i32, i32, i32, P, P, P, P, P]
+        L.oracle_kv_commit.argtypes = [P, P, i64, P, i32, i32, i32, P, P, i32, P, i32, i32, i32, i32, P, P]
+        L.oracle_philox4x32_10.argtypes = [P, P, P]
+        L.oracle_philox_uniforms.argtypes = [u64, u32, P, i32, P]
+        L.oracle_canon_exp.argtypes = [ctypes.c_float]
+        L.oracle_canon_exp.restype = ctypes.c_float
+        L.oracle_canon_exp_array.argtypes = [P, P, i64]
+        L.oracle_fx.argtypes = [ctypes.c_float]
+        L.oracle_fx.restype = u64
+        L.oracle_f64_to_bf16.argtypes = [f64]
+        L.oracle_f64_to_bf16.restype = ctypes.c_uint16
+        L.oracle_residual.argtypes = [P, P, i32, i32, P, P, P]
+        _lib = L
+    return _lib
+
+
+def _c(a, dtype):
+    """Contiguous numpy array of the given dtype (no copy when already so)."""
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def mask_build(parent, tree_off, n_max):
+    parent, tree_off = _c(parent, np.int32), _c(tree_off, np.int32)
+    B, T, W = len(tree_off) - 1, int(tree_off[-1]), (n_max + 63) // 64
+    mask = np.zeros((T, W), np.uint64)
+    depth = np.zeros(T, np.int32)
+    status = np.zeros(B, np.int32)
+    lib().oracle_tree_mask_build(_p(parent), _p(tree_off), B, n_max, _p(mask), _p(depth), _p(status))
+    return mask, depth, status
+
+
+def tree_attention(q, k_cache, v_cache, block_table, block_size, prefix_len, tree_off, parent, n_max,
+                   Hq, Hkv, D, dtype, scale, rows=None, want_f64=False):
+    """q, k_cache, v_cache: float32 arrays, or uint16 arrays of bfloat16 bits
+    when dtype == BF16.  Returns (out, out_f64 or None, status)."""
+    edt = np.float32 if dtype == F32 else np.uint16
+    q, k_cache, v_cache = _c(q, edt), _c(k_cache, edt), _c(v_cache, edt)
+    block_table = _c(block_table, np.int32)
+    prefix_len, tree_off, parent = _c(prefix_len, np.int32), _c(tree_off, np.int32), _c(parent, np.int32)
+    B, T = len(tree_off) - 1, int(tree_off[-1])
+    max_blocks = block_table.shape[1] if block_table.ndim == 2 else block_table.size // max(B, 1)
+    num_blocks = k_cache.size // (Hkv * block_size * D)
+    out = np.zeros((T, Hq, D), edt)
+    out64 = np.zeros((T, Hq, D), np.float64) if want_f64 else None
+    status = np.zeros(B, np.int32)
+    rows_a = _c(rows, np.int64) if rows is not None else None
+    lib().oracle_tree_attention(_p(q), _p(k_cache), _p(v_cache), _p(block_table), max_blocks, block_size, num_blocks,
+                                _p(prefix_len), _p(tree_off), _p(parent), B, n_max, Hq, Hkv, D, dtype, float(scale),
+                                _p(rows_a), 0 if rows_a is None else len(rows_a), _p(out), _p(out64), _p(status))
+    return out, out64, status
+
+
+def _verify_outputs(B, n_max):
+    return (np.full((B, n_max), -1, np.int32), np.zeros(B, np.int32), np.full((B, n_max), -1, np.int32),
+            np.zeros(B, np.int32), np.zeros(B, np.int32))
+
+
+def verify_greedy(p_logits, tokens, parent, tree_off, n_max):
+    p_logits = _c(p_logits, np.float32)
+    tokens, parent, tree_off = _c(tokens, np.int32), _c(parent, np.int32), _c(tree_off, np.int32)
+    B, V = len(tree_off) - 1, p_logits.shape[-1]
+    path, alen, emitted, nem, status = _verify_outputs(B, n_max)
+    lib().oracle_verify_greedy(_p(p_logits), _p(tokens), _p(parent), _p(tree_off), B, n_max, V,
+                               _p(path), _p(alen), _p(emitted), _p(nem), _p(status))
+    return dict(path=path, accept_len=alen, emitted=emitted, n_emitted=nem, status=status)
+
+
+def verify_stochastic(p_logits, q_probs, tokens, parent, tree_off, uniforms, n_max):
+    p_logits, q_probs = _c(p_logits, np.float32), _c(q_probs, np.float32)
+    tokens, parent, tree_off = _c(tokens, np.int32), _c(parent, np.int32), _c(tree_off, np.int32)
+    uniforms = _c(uniforms, np.uint32)
+    B, V = len(tree_off) - 1, p_logits.shape[-1]
+    path, alen, emitted, nem, status = _verify_outputs(B, n_max)
+    lib().oracle_verify_stochastic(_p(p_logits), _p(q_probs), _p(tokens), _p(parent), _p(tree_off), _p(uniforms),
+                                   B, n_max, V, _p(path), _p(alen), _p(emitted), _p(nem), _p(status))
+    return dict(path=path, accept_len=alen, emitted=emitted, n_emitted=nem, status=status)
+
+
+def kv_commit(k_cache, v_cache, block_table, block_size, prefix_len, path, accept_len, Hkv, D, dtype, status):
+    """Returns (k_new, v_new, new_len, status_out); the inputs are not modified."""
+    edt = np.float32 if dtype == F32 else np.uint16
+    k_new, v_new = np.array(k_cache, dtype=edt, copy=True, order="C"), np.array(v_cache, dtype=edt, copy=True, order="C")
+    block_table = _c(block_table, np.int32)
+    prefix_len, path, accept_len = _c(prefix_len, np.int32), _c(path, np.int32), _c(accept_len, np.int32)
+    st = np.array(status, dtype=np.int32, copy=True)
+    B = len(prefix_len)
+    max_blocks = block_table.shape[1]
+    num_blocks = k_new.size // (Hkv * block_size * D)
+    new_len = np.zeros(B, np.int32)
+    lib().oracle_kv_commit(_p(k_new), _p(v_new), k_new.size, _p(block_table), max_blocks, block_size, num_blocks,
+                           _p(prefix_len), _p(path), path.shape[1], _p(accept_len), B, Hkv, D, dtype,
+                           _p(new_len), _p(st))
+    return k_new, v_new, new_len, st
+
+
+def philox4x32_10(ctr, key):
+    ctr, key = _c(ctr, np.uint32), _c(key, np.uint32)
+    out = np.zeros(4, np.uint32)
+    lib().oracle_philox4x32_10(_p(ctr), _p(key), _p(out))
+    return out
+
+
+def philox_uniforms(seed, round_, tree_off):
+    tree_off = _c(tree_off, np.int32)
+    B, T = len(tree_off) - 1, int(tree_off[-1])
+    out = np.zeros((T, 2), np.uint32)
+    lib().oracle_philox_uniforms(ctypes.c_uint64(seed), ctypes.c_uint32(round_), _p(tree_off), B, _p(out))
+    return out
+
+
+def canon_exp(x):
+    x = _c(x, np.float32)
+    y = np.empty_like(x)
+    lib().oracle_canon_exp_array(_p(x), _p(y), x.size)
+    return y
+
+
+def fx(v):
+    return int(lib().oracle_fx(ctypes.c_float(v)))
+
+
+def f64_to_bf16_bits(x):
+    return int(lib().oracle_f64_to_bf16(float(x)))
+
+
+def residual(l, q, j):
+    """Target distribution r_j and weights d_j of one row after j rejections."""
+    l, q = _c(l, np.float32), _c(q, np.float32)
+    V = l.size
+    r, d, S = np.zeros(V, np.float32), np.zeros(V, np.float32), np.zeros(1, np.uint64)
+    lib().oracle_residual(_p(l), _p(q), V, j, _p(r), _p(d), _p(S))
+    return r, d, int(S[0])
