@@ -1,0 +1,363 @@
+"""Benchmark: one tree-verification pass per step on the Llama-style decode
+layer workload (B=8, 32/8 heads, D=128, bf16, prefix 2048, 64-node expansion
+trees, V=32000, stochastic verification, then KV commit).
+
+A step = spec_tree_mask_build + spec_tree_attention + spec_tree_verify_stochastic
++ spec_kv_commit over one batch whose inputs are already in HBM.  Three input
+sets rotate between steps (each ~205 MB, together far above the 129 MB L2),
+so every step reads its inputs from DRAM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  Metric: tree-verify tokens/s = tokens emitted by the
+verifier per second of pass time.  For N > 1 (torchrun) every rank runs an
+independent replica (requests are independent; no collective on the data path).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify tokens/s"
+UNIT = "tokens/s"
+WORKLOAD = ("Llama-style decode layer: B=8, 32 query / 8 KV heads, head_dim 128, bf16, prefix 2048, 64-node "
+            "expansion trees (4,2,2,1,1,1,1,1) per request, V=32000, stochastic verification, KV commit")
+N_SETS = 3
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(w, stats):
+    """Per-launch algorithmic bytes of each kernel (formulas of the design)."""
+    s = 2 if w.dtype == 1 else 4
+    Wd = (w.n_max + 63) // 64
+    n = (w.tree_off[1:] - w.tree_off[:-1]).tolist()
+    P = w.prefix_len.tolist()
+    attn = sum(2 * w.Hkv * w.D * s * (P[b] + n[b]) + 2 * n[b] * w.Hq * w.D * s + 8 * n[b] * Wd for b in range(w.B))
+    internal = stats["internal_nodes"]
+    verify = 4 * w.T * w.V + 4 * w.V * internal
+    mask = 4 * w.T + 12 * w.T + 8 * w.T * Wd
+    commit = 2 * 2 * w.Hkv * w.D * s * stats["moved_rows"]
+    return dict(mask=mask, attention=attn, verify=verify, commit=commit)
+
+
+def _tree_stats(w, accept_paths):
+    par = w.parent.tolist()
+    off = w.tree_off.tolist()
+    internal = 0
+    for b in range(w.B):
+        kids = set(par[off[b] + i] for i in range(1, off[b + 1] - off[b]))
+        internal += len(kids)
+    moved = 0
+    for row in accept_paths:
+        moved += sum(1 for i, p in enumerate(row) if p >= 0 and p != i)
+    return dict(internal_nodes=internal, moved_rows=moved)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_cpu_baseline(w, seconds_cap=30.0):
+    """The oracle as it stands (plain C, one thread) on a bounded sample of the
+    same workload: request 0's full pass (mask, attention, stochastic verify,
+    commit).  Returns (tokens/s, sample description, seconds)."""
+    import numpy as np
+    import torch
+    import oracle as O
+    from workloads.gen import Workload
+
+    b = 0
+    lo, hi = int(w.tree_off[b]), int(w.tree_off[b + 1])
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    nblk = int((w.prefix_len[b] + (hi - lo) + w.block_size - 1) // w.block_size)
+    bt = w.block_table[b:b + 1, :nblk].contiguous()
+    # a one-request view of the same cache (the blocks this request owns)
+    t0 = time.perf_counter()
+    par = w.parent[lo:hi].numpy()
+    toff = np.array([0, hi - lo], np.int32)
+    O.mask_build(par, toff, w.n_max)
+    O.tree_attention(bits(w.q[lo:hi]), bits(w.k_cache), bits(w.v_cache), bt.numpy(), w.block_size,
+                     w.prefix_len[b:b + 1].numpy(), toff, par, w.n_max, w.Hq, w.Hkv, w.D, w.dtype, w.scale)
+    r = O.verify_stochastic(w.p_logits[lo:hi].numpy(), w.q_probs[lo:hi].numpy(), w.tokens[lo:hi].numpy(), par, toff,
+                            w.uniforms[lo:hi].numpy().view(np.uint32), w.n_max)
+    O.kv_commit(bits(w.k_cache), bits(w.v_cache), bt.numpy(), w.block_size, w.prefix_len[b:b + 1].numpy(),
+                r["path"], r["accept_len"], w.Hkv, w.D, w.dtype, np.zeros(1, np.int32))
+    dt = time.perf_counter() - t0
+    tokens = int(r["n_emitted"][0])
+    return tokens / dt, f"request 0 of the batch (1 of {w.B}): full pass in the oracle, {dt:.2f} s", dt
+
+
+def bench_reference(args):
+    """--impl reference: the CPU oracle as the reference arm (timed on the host)."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import workloads as W
+    w = W.config1()
+    times, toks = [], 0
+    for i in range(args.warmup + args.steps):
+        v, sample, dt = run_cpu_baseline(w)
+        if i >= args.warmup:
+            times.append(dt)
+            toks = v * dt
+    total = sum(times)
+    value = toks * len(times) / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_gpu(args):
+    import torch
+    import workloads as W
+    import tree_speculative_verification_spec_gb300 as S
+    from tree_speculative_verification_spec_gb300 import build as B_
+    from tree_speculative_verification_spec_gb300.pipeline import DeviceBatch, VerifyPass
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    B_.build()
+    S.lib()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    sets, passes, works = [], [], []
+    for i in range(N_SETS):
+        w = W.config1(seed=1001 + 97 * rank + i)
+        works.append(w)
+        d = DeviceBatch.from_workload(w, device=dev)
+        sets.append(d)
+        passes.append(VerifyPass(d))
+    torch.cuda.synchronize()
+
+    def step(i, ev=None):
+        vp = passes[i % N_SETS]
+        if ev is not None:
+            ev[0].record(stream)
+        vp.mask_build()
+        if ev is not None:
+            ev[1].record(stream)
+        vp.attention(args.attn_flags)
+        if ev is not None:
+            ev[2].record(stream)
+        vp.verify(args.mode)
+        if ev is not None:
+            ev[3].record(stream)
+        vp.commit()
+        if ev is not None:
+            ev[4].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    stage = {k: [] for k in ("mask", "attention", "verify", "commit")}
+    for e in evs:
+        for j, k in enumerate(stage):
+            stage[k].append(e[j].elapsed_time(e[j + 1]))
+
+    # emitted tokens per step (verify inputs do not change between steps of one set)
+    tokens_per_set = [int(p.n_emitted[:p.batch.B].sum()) for p in passes]
+    status_ok = all(int(p.status[:p.batch.B].abs().sum()) == 0 for p in passes)
+    tokens = sum(tokens_per_set[(args.warmup + i) % N_SETS] for i in range(args.steps))
+    if world > 1:
+        t = torch.tensor([elapsed_ms, float(tokens)], dtype=torch.float64, device=dev)
+        mx = t.clone()
+        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+        sm = t.clone()
+        torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
+        elapsed_ms, tokens = float(mx[0]), float(sm[1])
+    value = tokens / (elapsed_ms / 1e3)
+
+    # --- e2e through the C ABI with host buffers: H2D of the step's inputs from
+    # pinned memory, the pass, D2H of the emitted tokens; KV cache is resident state.
+    e2e = run_e2e(args, works, sets, passes, stream, dev)
+
+    # --- roofline of the dominant kernel
+    peak, peak_kind = _peaks()
+    w0 = works[0]
+    stats = _tree_stats(w0, passes[0].path[:w0.B].tolist())
+    algo = algorithmic_bytes(w0, stats)
+    avg = {k: statistics.mean(v) for k, v in stage.items()}
+    dom = max(("attention", "verify"), key=lambda k: avg[k])
+    kernels = {k: {"ms": avg[k], "bytes": algo[k], "gbs": algo[k] / (avg[k] * 1e-3) / 1e9,
+                   "frac_hbm": algo[k] / (avg[k] * 1e-3) / 1e9 / peak} for k in avg}
+    achieved = kernels[dom]["gbs"]
+    launches_per_step = 4 + (1 if _attn_splits(passes[0]) > 1 else 0)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "verify": args.mode, "input_sets": N_SETS,
+                       "l2": "3 rotating input sets of ~205 MB each (inputs larger than L2)",
+                       "tokens_per_step": tokens / args.steps / max(world, 1), "status_ok": status_ok,
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "clocks": clk.summary(),
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind},
+            "kernels": kernels}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, _ = run_cpu_baseline(works[0])
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def _attn_splits(vp):
+    import tree_speculative_verification_spec_gb300 as S
+    b = vp.batch
+    return 2 if S.spec_attention_workspace_size(b.B, b.T, b.n_max, b.max_prefix, b.Hq, b.Hkv, b.D) > 256 else 1
+
+
+def run_e2e(args, works, sets, passes, stream, dev):
+    import torch
+    steps = max(3, args.steps)
+    host = []
+    for w in works:
+        h = {k: getattr(w, k).pin_memory() for k in ("q", "parent", "tokens", "tree_off", "prefix_len", "p_logits",
+                                                      "q_probs", "uniforms")}
+        host.append(h)
+    out_tok = [torch.empty((p.batch.B, p.batch.n_max), dtype=torch.int32).pin_memory() for p in passes]
+    out_n = [torch.empty(p.batch.B, dtype=torch.int32).pin_memory() for p in passes]
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = out_tok[0].numel() * 4 + out_n[0].numel() * 4
+
+    def e2e_step(i):
+        j = i % N_SETS
+        d, vp, h = sets[j], passes[j], host[j]
+        for k, t in h.items():
+            getattr(d, k).copy_(t, non_blocking=True)
+        vp.run(args.mode, args.attn_flags)
+        out_tok[j].copy_(vp.emitted, non_blocking=True)
+        out_n[j].copy_(vp.n_emitted, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        e2e_step(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    toks = sum(int(out_n[i % N_SETS].sum()) for i in range(steps))
+    return {"value": toks / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms / steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--mode", default="stochastic", choices=["stochastic", "greedy"])
+    ap.add_argument("--attn-flags", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,222 @@
+/*
+ * spectree.h -- C ABI of the GB300 (sm_103a) tree speculative verification
+ * library (libspectree.so).
+ *
+ * One verification pass of tree-based speculative inference: the target model
+ * checks a whole token tree in one forward pass, with every tree node attending
+ * to the committed prefix plus its own ancestors, then a verifier picks the
+ * accepted root path (greedy, or stochastic with the min(1, p/q) accept rule
+ * and the norm(max(p - q, 0)) residual), and the KV cache keeps only that path.
+ * Sources, by page title and section:
+ *   "SpecInfer Guide: Tree-Based Speculative LLM Serving": "Mathematical
+ *     Formulation of the Token Tree", "Tree-Based Parallel Decoding &
+ *     Topology-Aware Causal Masking", "Depth-First Flattening and KV Cache
+ *     Reuse", "Exact Output Verification: Greedy and Stochastic Sampling",
+ *     "Integration with Continuous Batching", "PagedKV Allocation with
+ *     Zero-Copy Pruning".
+ *   "Inference Optimization Techniques: Speed and Efficiency": the accept rule
+ *     and residual of the "Misconception" section, "Traced Example".
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is DEVICE memory owned by the caller, except where
+ *     a call says otherwise.  The library never allocates, frees or
+ *     synchronises; each call enqueues kernels on `stream` (a cudaStream_t,
+ *     NULL = the legacy default stream) and returns.
+ *   - A batch holds B requests.  Request b owns tree nodes
+ *     [tree_off[b], tree_off[b+1]) of every per-node array (ragged packing).
+ *     Inside a request nodes are numbered 0..n_b-1 (local index); node 0 is
+ *     the root, the last verified token, and parent[t] is the LOCAL index of
+ *     the parent (-1 for the root).  Parents come before children:
+ *     0 <= parent[i] < i.  n_b <= n_max <= 1024.
+ *   - mask rows have W = ceil(n_max / 64) 64-bit words.
+ *   - The return value reports errors visible on the host (bad scalar
+ *     arguments, NULL pointers, unsupported sizes, launch failures); on such
+ *     an error nothing is launched.  Errors that depend on device data are
+ *     or-ed into the caller's int32 status[B] as SPEC_DEV_* bits; no kernel
+ *     traps or asserts.
+ *   - Paged KV cache: k_cache and v_cache are [num_blocks][Hkv][block_size][D]
+ *     elements of `dtype`; slot s of request b lives in block
+ *     block_table[b * max_blocks + s / block_size], row s % block_size.  Slots
+ *     [0, prefix_len[b]) hold the committed prefix and slots
+ *     prefix_len[b] + v hold tree node v (already written by the caller).
+ */
+#ifndef SPECTREE_H
+#define SPECTREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t spec_status;
+
+/* Host-visible status codes (return values). */
+#define SPEC_OK 0
+#define SPEC_ERR_INVALID_ARG 1 /* NULL pointer, negative size, Hq not a multiple of Hkv, ... */
+#define SPEC_ERR_UNSUPPORTED 2 /* D not 64/128, n_max > 1024, V > 131072, block_size not a power of two in [8, 65536] */
+#define SPEC_ERR_CUDA 3        /* a CUDA launch or attribute call failed */
+#define SPEC_ERR_WORKSPACE 4   /* workspace smaller than the matching *_workspace_size() */
+
+/* Per-request device status bits, or-ed into status[b]. */
+#define SPEC_DEV_BAD_TREE 1   /* parent[0] != -1, parent[i] outside [0, i), n_b < 0 or n_b > n_max */
+#define SPEC_DEV_BAD_TOKEN 2  /* a node token outside [0, V) */
+#define SPEC_DEV_CAPACITY 4   /* prefix_len < 0, prefix_len > max_prefix, or prefix_len + n_b beyond the block table */
+#define SPEC_DEV_TIMEOUT 8    /* a bounded device wait expired (the kernel returned early) */
+#define SPEC_DEV_BAD_BLOCK 16 /* a block-table entry outside [0, num_blocks) */
+#define SPEC_DEV_BAD_PATH 32  /* a commit path that is not strictly increasing from node 0 */
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* spec_tree_attention flags */
+#define SPEC_ATTN_AUTO 0u       /* tcgen05 tensor-core path for bf16 when a KV group has >= 64 query rows */
+#define SPEC_ATTN_CUDA_CORE 1u  /* force the CUDA-core path */
+#define SPEC_ATTN_TCGEN05 2u    /* force the tcgen05 path (bf16 only) */
+
+/* Library version, (major << 16) | minor. */
+int spec_version(void);
+
+/* Human-readable name of a return code or of one SPEC_DEV_* bit. */
+const char* spec_status_string(spec_status s);
+
+/*
+ * Topology mask build.  "SpecInfer Guide", "The Topology-Aware 2D Causal Mask":
+ * M[u][v] = 0 if v is u or an ancestor of u, else -inf; here packed as bits.
+ *   parent   int32 [T]     local parent index per node (-1 at the root)
+ *   tree_off int32 [B+1]   request offsets into the node arrays
+ *   mask     uint64 [T][W] out: bit v of word v/64 of row u set iff v is u or an ancestor of u
+ *   depth    int32 [T]     out: number of ancestors of the node (root 0)
+ *   status   int32 [B]     out: WRITTEN (not or-ed): 0, or SPEC_DEV_BAD_TREE; this call
+ *                          starts a verification pass.  A bad request gets all-zero mask
+ *                          rows and depth -1.
+ */
+spec_status spec_tree_mask_build(const int32_t* parent, const int32_t* tree_off, int B, int n_max,
+                                 uint64_t* mask, int32_t* depth, int32_t* status, void* stream);
+
+/* Bytes of workspace spec_tree_attention needs for this shape (T = tree_off[B],
+ * max_prefix = the largest prefix_len the call may see). */
+size_t spec_attention_workspace_size(int B, int T, int n_max, int max_prefix, int Hq, int Hkv, int D);
+
+/*
+ * Tree attention.  "SpecInfer Guide", "Generalizing Attention to Tree
+ * Topologies" and "Depth-First Flattening and KV Cache Reuse": for request b,
+ * node u and query head h, out = sum_k softmax_k(scale * q . K_k) V_k over the
+ * keys k in slots [0, prefix_len[b]) (the committed prefix) and slots
+ * prefix_len[b] + v for every v with mask bit v of row u set (the node and
+ * its ancestors).  Query head h reads kv-head h / (Hq / Hkv).  fp32
+ * accumulation; bf16 inputs give bf16 output.
+ *   q        [T][Hq][D] dtype   queries (positions already applied; RoPE position = prefix + depth)
+ *   k_cache, v_cache            paged cache, see the conventions above
+ *   block_table int32 [B][max_blocks]
+ *   prefix_len  int32 [B]       committed prefix length per request (<= max_prefix)
+ *   mask        from spec_tree_mask_build
+ *   out      [T][Hq][D] dtype   out
+ *   workspace   device scratch of spec_attention_workspace_size() bytes
+ *   status   int32 [B]          in/out: or-ed with SPEC_DEV_CAPACITY / SPEC_DEV_BAD_BLOCK.
+ *                               Requests whose status is non-zero on entry are skipped;
+ *                               a flagged request's output rows are unspecified.
+ *   flags       SPEC_ATTN_*
+ */
+spec_status spec_tree_attention(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, int max_blocks, int block_size, int num_blocks,
+                                const int32_t* prefix_len, const int32_t* tree_off, const uint64_t* mask,
+                                int B, int T, int n_max, int max_prefix, int Hq, int Hkv, int D,
+                                spec_dtype dtype, float scale, void* out,
+                                void* workspace, size_t workspace_bytes, int32_t* status,
+                                uint32_t flags, void* stream);
+
+/* Bytes of workspace the verifiers need. */
+size_t spec_verify_workspace_size(int B, int n_max, int V);
+
+/*
+ * Greedy token-tree verification.  "SpecInfer Guide", "Greedy Verification
+ * Algorithm": starting at the root, descend into the child whose token equals
+ * argmax of the current node's target logits; when none matches, emit that
+ * argmax and stop.  p_logits[t] is the target's next-token logits after node
+ * t's sequence, so child c is tested against argmax(p_logits[parent c]).
+ * The accepted node f is the deepest node whose whole root path follows the
+ * argmax chain (ties between equally deep nodes: lowest node index; with
+ * distinct sibling tokens this is the walk above).  argmax ties go to the
+ * lowest token id.  Logits must be finite.
+ *   p_logits   float [T][V]
+ *   tokens     int32 [T]       draft token of each node (the root's is not used for matching)
+ *   parent, tree_off, mask, depth  as produced / consumed by spec_tree_mask_build
+ *   path       int32 [B][n_max] out: accepted nodes root first (local indices), then -1
+ *   accept_len int32 [B]       out: number of accepted nodes including the root
+ *   emitted    int32 [B][n_max] out: tokens of path[1..] then the correction / bonus token, then -1
+ *   n_emitted  int32 [B]       out: = accept_len
+ *   workspace  device scratch of spec_verify_workspace_size() bytes (no state between calls)
+ *   status     int32 [B]       in/out: or-ed with SPEC_DEV_BAD_TOKEN; a request whose status is
+ *                              non-zero after the call has accept_len = n_emitted = 0 and -1 rows.
+ */
+spec_status spec_tree_verify_greedy(const float* p_logits, const int32_t* tokens, const int32_t* parent,
+                                    const int32_t* tree_off, const uint64_t* mask, const int32_t* depth,
+                                    int B, int n_max, int V,
+                                    int32_t* path, int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
+                                    void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Stochastic token-tree verification (multi-step speculative sampling over a
+ * tree).  "SpecInfer Guide", "Stochastic Verification Algorithm" with the
+ * rule of "Inference Optimization Techniques" ("Misconception" section):
+ * a draft token x is accepted with probability min(1, p(x)/q(x)); after a
+ * rejection the target becomes norm(max(p - q, 0)).  The children of a node
+ * are tried in increasing node index, each against the residual left by the
+ * siblings rejected before it; the first accepted child becomes the current
+ * node.  When every child is rejected, a token is sampled from the last
+ * residual; at a leaf, the bonus token is sampled from p.  The emitted tokens
+ * follow the target distribution when each node's children were drawn
+ * i.i.d. from q_probs of that node.
+ * Arithmetic (fixed so that every decision is reproducible bit for bit):
+ * p = softmax(p_logits) with its own fp32 exp (x <= 0: Cody-Waite reduction,
+ * degree-7 Taylor polynomial), normalisers as exact fixed-point sums of
+ * trunc(v * 2^46); accept iff u * q(t) <= r(t) with u = (word0 >> 8) * 2^-24;
+ * terminal sample = smallest x whose fixed-point prefix sum exceeds
+ * floor(word1 * S / 2^32).
+ *   q_probs    float [T][V]    row u: the draft distribution the children of u were drawn from
+ *   uniforms   uint32 [T][2]   raw random words: [t][0] acceptance word of node t,
+ *                              [t][1] sampling word used if the walk stops at node t
+ *   other arguments as in spec_tree_verify_greedy (no mask / depth needed)
+ */
+spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_probs, const int32_t* tokens,
+                                        const int32_t* parent, const int32_t* tree_off, const uint32_t* uniforms,
+                                        int B, int n_max, int V,
+                                        int32_t* path, int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
+                                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * KV commit / rollback.  "SpecInfer Guide", "Depth-First Flattening and KV
+ * Cache Reuse" and "PagedKV Allocation with Zero-Copy Pruning": only the
+ * accepted path stays.  In place, for every kv-head: slot prefix_len[b] + i
+ * receives the old slot prefix_len[b] + path[b][i], i < accept_len[b] (rows
+ * already in place are not copied); new_len[b] = prefix_len[b] + accept_len[b].
+ * Requests with a non-zero status on entry, or accept_len 0, are untouched
+ * (new_len = prefix_len).  A path that is not strictly increasing from 0 or
+ * leaves the block table sets SPEC_DEV_BAD_PATH; a bad block id sets
+ * SPEC_DEV_BAD_BLOCK; such requests are untouched.
+ *   path        int32 [B][path_stride]  accepted local node indices, root first
+ *   accept_len  int32 [B]
+ *   new_len     int32 [B] out
+ *   status      int32 [B] in/out (or-ed)
+ */
+spec_status spec_kv_commit(void* k_cache, void* v_cache, const int32_t* block_table, int max_blocks,
+                           int block_size, int num_blocks, const int32_t* prefix_len, const int32_t* path,
+                           int path_stride, const int32_t* accept_len, int B, int Hkv, int D, spec_dtype dtype,
+                           int32_t* new_len, int32_t* status, void* stream);
+
+/*
+ * Philox4x32-10 random words for one verification round (Salmon et al.,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC'11): node u (local index)
+ * of request b uses counter (u, b, round, 0) and key (seed low 32 bits, seed
+ * high 32 bits); out[t][0] = output word 0, out[t][1] = output word 1.
+ *   tree_off int32 [B+1]; out uint32 [T][2]; n_max bounds n_b (larger requests are skipped).
+ */
+spec_status spec_philox_uniforms(uint64_t seed, uint32_t round, const int32_t* tree_off, int B, int n_max,
+                                 uint32_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECTREE_H */

@@ -358,9 +358,10 @@ def _p_row(key, V):
     return rng.dirichlet(np.full(V, 0.7))
 
 
-def _run_mc_tree(oracle, n_trials, V, root_kids, kid_kids, seed):
-    """Trials of a depth-2 tree whose draft tokens are i.i.d. draws from the
-    parent's draft row; p and q rows are fixed functions of the token path."""
+def mc_tree_inputs(n_trials, V, root_kids, kid_kids, seed):
+    """Inputs of n_trials depth-2 trees whose draft tokens are i.i.d. draws
+    from the parent's draft row; p and q rows are fixed functions of the token
+    path.  Returns (dict of verifier inputs, table of p rows by path)."""
     rng = np.random.default_rng(seed)
     key0 = seed * 1000
 
@@ -402,10 +403,15 @@ def _run_mc_tree(oracle, n_trials, V, root_kids, kid_kids, seed):
             flat = sel.reshape(n_trials, -1)
             logp[:, 1 + root_kids:][flat] = np.log(P1[(a, b)])
     uni = rng.integers(0, 2 ** 32, (n_trials * n, 2), dtype=np.uint64).astype(np.uint32)
-    r = oracle.verify_stochastic(logp.reshape(-1, V), qpr.reshape(-1, V), tokens.reshape(-1),
-                                 np.tile(parent, n_trials), np.arange(0, n * n_trials + 1, n, dtype=np.int32),
-                                 uni, n)
-    return r, P1
+    inputs = dict(p_logits=logp.reshape(-1, V), q_probs=qpr.reshape(-1, V), tokens=tokens.reshape(-1),
+                  parent=np.tile(parent, n_trials), tree_off=np.arange(0, n * n_trials + 1, n, dtype=np.int32),
+                  uniforms=uni, n_max=n)
+    return inputs, P1
+
+
+def _run_mc_tree(oracle, n_trials, V, root_kids, kid_kids, seed):
+    inputs, P1 = mc_tree_inputs(n_trials, V, root_kids, kid_kids, seed)
+    return oracle.verify_stochastic(**inputs), P1
 
 
 def _chisq_pvalue(counts, probs):

@@ -1,0 +1,378 @@
+"""GPU parity: every step of the pass through the C ABI against the CPU oracle
+on the same seeded inputs.  Bit-exact for masks, depths, uniforms, paths,
+emitted tokens, commit results and status words; attention within max-abs
+1e-5 (fp32) or 2e-2 + 1e-2 |ref| (bf16 inputs)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+import tree_speculative_verification_spec_gb300 as S
+from tree_speculative_verification_spec_gb300.pipeline import DeviceBatch, VerifyPass
+from parity import (attn_tolerance_ok, np_elems, oracle_attention, oracle_greedy, oracle_mask, oracle_stochastic,
+                    out_as_f32)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tree_speculative_verification_spec_gb300 import build
+    build.build()
+    S.lib()
+
+
+def _pass(w, **kw):
+    vp = VerifyPass(DeviceBatch.from_workload(w, **kw))
+    return vp
+
+
+# ------------------------------------------------------------------ mask ----
+
+def _ragged_trees(seed, sizes, n_max):
+    g = np.random.Generator(np.random.PCG64(seed))
+    pars = [W.random_parent_tree(n, g) if n > 0 else torch.zeros(0, dtype=torch.int32) for n in sizes]
+    return pars
+
+
+@pytest.mark.parametrize("sizes,n_max", [([16], 16), ([1, 64, 65, 0, 130], 130), ([1024], 1024),
+                                         ([300, 7, 0, 0, 257], 300)])
+def test_mask_build_parity(sizes, n_max):
+    pars = _ragged_trees(sum(sizes), sizes, n_max)
+    parent = torch.cat(pars)
+    tree_off = torch.tensor(np.cumsum([0] + sizes), dtype=torch.int32)
+    if len(sizes) > 2:  # plant a bad tree in request 1
+        parent[tree_off[1] + 3] = 70
+    m_ref, d_ref, s_ref = O.mask_build(parent.numpy(), tree_off.numpy(), n_max)
+    B, T, Wd = len(sizes), int(tree_off[-1]), (n_max + 63) // 64
+    mask = torch.zeros((T, Wd), dtype=torch.int64, device="cuda")
+    depth = torch.zeros(T, dtype=torch.int32, device="cuda")
+    status = torch.full((B,), 99, dtype=torch.int32, device="cuda")
+    S.spec_tree_mask_build(parent.cuda(), tree_off.cuda(), B, n_max, mask, depth, status)
+    torch.cuda.synchronize()
+    assert np.array_equal(mask.cpu().numpy().view(np.uint64), m_ref)
+    assert np.array_equal(depth.cpu().numpy(), d_ref)
+    assert np.array_equal(status.cpu().numpy(), s_ref)
+
+
+def test_mask_build_chain_and_printed_example():
+    parent = torch.tensor([-1, 0, 0, 1, 1, 2] + list(range(-1, 99)), dtype=torch.int32)
+    tree_off = torch.tensor([0, 6, 106], dtype=torch.int32)
+    m_ref, d_ref, s_ref = O.mask_build(parent.numpy(), tree_off.numpy(), 100)
+    mask = torch.zeros((106, 2), dtype=torch.int64, device="cuda")
+    depth = torch.zeros(106, dtype=torch.int32, device="cuda")
+    status = torch.zeros(2, dtype=torch.int32, device="cuda")
+    S.spec_tree_mask_build(parent.cuda(), tree_off.cuda(), 2, 100, mask, depth, status)
+    assert np.array_equal(mask.cpu().numpy().view(np.uint64), m_ref)
+    assert np.array_equal(depth.cpu().numpy(), d_ref)
+
+
+# ---------------------------------------------------------------- Philox ----
+
+@pytest.mark.parametrize("seed,rnd", [(0, 0), (0xdeadbeefcafef00d, 7), (12345, 0xffffffff)])
+def test_philox_parity(seed, rnd):
+    tree_off = torch.tensor([0, 16, 16, 80, 1104], dtype=torch.int32)
+    ref = O.philox_uniforms(seed, rnd, tree_off.numpy())
+    out = torch.zeros((1104, 2), dtype=torch.int32, device="cuda")
+    S.spec_philox_uniforms(seed, rnd, tree_off.cuda(), 4, 1024, out)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref)
+
+
+# ---------------------------------------------------------------- verify ----
+
+def _gpu_verify(w, mode):
+    vp = _pass(w)
+    vp.mask_build()
+    vp.verify(mode)
+    torch.cuda.synchronize()
+    return dict(path=vp.path.cpu().numpy(), accept_len=vp.accept_len.cpu().numpy(),
+                emitted=vp.emitted.cpu().numpy(), n_emitted=vp.n_emitted.cpu().numpy(),
+                status=vp.status.cpu().numpy())
+
+
+def _assert_verify_equal(got, ref, B):
+    for k in ("path", "accept_len", "emitted", "n_emitted", "status"):
+        assert np.array_equal(got[k][:B], ref[k][:B]), (k, got[k][:B], ref[k][:B])
+
+
+SMALL_VERIFY = [dict(seed=s, B=B, n_range=nr, V=V) for s, B, nr, V in [
+    (1, 4, (1, 12), 2), (2, 6, (1, 40), 7), (3, 5, (0, 64), 64), (4, 3, (1, 300), 513), (5, 2, (60, 90), 1000),
+    (6, 8, (1, 30), 4099), (7, 2, (10, 30), 32000), (8, 1, (5, 9), 40000), (9, 2, (3, 20), 128256)]]
+
+
+@pytest.mark.parametrize("cfg", SMALL_VERIFY, ids=lambda c: f"V{c['V']}_s{c['seed']}")
+@pytest.mark.parametrize("mode", ["greedy", "stochastic"])
+def test_verify_parity_random_trees(cfg, mode):
+    w = W.small_random(cfg["seed"], B=cfg["B"], n_range=cfg["n_range"], prefix_range=(0, 4), Hq=2, Hkv=1, D=64,
+                       V=cfg["V"], block_size=16)
+    if mode == "greedy":
+        # make matches likely: child tokens copy the parent's argmax half of the time
+        am = w.p_logits.argmax(1)
+        g = np.random.default_rng(cfg["seed"])
+        for b in range(w.B):
+            off = int(w.tree_off[b])
+            for u in range(1, int(w.tree_off[b + 1]) - off):
+                if g.random() < 0.6:
+                    w.tokens[off + u] = am[off + int(w.parent[off + u])]
+        ref = oracle_greedy(w)
+    else:
+        ref = oracle_stochastic(w)
+    got = _gpu_verify(w, mode)
+    _assert_verify_equal(got, ref, w.B)
+
+
+@pytest.mark.parametrize("mode", ["greedy", "stochastic"])
+def test_verify_parity_many_siblings_and_duplicates(mode):
+    """A star root with 200 children whose tokens repeat: long sibling loops,
+    many residual updates, equal sibling tokens."""
+    n, V, B = 201, 33, 3
+    g = np.random.default_rng(3)
+    parent = torch.tensor([-1] + [0] * (n - 1), dtype=torch.int32)
+    w = W.small_random(40, B=B, n_range=(n, n), prefix_range=(0, 1), Hq=2, Hkv=1, D=64, V=V, block_size=16)
+    w.parent = torch.cat([parent] * B)
+    w.tokens = torch.from_numpy(g.integers(0, 4, B * n).astype(np.int32))
+    # draft rows far from the target: rejections are frequent
+    w.q_probs = torch.softmax(torch.from_numpy(g.standard_normal((B * n, V)).astype(np.float32)) * 4, -1)
+    ref = oracle_greedy(w) if mode == "greedy" else oracle_stochastic(w)
+    got = _gpu_verify(w, mode)
+    _assert_verify_equal(got, ref, B)
+
+
+@pytest.mark.parametrize("mode", ["greedy", "stochastic"])
+def test_verify_bad_inputs(mode):
+    w = W.small_random(41, B=4, n_range=(3, 8), prefix_range=(0, 1), Hq=2, Hkv=1, D=64, V=50, block_size=16)
+    off = w.tree_off.numpy()
+    w.tokens[off[1] + 1] = 50          # out of range token
+    w.tokens[off[2]] = -3              # bad root token
+    w.parent[off[3] + 2] = 2           # parent not before child
+    ref = oracle_greedy(w) if mode == "greedy" else oracle_stochastic(w)
+    got = _gpu_verify(w, mode)
+    _assert_verify_equal(got, ref, w.B)
+    assert got["status"][0] == 0 and got["status"][1] == S.SPEC_DEV_BAD_TOKEN
+    assert got["status"][3] & S.SPEC_DEV_BAD_TREE
+
+
+def test_verify_empty_requests():
+    """Requests with no tree nodes are idle: accept_len 0, rows of -1, status 0."""
+    g = np.random.Generator(np.random.PCG64(42))
+    sizes = [0, 5, 0, 0, 3]
+    pars = [W.random_parent_tree(n, g) if n else torch.zeros(0, dtype=torch.int32) for n in sizes]
+    toks = [torch.from_numpy(g.integers(0, 50, n).astype(np.int32)) for n in sizes]
+    T = sum(sizes)
+    logits = torch.from_numpy(g.standard_normal((T, 50)).astype(np.float32))
+    draft = torch.softmax(logits + 1, -1)
+    w = W.gen._pack("empty requests", len(sizes), 2, 1, 64, W.BF16, 50, 8, 16, pars, toks, [3] * len(sizes), g,
+                    logits, draft)
+    for mode in ("greedy", "stochastic"):
+        ref = oracle_greedy(w) if mode == "greedy" else oracle_stochastic(w)
+        got = _gpu_verify(w, mode)
+        _assert_verify_equal(got, ref, w.B)
+        assert got["accept_len"].tolist() == [0, ref["accept_len"][1], 0, 0, ref["accept_len"][4]]
+
+
+@pytest.mark.parametrize("which", [0, 1, 2])
+@pytest.mark.parametrize("mode", ["greedy", "stochastic"])
+def test_verify_parity_workloads(which, mode):
+    """The pages' workloads at full size (configs 0, 1, 2)."""
+    w = W.make_config(which)
+    ref = oracle_greedy(w) if mode == "greedy" else oracle_stochastic(w)
+    got = _gpu_verify(w, mode)
+    _assert_verify_equal(got, ref, w.B)
+    assert (got["status"][:w.B] == 0).all()
+
+
+def test_verify_philox_uniforms_from_both_sides():
+    """Workload 0 as specified: stochastic verification with Philox words from
+    seed 0 (each side generates its own; the words match bit for bit)."""
+    w = W.make_config(0)
+    w.uniforms = torch.from_numpy(O.philox_uniforms(0, 0, w.tree_off.numpy()).view(np.int32))
+    ref = oracle_stochastic(w)
+    vp = _pass(w)
+    S.spec_philox_uniforms(0, 0, vp.batch.tree_off, w.B, w.n_max, vp.batch.uniforms)
+    vp.mask_build()
+    vp.verify("stochastic")
+    torch.cuda.synchronize()
+    assert vp.path.cpu().numpy()[0].tolist() == ref["path"][0].tolist()
+    assert vp.emitted.cpu().numpy()[0].tolist() == ref["emitted"][0].tolist()
+
+
+def test_stochastic_gpu_matches_oracle_on_monte_carlo_trees():
+    """The oracle's Monte-Carlo losslessness workload through the GPU verifier:
+    identical emitted tokens trial by trial (hence the same distribution)."""
+    from test_oracle_pins import mc_tree_inputs
+    V, N = 8, 20000
+    c, _ = mc_tree_inputs(N, V, 3, 2, 11)
+    r = O.verify_stochastic(**c)
+    B, n_max, dev = len(c["tree_off"]) - 1, c["n_max"], "cuda"
+    path = torch.zeros((B, n_max), dtype=torch.int32, device=dev)
+    alen = torch.zeros(B, dtype=torch.int32, device=dev)
+    emit = torch.zeros((B, n_max), dtype=torch.int32, device=dev)
+    nem = torch.zeros(B, dtype=torch.int32, device=dev)
+    st = torch.zeros(B, dtype=torch.int32, device=dev)
+    ws = torch.empty(S.spec_verify_workspace_size(B, n_max, V), dtype=torch.uint8, device=dev)
+
+    def d(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    S.spec_tree_verify_stochastic(d(c["p_logits"]), d(c["q_probs"]), d(c["tokens"]), d(c["parent"]),
+                                  d(c["tree_off"]), d(c["uniforms"].view(np.int32)), B, n_max, V, path, alen, emit,
+                                  nem, ws, st)
+    torch.cuda.synchronize()
+    assert np.array_equal(emit.cpu().numpy(), r["emitted"])
+    assert np.array_equal(alen.cpu().numpy(), r["accept_len"])
+
+
+# ------------------------------------------------------------- attention ----
+
+def _gpu_attention(w, flags=S.SPEC_ATTN_AUTO, max_prefix=None):
+    vp = _pass(w, max_prefix=max_prefix)
+    vp.mask_build()
+    vp.attention(flags)
+    torch.cuda.synchronize()
+    return out_as_f32(vp.out, w.dtype), vp.status.cpu().numpy()
+
+
+ATTN_CASES = [
+    dict(seed=1, B=3, n_range=(1, 40), prefix_range=(0, 300), Hq=8, Hkv=2, D=64, dtype=W.F32, block_size=16),
+    dict(seed=2, B=2, n_range=(1, 20), prefix_range=(100, 700), Hq=4, Hkv=4, D=128, dtype=W.F32, block_size=8),
+    dict(seed=3, B=3, n_range=(1, 70), prefix_range=(0, 900), Hq=8, Hkv=2, D=128, dtype=W.BF16, block_size=16),
+    dict(seed=4, B=2, n_range=(30, 130), prefix_range=(0, 1500), Hq=32, Hkv=8, D=128, dtype=W.BF16,
+         block_size=128),
+    dict(seed=5, B=4, n_range=(1, 9), prefix_range=(1, 520), Hq=16, Hkv=2, D=64, dtype=W.BF16, block_size=64),
+    dict(seed=6, B=1, n_range=(200, 200), prefix_range=(0, 0), Hq=8, Hkv=1, D=128, dtype=W.BF16, block_size=256),
+]
+
+
+@pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: f"s{c['seed']}_D{c['D']}_{'f32' if c['dtype'] == 0 else 'bf16'}")
+@pytest.mark.parametrize("flags", [S.SPEC_ATTN_AUTO, S.SPEC_ATTN_CUDA_CORE])
+def test_attention_parity_small(case, flags):
+    c = dict(case)
+    w = W.small_random(c.pop("seed"), V=16, **c)
+    ref, _, s_ref = oracle_attention(w)
+    got, st = _gpu_attention(w, flags)
+    assert np.array_equal(st[:w.B], s_ref)
+    ref32 = ref.astype(np.float32) if w.dtype == W.F32 else (ref.astype(np.uint32) << 16).view(np.float32)
+    ok = attn_tolerance_ok(got.reshape(ref32.shape), ref32, w.dtype)
+    assert ok.all(), float(np.abs(got.reshape(ref32.shape) - ref32).max())
+
+
+def test_attention_parity_workload0():
+    w = W.make_config(0)
+    ref, _, s_ref = oracle_attention(w)
+    got, st = _gpu_attention(w)
+    assert (st[:1] == 0).all()
+    assert np.abs(got.reshape(ref.shape) - ref).max() <= 1e-5
+
+
+def test_attention_capacity_and_bad_blocks():
+    w = W.small_random(9, B=3, n_range=(3, 9), prefix_range=(10, 60), Hq=4, Hkv=2, D=64, dtype=W.BF16, V=16,
+                       block_size=16)
+    w.prefix_len[0] = w.block_table.shape[1] * 16  # beyond the block table
+    w.block_table[1, 0] = w.num_blocks + 5         # bad block id
+    _, _, s_ref = oracle_attention(w)
+    got, st = _gpu_attention(w, max_prefix=int(w.prefix_len.max()))
+    assert st[0] & S.SPEC_DEV_CAPACITY and st[1] & S.SPEC_DEV_BAD_BLOCK and st[2] == 0
+    assert s_ref[0] & O.ST_CAPACITY and s_ref[1] & O.ST_BAD_BLOCK
+
+
+def _sampled_rows(w, k, seed):
+    g = np.random.default_rng(seed)
+    return np.sort(g.choice(w.T * w.Hq, size=min(k, w.T * w.Hq), replace=False)).astype(np.int64)
+
+
+@pytest.mark.parametrize("which", [1, 2, 3])
+def test_attention_parity_workloads_sampled(which):
+    """Full-size workloads (launch configuration of the benchmark) checked on
+    sampled (node, head) rows the oracle computes one by one."""
+    w = W.make_config(which)
+    rows = _sampled_rows(w, 96, which)
+    ref, _, s_ref = oracle_attention(w, rows=rows)
+    got, st = _gpu_attention(w)
+    assert (st[:w.B] == 0).all() and (s_ref == 0).all()
+    ref32 = (ref.astype(np.uint32) << 16).view(np.float32).reshape(-1, w.D)[rows]
+    g = got.reshape(-1, w.D)[rows]
+    assert attn_tolerance_ok(g, ref32, w.dtype).all(), float(np.abs(g - ref32).max())
+
+
+# ---------------------------------------------------------------- commit ----
+
+def _oracle_commit(w, ref_v):
+    st = np.zeros(w.B, np.int32)
+    return O.kv_commit(np_elems(w.k_cache, w.dtype), np_elems(w.v_cache, w.dtype), w.block_table.numpy(),
+                       w.block_size, w.prefix_len.numpy(), ref_v["path"], ref_v["accept_len"], w.Hkv, w.D, w.dtype,
+                       st)
+
+
+@pytest.mark.parametrize("dtype,D,bs", [(W.BF16, 128, 16), (W.F32, 64, 8), (W.BF16, 64, 256)])
+def test_commit_parity(dtype, D, bs):
+    w = W.small_random(51, B=5, n_range=(1, 70), prefix_range=(0, 200), Hq=4, Hkv=2, D=D, dtype=dtype, V=3,
+                       block_size=bs)
+    # tokens copy the argmax chain so paths are long
+    am = w.p_logits.argmax(1)
+    for b in range(w.B):
+        off = int(w.tree_off[b])
+        for u in range(1, int(w.tree_off[b + 1]) - off):
+            w.tokens[off + u] = am[off + int(w.parent[off + u])]
+    ref_v = oracle_greedy(w)
+    k_ref, v_ref, nl_ref, st_ref = _oracle_commit(w, ref_v)
+    vp = _pass(w)
+    vp.mask_build()
+    vp.verify("greedy")
+    vp.commit()
+    torch.cuda.synchronize()
+    assert np.array_equal(vp.accept_len.cpu().numpy(), ref_v["accept_len"])
+    assert (ref_v["accept_len"] > 2).any()
+    assert np.array_equal(np_elems(vp.batch.k_cache, dtype), k_ref)
+    assert np.array_equal(np_elems(vp.batch.v_cache, dtype), v_ref)
+    assert np.array_equal(vp.new_len.cpu().numpy(), nl_ref)
+    assert np.array_equal(vp.status.cpu().numpy(), st_ref)
+
+
+def test_commit_bad_paths_and_failed_requests():
+    w = W.small_random(52, B=3, n_range=(6, 6), prefix_range=(5, 5), Hq=2, Hkv=1, D=64, dtype=W.BF16, V=3,
+                       block_size=8)
+    d = DeviceBatch.from_workload(w)
+    path = torch.tensor([[0, 2, 1, -1, -1, -1], [0, 1, 3, -1, -1, -1], [0, 1, -1, -1, -1, -1]], dtype=torch.int32)
+    alen = torch.tensor([3, 3, 2], dtype=torch.int32)
+    status = torch.tensor([0, 0, S.SPEC_DEV_BAD_TOKEN], dtype=torch.int32)
+    k0, v0 = d.k_cache.clone(), d.v_cache.clone()
+    new_len = torch.zeros(3, dtype=torch.int32, device="cuda")
+    st = status.cuda()
+    S.spec_kv_commit(d.k_cache, d.v_cache, d.block_table, d.max_blocks, d.block_size, d.num_blocks, d.prefix_len,
+                     path.cuda(), 6, alen.cuda(), 3, 1, 64, new_len, st)
+    torch.cuda.synchronize()
+    k_ref, v_ref, nl_ref, st_ref = O.kv_commit(np_elems(w.k_cache, w.dtype), np_elems(w.v_cache, w.dtype),
+                                               w.block_table.numpy(), 8, w.prefix_len.numpy(), path.numpy(),
+                                               alen.numpy(), 1, 64, W.BF16, status.numpy())
+    assert st.cpu().tolist() == st_ref.tolist() == [S.SPEC_DEV_BAD_PATH, 0, S.SPEC_DEV_BAD_TOKEN]
+    assert new_len.cpu().tolist() == nl_ref.tolist()
+    assert np.array_equal(np_elems(d.k_cache, W.BF16), k_ref)
+    assert np.array_equal(np_elems(d.v_cache, W.BF16), v_ref)
+
+
+# ------------------------------------------------------------- full pass ----
+
+@pytest.mark.parametrize("mode", ["stochastic", "greedy"])
+def test_full_pass_workload1(mode):
+    """The benchmark's pass (workload 1) end to end: mask, attention, verify,
+    commit; verify and commit exact, attention on sampled rows."""
+    w = W.make_config(1)
+    ref_m = oracle_mask(w)
+    ref_v = oracle_greedy(w) if mode == "greedy" else oracle_stochastic(w)
+    rows = _sampled_rows(w, 64, 17)
+    ref_a, _, _ = oracle_attention(w, rows=rows)
+    k_ref, v_ref, nl_ref, st_ref = _oracle_commit(w, ref_v)
+    vp = _pass(w)
+    vp.run(mode)
+    torch.cuda.synchronize()
+    assert np.array_equal(vp.mask.cpu().numpy().view(np.uint64), ref_m[0])
+    for k in ("path", "accept_len", "emitted", "n_emitted"):
+        assert np.array_equal(getattr(vp, k).cpu().numpy(), ref_v[k]), k
+    got = out_as_f32(vp.out, w.dtype).reshape(-1, w.D)[rows]
+    ref32 = (ref_a.astype(np.uint32) << 16).view(np.float32).reshape(-1, w.D)[rows]
+    assert attn_tolerance_ok(got, ref32, w.dtype).all()
+    assert np.array_equal(np_elems(vp.batch.k_cache, w.dtype), k_ref)
+    assert np.array_equal(np_elems(vp.batch.v_cache, w.dtype), v_ref)
+    assert np.array_equal(vp.new_len.cpu().numpy(), nl_ref)

@@ -1,0 +1,149 @@
+"""ctypes binding of libspectree.so: one Python function per C-ABI entry point,
+with the same name.  Argument marshalling only (torch tensors -> device
+pointers, the current CUDA stream -> cudaStream_t); every step of the hot path
+runs in the library's kernels.  There is no CPU fallback: when the library
+cannot be loaded, every call raises."""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspectree.so")
+
+SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA, SPEC_ERR_WORKSPACE = 0, 1, 2, 3, 4
+SPEC_DEV_BAD_TREE, SPEC_DEV_BAD_TOKEN, SPEC_DEV_CAPACITY, SPEC_DEV_TIMEOUT = 1, 2, 4, 8
+SPEC_DEV_BAD_BLOCK, SPEC_DEV_BAD_PATH = 16, 32
+SPEC_F32, SPEC_BF16 = 0, 1
+SPEC_ATTN_AUTO, SPEC_ATTN_CUDA_CORE, SPEC_ATTN_TCGEN05 = 0, 1, 2
+
+# C signatures (argument ctypes, return ctype) of every exported entry point
+_P, _I, _U32, _U64, _SZ, _F = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_size_t,
+                               ctypes.c_float)
+SIGNATURES = {
+    "spec_version": ([], _I),
+    "spec_status_string": ([_I], ctypes.c_char_p),
+    "spec_tree_mask_build": ([_P, _P, _I, _I, _P, _P, _P, _P], _I),
+    "spec_attention_workspace_size": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
+    "spec_tree_attention": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _SZ,
+                             _P, _U32, _P], _I),
+    "spec_verify_workspace_size": ([_I, _I, _I], _SZ),
+    "spec_tree_verify_greedy": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
+    "spec_tree_verify_stochastic": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
+    "spec_kv_commit": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "spec_philox_uniforms": ([_U64, _U32, _P, _I, _I, _P, _P], _I),
+}
+
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} returned {code} ({status_string(code)})")
+
+
+def lib():
+    """Load libspectree.so (raises when it is missing: no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "tree_speculative_verification_spec_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def status_string(code):
+    return lib().spec_status_string(int(code)).decode()
+
+
+def version():
+    return lib().spec_version()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor arguments must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, code):
+    if code != SPEC_OK:
+        raise SpecError(fn, code)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def spec_tree_mask_build(parent, tree_off, B, n_max, mask, depth, status, stream=None):
+    _check("spec_tree_mask_build", lib().spec_tree_mask_build(
+        _ptr(parent), _ptr(tree_off), B, n_max, _ptr(mask), _ptr(depth), _ptr(status), _stream(stream)))
+
+
+def spec_attention_workspace_size(B, T, n_max, max_prefix, Hq, Hkv, D):
+    return int(lib().spec_attention_workspace_size(B, T, n_max, max_prefix, Hq, Hkv, D))
+
+
+def spec_tree_attention(q, k_cache, v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len, tree_off,
+                        mask, B, T, n_max, max_prefix, Hq, Hkv, D, scale, out, workspace, status,
+                        flags=SPEC_ATTN_AUTO, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("spec_tree_attention", lib().spec_tree_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_blocks, block_size, num_blocks,
+        _ptr(prefix_len), _ptr(tree_off), _ptr(mask), B, T, n_max, max_prefix, Hq, Hkv, D, _dtype_code(q),
+        float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), flags, _stream(stream)))
+
+
+def spec_verify_workspace_size(B, n_max, V):
+    return int(lib().spec_verify_workspace_size(B, n_max, V))
+
+
+def spec_tree_verify_greedy(p_logits, tokens, parent, tree_off, mask, depth, B, n_max, V, path, accept_len,
+                            emitted, n_emitted, workspace, status, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("spec_tree_verify_greedy", lib().spec_tree_verify_greedy(
+        _ptr(p_logits), _ptr(tokens), _ptr(parent), _ptr(tree_off), _ptr(mask), _ptr(depth), B, n_max, V,
+        _ptr(path), _ptr(accept_len), _ptr(emitted), _ptr(n_emitted), _ptr(workspace), ws_bytes, _ptr(status),
+        _stream(stream)))
+
+
+def spec_tree_verify_stochastic(p_logits, q_probs, tokens, parent, tree_off, uniforms, B, n_max, V, path,
+                                accept_len, emitted, n_emitted, workspace, status, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("spec_tree_verify_stochastic", lib().spec_tree_verify_stochastic(
+        _ptr(p_logits), _ptr(q_probs), _ptr(tokens), _ptr(parent), _ptr(tree_off), _ptr(uniforms), B, n_max, V,
+        _ptr(path), _ptr(accept_len), _ptr(emitted), _ptr(n_emitted), _ptr(workspace), ws_bytes, _ptr(status),
+        _stream(stream)))
+
+
+def spec_kv_commit(k_cache, v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len, path, path_stride,
+                   accept_len, B, Hkv, D, new_len, status, stream=None):
+    _check("spec_kv_commit", lib().spec_kv_commit(
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_blocks, block_size, num_blocks, _ptr(prefix_len),
+        _ptr(path), path_stride, _ptr(accept_len), B, Hkv, D, _dtype_code(k_cache), _ptr(new_len), _ptr(status),
+        _stream(stream)))
+
+
+def spec_philox_uniforms(seed, round_, tree_off, B, n_max, out, stream=None):
+    _check("spec_philox_uniforms", lib().spec_philox_uniforms(
+        ctypes.c_uint64(seed), ctypes.c_uint32(round_), _ptr(tree_off), B, n_max, _ptr(out), _stream(stream)))
