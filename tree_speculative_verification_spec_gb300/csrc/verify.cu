@@ -373,6 +373,9 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
           cluster_sync_all<C>();  // D is read across the cluster by the next test
         }
       }
+      // A CTA may read a peer's shared memory (D[tok]) right before the loop
+      // ends: no CTA of the cluster leaves before every such read is done.
+      cluster_sync_all<C>();
       if (bad_tok) {
         if (rank == 0 && threadIdx.x == 0) atomicOr(&a.status[b], SPEC_DEV_BAD_TOKEN);
       } else if (accepted >= 0) {
