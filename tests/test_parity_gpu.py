@@ -246,8 +246,10 @@ ATTN_CASES = [
 
 
 @pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: f"s{c['seed']}_D{c['D']}_{'f32' if c['dtype'] == 0 else 'bf16'}")
-@pytest.mark.parametrize("flags", [S.SPEC_ATTN_AUTO, S.SPEC_ATTN_CUDA_CORE])
+@pytest.mark.parametrize("flags", [S.SPEC_ATTN_AUTO, S.SPEC_ATTN_CUDA_CORE, S.SPEC_ATTN_TCGEN05])
 def test_attention_parity_small(case, flags):
+    if flags == S.SPEC_ATTN_TCGEN05 and case["dtype"] != W.BF16:
+        pytest.skip("the tensor-core path takes bf16")
     c = dict(case)
     w = W.small_random(c.pop("seed"), V=16, **c)
     ref, _, s_ref = oracle_attention(w)
@@ -256,6 +258,32 @@ def test_attention_parity_small(case, flags):
     ref32 = ref.astype(np.float32) if w.dtype == W.F32 else (ref.astype(np.uint32) << 16).view(np.float32)
     ok = attn_tolerance_ok(got.reshape(ref32.shape), ref32, w.dtype)
     assert ok.all(), float(np.abs(got.reshape(ref32.shape) - ref32).max())
+
+
+TC_CASES = [  # (B, n_range, prefix_range, Hq, Hkv, D, block_size)
+    (2, (1, 40), (0, 0), 8, 2, 128, 8),
+    (3, (20, 64), (100, 600), 32, 8, 128, 16),
+    (2, (1, 33), (120, 129), 16, 4, 128, 32),
+    (2, (60, 200), (0, 400), 8, 1, 128, 64),
+    (1, (30, 40), (3000, 5000), 32, 8, 128, 256),  # long prefix: several key splits
+    (2, (5, 90), (200, 700), 16, 4, 64, 16),
+    (1, (128, 128), (127, 127), 4, 1, 64, 512),
+    (4, (1, 3), (1, 2000), 32, 8, 128, 128),        # few rows: padded 128-row tile
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: f"B{c[0]}_D{c[5]}_bs{c[6]}_P{c[2][1]}")
+def test_attention_tcgen05_layouts(case):
+    B, nr, pr, Hq, Hkv, D, bs = case
+    w = W.small_random(sum(nr) + pr[1] + bs, B=B, n_range=nr, prefix_range=pr, Hq=Hq, Hkv=Hkv, D=D, dtype=W.BF16,
+                       V=16, block_size=bs)
+    ref, _, s_ref = oracle_attention(w)
+    got, st = _gpu_attention(w, S.SPEC_ATTN_TCGEN05)
+    assert (st[:w.B] == 0).all() and (s_ref == 0).all()
+    ref32 = (ref.astype(np.uint32) << 16).view(np.float32)
+    g = got.reshape(ref32.shape)
+    bad = ~attn_tolerance_ok(g, ref32, w.dtype)
+    assert not bad.any(), (int(bad.sum()), float(np.abs(g - ref32).max()), np.argwhere(bad)[:5].tolist())
 
 
 def test_attention_parity_workload0():

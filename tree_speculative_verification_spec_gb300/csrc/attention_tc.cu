@@ -1,17 +1,587 @@
-// Tree attention on the tcgen05 tensor cores (bf16 inputs, fp32 accumulation in TMEM).
+// Tree attention on the 5th-generation tensor cores (tcgen05), bf16 inputs,
+// fp32 accumulation in tensor memory.
+//
+// "SpecInfer Guide", "Generalizing Attention to Tree Topologies" and "The
+// Topology-Aware 2D Causal Mask": the rows of one CTA are 128 (tree node,
+// query head) pairs of one kv-head group, so the K/V stream of the group is
+// shared by all its query heads (GQA) and all its tree nodes.  Per 128-key
+// tile j of the CTA's key range:
+//   S_j = Q K_j^T            tcgen05.mma, A = Q (smem), B = K tile (smem), D in TMEM
+//   P_j = exp2(S_j*c - m)    softmax warps: TMEM -> registers -> bf16 P (smem);
+//                            the ancestor bitmask is applied only on tiles that
+//                            reach past the prefix
+//   O  += P_j V_j            tcgen05.mma, A = P (smem), B = V tile (smem, MN-major)
+// K and V tiles arrive by TMA (2-D tensor maps over the paged cache, one box
+// per page or per 128 rows), 128-byte swizzled, into two-stage rings.  S is
+// double-buffered in TMEM so S_{j+1} runs on the tensor core while the
+// softmax warps work on S_j.  O is rescaled only when a row maximum grows by
+// more than 2^8 (the stale maximum is exact for the final normalisation);
+// the rescale happens while the P buffer is anyway waiting for PV_{j-1}.
+//
+// Warp roles (256 threads): warp 0 issues TMA, warp 1 issues MMAs and owns
+// the TMEM allocation, warps 4-7 run softmax and the epilogue (thread r <->
+// accumulator row r <-> TMEM lane r).  Every mbarrier wait is bounded: on
+// expiry the CTA records SPEC_DEV_TIMEOUT, drains its own copies and MMAs,
+// frees TMEM and returns.
+#include <cuda.h>
+
 #include "attention.cuh"
 
 namespace spectree {
 
-bool attention_tc_enabled(int D) {
-  (void)D;
+namespace tc {
+
+constexpr int BM = 128;       // rows per CTA (M of the MMA)
+constexpr int BN = 128;       // keys per tile
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kWaitLimit = 1u << 25;  // bounded mbarrier polls
+constexpr float kRescaleLog2 = 8.0f;        // rescale O when the row max grows by > 2^8
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false when the limit expired or another role gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
   return false;
 }
 
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), sm_100
+// family descriptor version 1.  Addresses and offsets in bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A K-major,
+// B K-major (b_mn = 0) or MN-major (b_mn = 1), M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n, uint32_t b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn << 16) | ((n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& ra, float& rb) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  ra = __low2float(h);
+  rb = __high2float(h);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int D>
+struct Layout {
+  static constexpr int DH = D / 64;                 // 128-byte halves of a row
+  static constexpr uint32_t kQ = BM * D * 2;        // Q tile bytes
+  static constexpr uint32_t kKV = BN * D * 2;       // one K (or V) stage
+  static constexpr uint32_t kP = BM * BN * 2;       // P tile
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kQ;
+  static constexpr uint32_t kOffV = kQ + 2 * kKV;
+  static constexpr uint32_t kOffP = kQ + 4 * kKV;
+  static constexpr uint32_t kBytes = kOffP + kP;
+  // one CTA per SM: TMEM is allocated whole (512 columns)
+  static constexpr uint32_t kDyn = (kBytes + 1024 < 120 * 1024 ? 120 * 1024 : kBytes + 1024);
+};
+
+struct TcParams {
+  AttnArgs a;
+  int box_rows;      // rows per TMA box: min(block_size, 128)
+  long long rows_total;  // num_blocks * Hkv * block_size (rows of the 2-D cache view)
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                   const TcParams prm) {
+  using L_ = Layout<D>;
+  const AttnArgs& a = prm.a;
+  extern __shared__ uint8_t dyn_raw[];
+  __shared__ uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full, pv_done, drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag, bad_block;
+
+  const int mt = blockIdx.x, split = blockIdx.y;
+  const int b = blockIdx.z / a.Hkv, kvh = blockIdx.z % a.Hkv;
+  const int off = a.tree_off[b];
+  const int n = a.tree_off[b + 1] - off;
+  const int P = a.prefix_len[b];
+  const int g = a.g;
+  const int R = n * g;
+  if (n <= 0 || n > a.n_max || mt * BM >= R || off < 0 || off + n > a.T) return;
+  if (*(volatile int32_t*)&a.status[b] != 0) return;
+  if (P < 0 || P > a.max_prefix || (long long)P + n > (long long)a.max_blocks * a.block_size) {
+    if (threadIdx.x == 0 && mt == 0 && split == 0 && kvh == 0) atomicOr(&a.status[b], SPEC_DEV_CAPACITY);
+    return;
+  }
+  const int Lk = P + n;
+  const int k_begin = split * a.chunk;
+  const int k_end = min(Lk, k_begin + a.chunk);
+  if (k_begin >= k_end) return;
+  const int ntiles = (k_end - k_begin + BN - 1) / BN;
+
+  // 1024-byte aligned dynamic shared memory (128-byte swizzle atoms)
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(&p_full, 128);
+    mbar_init(&pv_done, 1);
+    mbar_init(&drain, 1);
+    abort_flag = 0;
+    bad_block = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+
+  // Q tile: row r = (node r / g, head kvh*g + r % g); rows past the group are zero.
+  {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+    constexpr int CPR = D / 8;  // 16-byte chunks per row
+    for (int c = threadIdx.x; c < BM * CPR; c += kThreads) {
+      const int r = c / CPR, ch = c % CPR;
+      const int row = mt * BM + r;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (row < R) {
+        const int t = off + row / g, hh = kvh * g + row % g;
+        v = *reinterpret_cast<const uint4*>(q + ((size_t)t * a.Hq + hh) * D + ch * 8);
+      }
+      const int h = ch >> 3, cc = ch & 7;
+      *reinterpret_cast<uint4*>(smem + L_::kOffQ + h * (BM * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 256;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+      const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
+      const int bs = a.block_size, br = prm.box_rows;
+      const int nbox = BN / br;
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int st = j & 1;
+        const int k0 = k_begin + j * BN;
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          uint64_t* full = kv == 0 ? &k_full[st] : &v_full[st];
+          uint64_t* empty = kv == 0 ? &k_empty[st] : &v_empty[st];
+          if (j >= 2 && !mbar_wait(empty, ((j >> 1) - 1) & 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full, L_::kKV);
+          const CUtensorMap* map = kv == 0 ? &tmap_k : &tmap_v;
+          const uint32_t dst0 = sbase + (kv == 0 ? L_::kOffK : L_::kOffV) + st * L_::kKV;
+          for (int i = 0; i < nbox; ++i) {
+            const int k = k0 + i * br;
+            int y = (int)min(prm.rows_total, (long long)INT32_MAX);  // out of range: zero fill
+            if (k < Lk) {
+              const int blk = bt[k / bs];
+              if (blk >= 0 && blk < a.num_blocks) y = (int)(((long long)blk * a.Hkv + kvh) * bs + (k % bs));
+              else bad_block = 1;
+            }
+#pragma unroll
+            for (int h = 0; h < L_::DH; ++h) tma_load_2d(dst0 + h * (BN * 128) + i * br * 128, map, h * 64, y, full);
+          }
+        }
+        if (ok) issued = j + 1;
+      }
+      // drain: every issued load has landed before the CTA can exit
+      for (int j = max(0, issued - 2); j < issued; ++j) {
+        mbar_wait(&k_full[j & 1], (j >> 1) & 1, &abort_flag);
+        mbar_wait(&v_full[j & 1], (j >> 1) & 1, &abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(BN, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16(D, 1);
+      const uint32_t qaddr = sbase + L_::kOffQ, paddr = sbase + L_::kOffP;
+      bool ok = true;
+      auto issue_pv = [&](int i) -> bool {
+        if (!mbar_wait(&p_full, i & 1, &abort_flag)) return false;
+        if (!mbar_wait(&v_full[i & 1], (i >> 1) & 1, &abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t vaddr = sbase + L_::kOffV + (i & 1) * L_::kKV;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(paddr + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(vaddr + kk * 2048, BN * 128, 1024);
+          umma_bf16(tO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&pv_done);
+        umma_commit(&v_empty[i & 1]);
+        return true;
+      };
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(&k_full[st], (j >> 1) & 1, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (j >= 2 && !mbar_wait(&s_free[st], ((j >> 1) - 1) & 1, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kaddr = sbase + L_::kOffK + st * L_::kKV;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          const uint32_t ob = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+          umma_bf16(tS + st * BN, smem_desc_sw128(qaddr + o, 16, 1024), smem_desc_sw128(kaddr + ob, 16, 1024),
+                    idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[st]);
+        umma_commit(&k_empty[st]);
+        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+      }
+      if (ok) issue_pv(ntiles - 1);
+      // drain: every issued MMA has completed before TMEM is freed
+      umma_commit(&drain);
+      mbar_wait(&drain, 0, &abort_flag);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int r = threadIdx.x - 128;  // accumulator row == TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
+    const int row = mt * BM + r;
+    const bool valid = row < R;
+    const int t = valid ? off + row / g : off;
+    const uint64_t* mrow = a.mask + (size_t)t * a.W;
+    float m_used = -INFINITY, lsum = 0.0f;
+    bool ok = true;
+    // tcgen05.ld / st are warp-collective: every decision before one is warp-uniform
+    auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool w = mbar_wait(bar, parity, &abort_flag);
+      return __all_sync(0xffffffffu, w);
+    };
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int st = j & 1;
+      const int k0 = k_begin + j * BN;
+      if (!wait_warp(&s_full[st], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + st * BN + c * 32 + lane_off, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[st]);
+
+      // visibility: prefix keys, then the node's ancestor bits on the tree tail
+      float factor = 1.0f;
+      bool rescale = false;
+      if (valid) {
+        const bool plain = (k0 + BN <= k_end) && (k0 + BN <= P);
+        float mt_ = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t vis = 0xffffffffu;
+          if (!plain) {
+            vis = 0;
+            for (int e = 0; e < 32; ++e) {
+              const int k = k0 + c * 32 + e;
+              bool vk = k < k_end;
+              if (vk && k >= P) vk = (mrow[(k - P) >> 6] >> ((k - P) & 63)) & 1ull;
+              vis |= (uint32_t)vk << e;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = ((vis >> e) & 1u) ? s[c * 32 + e] * a.scale_log2 : -INFINITY;
+            s[c * 32 + e] = x;
+            mt_ = fmaxf(mt_, x);
+          }
+        }
+        if (mt_ > m_used + kRescaleLog2) {
+          rescale = j > 0;
+          factor = fast_exp2(m_used - mt_);  // 0 when m_used = -inf
+          lsum *= factor;
+          m_used = mt_;
+        }
+      }
+      // P row (bf16), its sum accumulated from the rounded values the MMA sees
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int e = 0; e < BN; e += 2) {
+        float p0 = 0.0f, p1 = 0.0f;
+        if (valid) {
+          p0 = s[e] == -INFINITY ? 0.0f : fast_exp2(s[e] - m_used);
+          p1 = s[e + 1] == -INFINITY ? 0.0f : fast_exp2(s[e + 1] - m_used);
+        }
+        float r0, r1;
+        pk[e >> 1] = pack_bf16(p0, p1, r0, r1);
+        lsum += r0 + r1;
+      }
+      if (j >= 1) {
+        if (!wait_warp(&pv_done, (j - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? factor : 1.0f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tO + c * 32 + lane_off, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
+            tmem_st32(tO + c * 32 + lane_off, v);
+          }
+          tmem_wait_st();
+        }
+      }
+      // a tile reaching past the key range: zero its V rows there (no stale
+      // values, possibly non-finite, may meet a zero probability)
+      if (k0 + BN > k_end) {
+        if (!wait_warp(&v_full[st], (j >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int zr = k_end - k0;
+        uint8_t* vst = smem + L_::kOffV + st * L_::kKV;
+        for (int idx = r; idx < (BN - zr) * L_::DH * 8; idx += 128) {
+          const int rr = zr + idx / (L_::DH * 8), rest = idx % (L_::DH * 8);
+          *reinterpret_cast<uint4*>(vst + (rest >> 3) * (BN * 128) + rr * 128 + ((rest & 7) << 4)) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      uint8_t* prow = smem + L_::kOffP + r * 128;
+#pragma unroll
+      for (int c = 0; c < BN / 8; ++c) {
+        const int h = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(prow + h * (BM * 128) + ((cc ^ (r & 7)) << 4)) =
+            make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+    }
+    // epilogue: O row from TMEM
+    if (ok && wait_warp(&pv_done, (ntiles - 1) & 1)) {
+      tc_fence_after();
+      const size_t orow = (size_t)t * a.Hq + kvh * g + (valid ? row % g : 0);
+      const float inv = 1.0f / lsum;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + c * 32 + lane_off, v);
+        tmem_wait_ld();
+        if (!valid) continue;
+        if (a.splits == 1) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + orow * D + c * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            float d0, d1;
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv, d0, d1);
+            w.y = pack_bf16(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv, d0, d1);
+            w.z = pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv, d0, d1);
+            w.w = pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv, d0, d1);
+            *reinterpret_cast<uint4*>(out + e) = w;
+          }
+        } else {
+          float* wo = a.ws_o + ((size_t)split * a.T * a.Hq + orow) * D + c * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(wo + e) = make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                                             __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+        }
+      }
+      if (valid && a.splits > 1) {
+        float* wml = a.ws_ml + ((size_t)split * a.T * a.Hq + orow) * 2;
+        wml[0] = m_used;
+        wml[1] = lsum;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (bad_block) atomicOr(&a.status[b], SPEC_DEV_BAD_BLOCK);
+    if (abort_flag) atomicOr(&a.status[b], SPEC_DEV_TIMEOUT);
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool attention_tc_enabled(int D) { return D == 64 || D == 128; }
+
+static bool make_cache_map(CUtensorMap* m, const void* base, long long rows, int D, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+static cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t stream) {
+  tc::TcParams prm;
+  prm.a = a;
+  prm.box_rows = a.block_size < tc::BN ? a.block_size : tc::BN;
+  prm.rows_total = (long long)a.num_blocks * a.Hkv * a.block_size;
+  if (prm.rows_total >= (long long)INT32_MAX) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap mk, mv;
+  if (!make_cache_map(&mk, a.k_cache, prm.rows_total, D, prm.box_rows) ||
+      !make_cache_map(&mv, a.v_cache, prm.rows_total, D, prm.box_rows))
+    return cudaErrorInvalidValue;
+  auto kern = tc::attn_tc_kernel<D>;
+  const int dyn = (int)tc::Layout<D>::kDyn;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+  if (e != cudaSuccess) return e;
+  const int rows_max = a.n_max * a.g;
+  dim3 grid((rows_max + tc::BM - 1) / tc::BM, a.splits, a.B * a.Hkv);
+  kern<<<grid, tc::kThreads, dyn, stream>>>(mk, mv, prm);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream) {
-  (void)a;
-  (void)stream;
-  return cudaErrorNotSupported;
+  if (a.D == 64) return launch_tc_d<64>(a, stream);
+  if (a.D == 128) return launch_tc_d<128>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace spectree
