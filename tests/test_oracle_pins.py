@@ -655,3 +655,25 @@ def test_stochastic_children_tried_in_increasing_index(oracle):
     logits[0] = [0.0, -30.0, 0.0, 0.0, 0.0]
     r = oracle.verify_stochastic(logits, qp, tokens, parent, [0, 7], uni, 7)
     assert r["path"][0, :3].tolist() == [0, 4, 5]
+
+
+def test_stochastic_zero_sum_residual_keeps_the_target(oracle):
+    """Reading of the residual step when max(r - q, 0) sums to zero (q >= r
+    everywhere: impossible for two normalised distributions except through
+    rounding): the target stays r, so the walk samples from p itself."""
+    V = 6
+    logits = np.log(np.array([0.3, 0.25, 0.2, 0.1, 0.1, 0.05])).astype(np.float32)
+    r0, _, _ = oracle.residual(logits, np.zeros(V, np.float32), 0)
+    q = (r0 * np.float32(1.001)).astype(np.float32)
+    parent = np.array([-1, 0, 0], np.int32)
+    tokens = np.array([0, 1, 2], np.int32)
+    rows = np.stack([logits] * 3)
+    qp = np.stack([q] * 3)
+    # both children rejected (largest acceptance word), then the sample
+    cdf = np.cumsum(r0.astype(np.float64))
+    for frac in [0.0, 0.1, 0.29, 0.31, 0.5, 0.6, 0.74, 0.8, 0.9, 0.96, 0.999]:
+        U = int(frac * 2 ** 32)
+        uni = np.array([[0, U], [0xffffffff, 0], [0xffffffff, 0]], np.uint32)
+        r = oracle.verify_stochastic(rows, qp, tokens, parent, [0, 3], uni, 3)
+        expect = int(np.searchsorted(cdf, U / 2 ** 32, side="right"))
+        assert r["accept_len"][0] == 1 and r["emitted"][0, 0] == expect, frac

@@ -141,6 +141,21 @@ def test_verify_parity_many_siblings_and_duplicates(mode):
     _assert_verify_equal(got, ref, B)
 
 
+def test_verify_zero_sum_residual_fallback():
+    """q >= r everywhere at some nodes: the first rejection leaves a zero-sum
+    residual and the state must stay r (then a sample from p)."""
+    w = W.small_random(44, B=6, n_range=(2, 40), prefix_range=(0, 1), Hq=2, Hkv=1, D=64, V=33000, block_size=16)
+    g = np.random.default_rng(5)
+    for t in range(w.T):
+        if g.random() < 0.5:
+            r0, _, _ = O.residual(w.p_logits[t].numpy(), np.zeros(w.V, np.float32), 0)
+            w.q_probs[t] = torch.from_numpy((r0 * np.float32(1.001)).astype(np.float32))
+    w.uniforms[:, 0] = -1  # every acceptance word at its maximum: many rejections
+    ref = oracle_stochastic(w)
+    got = _gpu_verify(w, "stochastic")
+    _assert_verify_equal(got, ref, w.B)
+
+
 @pytest.mark.parametrize("mode", ["greedy", "stochastic"])
 def test_verify_bad_inputs(mode):
     w = W.small_random(41, B=4, n_range=(3, 8), prefix_range=(0, 1), Hq=2, Hkv=1, D=64, V=50, block_size=16)

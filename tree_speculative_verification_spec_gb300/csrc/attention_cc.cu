@@ -242,8 +242,11 @@ cudaError_t launch_attention_combine(const AttnArgs& a, spec_dtype dt, cudaStrea
   return cudaGetLastError();
 }
 
-// Split plan: enough (request, kv-head, row tile, split) units for about two
-// waves of 152 SMs, key chunks of at least 512 keys, multiples of 128.
+// Split plan.  The tensor-core kernel holds a whole SM per CTA (all of TMEM),
+// so the plan minimises waves x per-CTA time: a wave of the 152 SMs costs a
+// fixed ~4 us (set-up, first loads, epilogue) plus ~1.3 us per 128-key tile.
+// The CUDA-core kernel (several CTAs per SM) targets about two waves of CTAs.
+// Key chunks are multiples of 128 keys.
 AttnPlan attention_plan(int B, int n_max, int max_prefix, int Hq, int Hkv, int D, bool bf16, unsigned flags) {
   (void)D;
   AttnPlan p;
@@ -256,9 +259,24 @@ AttnPlan attention_plan(int B, int n_max, int max_prefix, int Hq, int Hkv, int D
   p.row_tile = p.use_tc ? 128 : kCcRows;
   const long long units = (long long)B * Hkv * ((rows_max + p.row_tile - 1) / p.row_tile);
   const long long max_len = (long long)max_prefix + n_max;
-  const long long target = 2 * 152;
-  long long splits = units > 0 ? (target + units - 1) / units : 1;
-  splits = std::max(1LL, std::min(splits, (max_len + 511) / 512));
+  long long splits = 1;
+  if (p.use_tc) {
+    double best = 1e300;
+    const long long smax = std::max(1LL, std::min(64LL, (max_len + 127) / 128));
+    for (long long sp = 1; sp <= smax; ++sp) {
+      const long long chunk = ((max_len + sp - 1) / sp + 127) / 128 * 128;
+      const long long waves = (units * sp + 151) / 152;
+      const double cost = (double)waves * (4.0 + 1.3 * (double)(chunk / 128));
+      if (cost < best * 0.97) {  // prefer fewer splits (less partial traffic) on near-ties
+        best = cost;
+        splits = sp;
+      }
+    }
+  } else {
+    const long long target = 2 * 152;
+    splits = units > 0 ? (target + units - 1) / units : 1;
+    splits = std::max(1LL, std::min(splits, (max_len + 511) / 512));
+  }
   long long chunk = (max_len + splits - 1) / splits;
   chunk = (chunk + 127) / 128 * 128;
   if (chunk < 128) chunk = 128;

@@ -18,9 +18,12 @@
 // more than 2^8 (the stale maximum is exact for the final normalisation);
 // the rescale happens while the P buffer is anyway waiting for PV_{j-1}.
 //
-// Warp roles (256 threads): warp 0 issues TMA, warp 1 issues MMAs and owns
-// the TMEM allocation, warps 4-7 run softmax and the epilogue (thread r <->
-// accumulator row r <-> TMEM lane r).  Every mbarrier wait is bounded: on
+// Warp roles (384 threads): warp 0 issues TMA from the start, warp 1 issues
+// MMAs and owns the TMEM allocation, warps 2-11 stage the Q tile, warps 4-11
+// run softmax and the epilogue: two threads per accumulator row (row r ==
+// TMEM lane r, the warp's lane quadrant), each owning one 64-column half of
+// S, P and O; their row maxima meet through shared memory and a 64-thread
+// mbarrier per lane quadrant.  Every mbarrier wait is bounded: on
 // expiry the CTA records SPEC_DEV_TIMEOUT, drains its own copies and MMAs,
 // frees TMEM and returns.
 #include <cuda.h>
@@ -33,7 +36,8 @@ namespace tc {
 
 constexpr int BM = 128;       // rows per CTA (M of the MMA)
 constexpr int BN = 128;       // keys per tile
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;        // warp 0 TMA, warp 1 MMA, warps 2-11 Q load, warps 4-11 softmax
+constexpr int kSoftmaxThreads = 256;  // two threads per accumulator row
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 25;  // bounded mbarrier polls
 constexpr float kRescaleLog2 = 8.0f;        // rescale O when the row max grows by > 2^8
@@ -172,11 +176,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                    const TcParams prm) {
   using L_ = Layout<D>;
+  constexpr int HC = BN / 2;        // score columns per softmax thread
+  constexpr int OC = D / 2;         // output columns per softmax thread
   const AttnArgs& a = prm.a;
   extern __shared__ uint8_t dyn_raw[];
-  __shared__ uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full, pv_done, drain;
+  __shared__ uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full, pv_done, q_full,
+      drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag, bad_block;
+  __shared__ float xchg[2][2][BM];  // [tile parity][column half][row]: partial row maxima
+  __shared__ float lfin[2][BM];     // final partial row sums
+  __shared__ uint64_t xbar[2][4], lbar[4];  // pair exchanges per lane quadrant (bounded waits)
 
   const int mt = blockIdx.x, split = blockIdx.y;
   const int b = blockIdx.z / a.Hkv, kvh = blockIdx.z % a.Hkv;
@@ -209,11 +219,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
+      mbar_init(&s_free[i], kSoftmaxThreads);
     }
-    mbar_init(&p_full, 128);
+    mbar_init(&p_full, kSoftmaxThreads);
     mbar_init(&pv_done, 1);
+    mbar_init(&q_full, kThreads - 64);
     mbar_init(&drain, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&xbar[0][i], 64);
+      mbar_init(&xbar[1][i], 64);
+      mbar_init(&lbar[i], 64);
+    }
     abort_flag = 0;
     bad_block = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -224,24 +240,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-
-  // Q tile: row r = (node r / g, head kvh*g + r % g); rows past the group are zero.
-  {
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-    constexpr int CPR = D / 8;  // 16-byte chunks per row
-    for (int c = threadIdx.x; c < BM * CPR; c += kThreads) {
-      const int r = c / CPR, ch = c % CPR;
-      const int row = mt * BM + r;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (row < R) {
-        const int t = off + row / g, hh = kvh * g + row % g;
-        v = *reinterpret_cast<const uint4*>(q + ((size_t)t * a.Hq + hh) * D + ch * 8);
-      }
-      const int h = ch >> 3, cc = ch & 7;
-      *reinterpret_cast<uint4*>(smem + L_::kOffQ + h * (BM * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
-    }
-  }
-  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -273,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dst0 = sbase + (kv == 0 ? L_::kOffK : L_::kOffV) + st * L_::kKV;
           for (int i = 0; i < nbox; ++i) {
             const int k = k0 + i * br;
-            int y = (int)min(prm.rows_total, (long long)INT32_MAX);  // out of range: zero fill
+            int y = (int)prm.rows_total;  // out of range: zero fill
             if (k < Lk) {
               const int blk = bt[k / bs];
               if (blk >= 0 && blk < a.num_blocks) y = (int)(((long long)blk * a.Hkv + kvh) * bs + (k % bs));
@@ -297,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16(BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(D, 1);
       const uint32_t qaddr = sbase + L_::kOffQ, paddr = sbase + L_::kOffP;
-      bool ok = true;
+      bool ok = mbar_wait(&q_full, 0, &abort_flag);
       auto issue_pv = [&](int i) -> bool {
         if (!mbar_wait(&p_full, i & 1, &abort_flag)) return false;
         if (!mbar_wait(&v_full[i & 1], (i >> 1) & 1, &abort_flag)) return false;
@@ -341,167 +339,216 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&drain);
       mbar_wait(&drain, 0, &abort_flag);
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int r = threadIdx.x - 128;  // accumulator row == TMEM lane
-    const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
-    const int row = mt * BM + r;
-    const bool valid = row < R;
-    const int t = valid ? off + row / g : off;
-    const uint64_t* mrow = a.mask + (size_t)t * a.W;
-    float m_used = -INFINITY, lsum = 0.0f;
-    bool ok = true;
-    // tcgen05.ld / st are warp-collective: every decision before one is warp-uniform
-    auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
-      const bool w = mbar_wait(bar, parity, &abort_flag);
-      return __all_sync(0xffffffffu, w);
-    };
-    for (int j = 0; j < ntiles && ok; ++j) {
-      const int st = j & 1;
-      const int k0 = k_begin + j * BN;
-      if (!wait_warp(&s_full[st], (j >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[BN];
+  } else {
+    // ------------------------------------------------ Q tile (warps 2..11)
+    // row r = (node r / g, head kvh*g + r % g); rows past the group are zero
+    {
+      const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+      constexpr int CPR = D / 8;  // 16-byte chunks per row
+      constexpr int NT = kThreads - 64;
+      constexpr int NQ = (BM * CPR + NT - 1) / NT;  // chunks per thread: all loads first
+      uint4 v[NQ];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + st * BN + c * 32 + lane_off, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
-      }
-      tc_fence_before();
-      mbar_arrive(&s_free[st]);
-
-      // visibility: prefix keys, then the node's ancestor bits on the tree tail
-      float factor = 1.0f;
-      bool rescale = false;
-      if (valid) {
-        const bool plain = (k0 + BN <= k_end) && (k0 + BN <= P);
-        float mt_ = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t vis = 0xffffffffu;
-          if (!plain) {
-            vis = 0;
-            for (int e = 0; e < 32; ++e) {
-              const int k = k0 + c * 32 + e;
-              bool vk = k < k_end;
-              if (vk && k >= P) vk = (mrow[(k - P) >> 6] >> ((k - P) & 63)) & 1ull;
-              vis |= (uint32_t)vk << e;
-            }
-          }
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float x = ((vis >> e) & 1u) ? s[c * 32 + e] * a.scale_log2 : -INFINITY;
-            s[c * 32 + e] = x;
-            mt_ = fmaxf(mt_, x);
-          }
-        }
-        if (mt_ > m_used + kRescaleLog2) {
-          rescale = j > 0;
-          factor = fast_exp2(m_used - mt_);  // 0 when m_used = -inf
-          lsum *= factor;
-          m_used = mt_;
+      for (int i = 0; i < NQ; ++i) {
+        const int c = threadIdx.x - 64 + i * NT;
+        const int r = c / CPR, ch = c % CPR;
+        const int row = mt * BM + r;
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (c < BM * CPR && row < R) {
+          const int t = off + row / g, hh = kvh * g + row % g;
+          v[i] = *reinterpret_cast<const uint4*>(q + ((size_t)t * a.Hq + hh) * D + ch * 8);
         }
       }
-      // P row (bf16), its sum accumulated from the rounded values the MMA sees
-      uint32_t pk[BN / 2];
 #pragma unroll
-      for (int e = 0; e < BN; e += 2) {
-        float p0 = 0.0f, p1 = 0.0f;
-        if (valid) {
-          p0 = s[e] == -INFINITY ? 0.0f : fast_exp2(s[e] - m_used);
-          p1 = s[e + 1] == -INFINITY ? 0.0f : fast_exp2(s[e + 1] - m_used);
-        }
-        float r0, r1;
-        pk[e >> 1] = pack_bf16(p0, p1, r0, r1);
-        lsum += r0 + r1;
+      for (int i = 0; i < NQ; ++i) {
+        const int c = threadIdx.x - 64 + i * NT;
+        if (c >= BM * CPR) break;
+        const int r = c / CPR, ch = c % CPR;
+        const int h = ch >> 3, cc = ch & 7;
+        *reinterpret_cast<uint4*>(smem + L_::kOffQ + h * (BM * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v[i];
       }
-      if (j >= 1) {
-        if (!wait_warp(&pv_done, (j - 1) & 1)) {
+      fence_async_smem();
+      mbar_arrive(&q_full);
+    }
+    if (warp >= 4) {
+      // -------------------------------------------------- softmax + epilogue
+      // two threads per accumulator row: column half `half` of S, P and O
+      const int quad = warp & 3, half = (warp - 4) >> 2;
+      const int r = quad * 32 + lane;  // accumulator row == TMEM lane
+      const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+      const int row = mt * BM + r;
+      const bool valid = row < R;
+      const int t = valid ? off + row / g : off;
+      const uint64_t* mrow = a.mask + (size_t)t * a.W;
+      const float c2 = a.scale_log2;
+      float m_used = -INFINITY, lpart[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      bool ok = true;
+      // tcgen05.ld / st are warp-collective: every decision before one is warp-uniform
+      auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const bool w = mbar_wait(bar, parity, &abort_flag);
+        return __all_sync(0xffffffffu, w);
+      };
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int st = j & 1;
+        const int k0 = k_begin + j * BN;
+        const int c0 = k0 + half * HC;  // first key of this thread's columns
+        if (!wait_warp(&s_full[st], (j >> 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float f = rescale ? factor : 1.0f;
+        float x[HC];
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tO + c * 32 + lane_off, v);
-            tmem_wait_ld();
+        for (int c = 0; c < HC / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tS + st * BN + half * HC + c * 32 + lane_off, v);
+          tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
-            tmem_st32(tO + c * 32 + lane_off, v);
-          }
-          tmem_wait_st();
+          for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]) * c2;
         }
-      }
-      // a tile reaching past the key range: zero its V rows there (no stale
-      // values, possibly non-finite, may meet a zero probability)
-      if (k0 + BN > k_end) {
-        if (!wait_warp(&v_full[st], (j >> 1) & 1)) {
+        tc_fence_before();
+        mbar_arrive(&s_free[st]);
+
+        // visibility: the tile reaches past the prefix (tree tail) or the range end
+        const bool plain = (c0 + HC <= k_end) && (c0 + HC <= P);
+        if (!plain) {
+#pragma unroll
+          for (int c = 0; c < HC / 32; ++c) {
+            uint32_t vis = 0;
+            for (int e = 0; e < 32; ++e) {
+              const int k = c0 + c * 32 + e;
+              bool vk = k < k_end;
+              if (vk && k >= P) vk = (mrow[(k - P) >> 6] >> ((k - P) & 63)) & 1ull;
+              vis |= (uint32_t)vk << e;
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (!((vis >> e) & 1u)) x[c * 32 + e] = -INFINITY;
+          }
+        }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < HC; ++e) mx[e & 3] = fmaxf(mx[e & 3], x[e]);
+        float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        // combine with the partner thread (same row, other column half)
+        xchg[j & 1][half][r] = mloc;
+        mbar_arrive(&xbar[j & 1][quad]);
+        if (!wait_warp(&xbar[j & 1][quad], (j >> 1) & 1)) {
           ok = false;
           break;
         }
-        const int zr = k_end - k0;
-        uint8_t* vst = smem + L_::kOffV + st * L_::kKV;
-        for (int idx = r; idx < (BN - zr) * L_::DH * 8; idx += 128) {
-          const int rr = zr + idx / (L_::DH * 8), rest = idx % (L_::DH * 8);
-          *reinterpret_cast<uint4*>(vst + (rest >> 3) * (BN * 128) + rr * 128 + ((rest & 7) << 4)) =
-              make_uint4(0, 0, 0, 0);
+        const float mtile = valid ? fmaxf(mloc, xchg[j & 1][half ^ 1][r]) : -INFINITY;
+
+        float factor = 1.0f;
+        bool rescale = false;
+        if (mtile > m_used + kRescaleLog2) {
+          rescale = j > 0;
+          factor = fast_exp2(m_used - mtile);  // 0 when m_used = -inf
+#pragma unroll
+          for (int i = 0; i < 4; ++i) lpart[i] *= factor;
+          m_used = mtile;
         }
-      }
-      uint8_t* prow = smem + L_::kOffP + r * 128;
+        // P (bf16) for this thread's 64 columns; sums from the fp32 values
+        uint32_t pk[HC / 2];
+        const float mneg = -m_used;
 #pragma unroll
-      for (int c = 0; c < BN / 8; ++c) {
-        const int h = c >> 3, cc = c & 7;
-        *reinterpret_cast<uint4*>(prow + h * (BM * 128) + ((cc ^ (r & 7)) << 4)) =
-            make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
-      }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_full);
-    }
-    // epilogue: O row from TMEM
-    if (ok && wait_warp(&pv_done, (ntiles - 1) & 1)) {
-      tc_fence_after();
-      const size_t orow = (size_t)t * a.Hq + kvh * g + (valid ? row % g : 0);
-      const float inv = 1.0f / lsum;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + c * 32 + lane_off, v);
-        tmem_wait_ld();
-        if (!valid) continue;
-        if (a.splits == 1) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + orow * D + c * 32;
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            float d0, d1;
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv, d0, d1);
-            w.y = pack_bf16(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv, d0, d1);
-            w.z = pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv, d0, d1);
-            w.w = pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv, d0, d1);
-            *reinterpret_cast<uint4*>(out + e) = w;
+        for (int e = 0; e < HC; e += 2) {
+          float p0 = 0.0f, p1 = 0.0f;
+          if (valid && m_used != -INFINITY) {
+            p0 = fast_exp2(x[e] + mneg);  // -inf gives 0
+            p1 = fast_exp2(x[e + 1] + mneg);
           }
-        } else {
-          float* wo = a.ws_o + ((size_t)split * a.T * a.Hq + orow) * D + c * 32;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(wo + e) = make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                                             __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+          lpart[(e >> 1) & 3] += p0 + p1;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h2);
         }
+        if (j >= 1) {
+          if (!wait_warp(&pv_done, (j - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, rescale)) {
+            const float f = rescale ? factor : 1.0f;
+#pragma unroll
+            for (int c = 0; c < OC / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tO + half * OC + c * 32 + lane_off, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
+              tmem_st32(tO + half * OC + c * 32 + lane_off, v);
+            }
+            tmem_wait_st();
+          }
+        }
+        // a tile reaching past the key range: zero its V rows there (no stale
+        // values, possibly non-finite, may meet a zero probability)
+        if (k0 + BN > k_end) {
+          if (!wait_warp(&v_full[st], (j >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const int zr = k_end - k0;
+          uint8_t* vst = smem + L_::kOffV + st * L_::kKV;
+          const int sidx = threadIdx.x - 128;
+          for (int idx = sidx; idx < (BN - zr) * L_::DH * 8; idx += kSoftmaxThreads) {
+            const int rr = zr + idx / (L_::DH * 8), rest = idx % (L_::DH * 8);
+            *reinterpret_cast<uint4*>(vst + (rest >> 3) * (BN * 128) + rr * 128 + ((rest & 7) << 4)) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        // P half `half` holds keys [64*half, 64*half + 64): 8 swizzled 16-byte chunks
+        uint8_t* prow = smem + L_::kOffP + half * (BM * 128) + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
+              make_uint4(pk[cc * 4], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full);
       }
-      if (valid && a.splits > 1) {
-        float* wml = a.ws_ml + ((size_t)split * a.T * a.Hq + orow) * 2;
-        wml[0] = m_used;
-        wml[1] = lsum;
+      // epilogue: this thread's half of the O row
+      lfin[half][r] = (lpart[0] + lpart[1]) + (lpart[2] + lpart[3]);
+      mbar_arrive(&lbar[quad]);
+      ok = ok && wait_warp(&lbar[quad], 0);
+      const float lsum = lfin[0][r] + lfin[1][r];
+      if (ok && wait_warp(&pv_done, (ntiles - 1) & 1)) {
+        tc_fence_after();
+        const size_t orow = (size_t)t * a.Hq + kvh * g + (valid ? row % g : 0);
+        const float inv = 1.0f / lsum;
+#pragma unroll
+        for (int c = 0; c < OC / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + half * OC + c * 32 + lane_off, v);
+          tmem_wait_ld();
+          if (!valid) continue;
+          const int col = half * OC + c * 32;
+          if (a.splits == 1) {
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + orow * D + col;
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              float d0, d1;
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv, d0, d1);
+              w.y = pack_bf16(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv, d0, d1);
+              w.z = pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv, d0, d1);
+              w.w = pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv, d0, d1);
+              *reinterpret_cast<uint4*>(out + e) = w;
+            }
+          } else {
+            float* wo = a.ws_o + ((size_t)split * a.T * a.Hq + orow) * D + col;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(wo + e) = make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                                               __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+          }
+        }
+        if (valid && a.splits > 1 && half == 0) {
+          float* wml = a.ws_ml + ((size_t)split * a.T * a.Hq + orow) * 2;
+          wml[0] = m_used;
+          wml[1] = lsum;
+        }
       }
     }
   }

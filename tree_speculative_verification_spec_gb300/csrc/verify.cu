@@ -21,9 +21,8 @@ namespace cg = cooperative_groups;
 
 namespace spectree {
 
-constexpr int kVerifyThreads = 512;
-constexpr int kSlice = 16384;  // vocabulary entries per CTA
-// clusters of up to 8 CTAs: 8 * kSlice >= SPEC_MAX_VOCAB
+constexpr int kVerifyThreads = 256;
+constexpr int kSlice = 8192;  // vocabulary entries per CTA (wider slices above 8 * kSlice)
 
 // ---------------------------------------------------------------------------
 // fp32 arithmetic contract of the stochastic verifier.  Every operation is a
@@ -38,22 +37,36 @@ constexpr int kSlice = 16384;  // vocabulary entries per CTA
 // rounded fp32 values, written as exact hex literals.  x < -87 gives 0.
 __device__ __forceinline__ float canon_exp(float x) {
   if (!(x >= -87.0f)) return 0.0f;
-  const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));  // log2(e)
-  float r = fmaf(-n, 0x1.62e4p-1f, x);                   // ln2, high 16 bits
-  r = fmaf(-n, 0x1.7f7d1cp-20f, r);                      // ln2 - high part
-  float p = 0x1.a01a02p-13f;                             // 1/7!
-  p = fmaf(p, r, 0x1.6c16c2p-10f);                       // 1/6!
-  p = fmaf(p, r, 0x1.111112p-7f);                        // 1/5!
-  p = fmaf(p, r, 0x1.555556p-5f);                        // 1/4!
-  p = fmaf(p, r, 0x1.555556p-3f);                        // 1/3!
+  const float t = __fmul_rn(x, 0x1.715476p+0f);  // x * log2(e)
+  // rint(t) without a conversion unit op: adding 1.5 * 2^23 leaves the integer
+  // (rounded to nearest, ties to even) in the low mantissa bits; |t| < 2^22.
+  const float big = __fadd_rn(t, 12582912.0f);
+  const float n = __fsub_rn(big, 12582912.0f);
+  const int ni = __float_as_int(big) - 0x4B400000;
+  float r = fmaf(-n, 0x1.62e4p-1f, x);    // ln2, high 16 bits
+  r = fmaf(-n, 0x1.7f7d1cp-20f, r);       // ln2 - high part
+  float p = 0x1.a01a02p-13f;              // 1/7!
+  p = fmaf(p, r, 0x1.6c16c2p-10f);        // 1/6!
+  p = fmaf(p, r, 0x1.111112p-7f);         // 1/5!
+  p = fmaf(p, r, 0x1.555556p-5f);         // 1/4!
+  p = fmaf(p, r, 0x1.555556p-3f);         // 1/3!
   p = fmaf(p, r, 0.5f);
   p = fmaf(p, r, 1.0f);
   p = fmaf(p, r, 1.0f);
-  return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+  return __fmul_rn(p, __int_as_float((ni + 127) << 23));
 }
 
 // Fixed-point weight trunc(v * 2^46) and the normaliser of a sum of them.
-__device__ __forceinline__ unsigned long long fx(float v) { return __float2ull_rz(__fmul_rn(v, 0x1p46f)); }
+// trunc(v * 2^46) for 0 <= v < 2 from the bit fields (no conversion unit op):
+// v = m * 2^(e - 150) with the 24-bit significand m, so v * 2^46 = m * 2^(e - 104).
+__device__ __forceinline__ unsigned long long fx(float v) {
+  const uint32_t bits = __float_as_uint(v);
+  const int e = (int)((bits >> 23) & 0xFFu);
+  const unsigned long long m = (unsigned long long)((bits & 0x7FFFFFu) | 0x800000u);
+  const int sh = e - 104;
+  if (e == 0) return 0ull;  // zero or subnormal: below 2^-126 * 2^46
+  return sh >= 0 ? (m << sh) : (sh > -24 ? (m >> (-sh)) : 0ull);
+}
 __device__ __forceinline__ float z_of(unsigned long long S) { return __fmul_rn(__ull2float_rn(S), 0x1p-46f); }
 
 // floor(U * S / 2^32), exact for U < 2^32, S < 2^64.
@@ -225,7 +238,7 @@ __device__ int collect_children(const int32_t* par, int n, int u, int* kids, int
   __syncthreads();
   for (int base = u + 1; base < n; base += blockDim.x) {
     const int c = base + threadIdx.x;
-    const bool is = c < n && par[c] == u;
+    const bool is = c < n && __ldg(par + c) == u;
     const unsigned m = __ballot_sync(0xffffffffu, is);
     if (lane == 0) s_wofs[w] = __popc(m);
     __syncthreads();
@@ -245,17 +258,36 @@ __device__ int collect_children(const int32_t* par, int n, int u, int* kids, int
   return *s_cnt;
 }
 
+// Bulk copy of one row slice (global -> this CTA's shared memory) completing
+// on an mbarrier, and a bounded wait for it.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool bulk_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 26); ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
 template <int MODE, int C>
-__global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a) {
   extern __shared__ float4 dyn_smem[];
   float* D = reinterpret_cast<float*>(dyn_smem);  // stochastic: the node's weights slice
   __shared__ Red red;
   __shared__ XSlot xs;
-  __shared__ int32_t s_par[SPEC_MAX_NODES];
   __shared__ int32_t s_kids[SPEC_MAX_NODES];
   __shared__ int s_cnt, s_last, s_flag;
   __shared__ int s_wofs[kVerifyThreads / 32];
   __shared__ uint64_t s_match[SPEC_MAX_WORDS];
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ float s_z[SPEC_MAX_NODES];  // normalisers of the residual steps applied so far
 
   const int rank = (int)(blockIdx.x % C);
   const int u = (int)(blockIdx.x / C);
@@ -273,6 +305,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
   const int V = a.V;
   const int x0 = rank * a.slice;
   const int x1 = min(V, x0 + a.slice);
+  const int len = max(0, x1 - x0);
   const int t = off + u;
 
   if (work && rank == 0 && threadIdx.x == 0) {
@@ -282,18 +315,28 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
   if (work) {
     const float* prow = a.p_logits + (size_t)t * V;
     if constexpr (MODE == 0) {
-      // ---- greedy: argmax of row u, ties to the lowest token id ----
+      // ---- greedy: argmax of row u, ties to the lowest token id; four
+      // independent 16-byte loads in flight per thread ----
       float bv = -INFINITY;
       int bi = 0x7fffffff;
       if ((V & 3) == 0) {
         const float4* p4 = reinterpret_cast<const float4*>(prow);
-        for (int j = (x0 >> 2) + threadIdx.x; j < (x1 >> 2); j += blockDim.x) {
-          const float4 v = __ldcs(p4 + j);
-          const int x = j << 2;
-          if (v.x > bv) { bv = v.x; bi = x; }
-          if (v.y > bv) { bv = v.y; bi = x + 1; }
-          if (v.z > bv) { bv = v.z; bi = x + 2; }
-          if (v.w > bv) { bv = v.w; bi = x + 3; }
+        const int j0 = x0 >> 2, j1 = x1 >> 2;
+        for (int j = j0 + threadIdx.x; j < j1; j += 4 * kVerifyThreads) {
+          float4 v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int jj = j + q * kVerifyThreads;
+            v[q] = jj < j1 ? __ldcs(p4 + jj) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int x = (j + q * kVerifyThreads) << 2;
+            if (v[q].x > bv) { bv = v[q].x; bi = x; }
+            if (v[q].y > bv) { bv = v[q].y; bi = x + 1; }
+            if (v[q].z > bv) { bv = v[q].z; bi = x + 2; }
+            if (v[q].w > bv) { bv = v[q].w; bi = x + 3; }
+          }
         }
       } else {
         for (int x = x0 + threadIdx.x; x < x1; x += blockDim.x) {
@@ -306,40 +349,59 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
     } else {
       // ---- stochastic: row state of node u ----
       const float* qrow = a.q_probs + (size_t)t * V;
-      const int len = x1 - x0;
-      float lmax = -INFINITY;
+      const int lenp = (len + 3) & ~3;  // padded to whole float4 (pad = -inf: weight 0)
       if ((V & 3) == 0) {
-        const float4* p4 = reinterpret_cast<const float4*>(prow + x0);
-        float4* D4 = reinterpret_cast<float4*>(D);
-        for (int j = threadIdx.x; j < (len >> 2); j += blockDim.x) {
-          const float4 v = __ldcs(p4 + j);
-          D4[j] = v;
-          lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+        // one bulk copy of the slice into shared memory
+        if (threadIdx.x == 0) {
+          asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&s_bar)) : "memory");
+          asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&s_bar)),
+                       "r"((uint32_t)(len * 4))
+                       : "memory");
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                  smem_addr(D)),
+              "l"(prow + x0), "r"((uint32_t)(len * 4)), "r"(smem_addr(&s_bar))
+              : "memory");
+        }
+        __syncthreads();
+        if (!bulk_wait(&s_bar, 0)) {
+          if (threadIdx.x == 0) atomicOr(&a.status[b], SPEC_DEV_TIMEOUT);
+          bulk_wait(&s_bar, 0);  // drain before the buffer is touched
         }
       } else {
-        for (int j = threadIdx.x; j < len; j += blockDim.x) {
-          const float v = __ldcs(prow + x0 + j);
-          D[j] = v;
-          lmax = fmaxf(lmax, v);
-        }
+        for (int j = threadIdx.x; j < len; j += blockDim.x) D[j] = __ldcs(prow + x0 + j);
+      }
+      for (int j = len + threadIdx.x; j < lenp; j += blockDim.x) D[j] = -INFINITY;
+      __syncthreads();
+      float4* D4 = reinterpret_cast<float4*>(D);
+      float lmax = -INFINITY;
+      for (int j = threadIdx.x; j < (lenp >> 2); j += blockDim.x) {
+        const float4 v = D4[j];
+        lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
       }
       const float m = cluster_max<C>(lmax, red, &xs);
       unsigned long long ls = 0;
-      for (int j = threadIdx.x; j < len; j += blockDim.x) {
-        const float e = canon_exp(__fsub_rn(D[j], m));
-        D[j] = e;
-        ls += fx(e);
+      for (int j = threadIdx.x; j < (lenp >> 2); j += blockDim.x) {
+        float4 v = D4[j];
+        v.x = canon_exp(__fsub_rn(v.x, m));
+        v.y = canon_exp(__fsub_rn(v.y, m));
+        v.z = canon_exp(__fsub_rn(v.z, m));
+        v.w = canon_exp(__fsub_rn(v.w, m));
+        D4[j] = v;
+        ls += fx(v.x) + fx(v.y) + fx(v.z) + fx(v.w);
       }
       unsigned long long S = cluster_sum<C>(ls, red, &xs);
       float Z = z_of(S);
 
       // children of u in increasing index
-      for (int i = threadIdx.x; i < n; i += blockDim.x) s_par[i] = a.parent[off + i];
-      __syncthreads();
-      const int k = collect_children(s_par, n, u, s_kids, &s_cnt, s_wofs);
+      const int k = collect_children(a.parent + off, n, u, s_kids, &s_cnt, s_wofs);
 
       int accepted = -1;
       bool bad_tok = false;
+      bool frozen = false;      // a zero-sum residual froze the state (see below)
+      int nsteps = 0;           // residual steps applied to D
+      unsigned long long lt = ls;  // this CTA's share of S
       for (int i = 0; i < k; ++i) {
         const int c = s_kids[i];
         const int tok = a.tokens[off + c];
@@ -362,14 +424,52 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
           accepted = c;
           break;
         }
-        // rejection: next residual d = max(r - q, 0), r = d / Z_new
+        if (frozen) continue;  // the next residual would be the same all-zero one
+        // rejection: d <- max(d / Z - q, 0) in place, S <- sum FX(d)
+        s_z[nsteps] = Z;
+        cluster_sync_all<C>();  // every CTA has read D[tok] before it changes
         unsigned long long ln = 0;
-        for (int j = threadIdx.x; j < len; j += blockDim.x) ln += fx(resid(D[j], Z, __ldg(qrow + x0 + j)));
-        const unsigned long long Sn = cluster_sum<C>(ln, red, &xs);
+        if ((V & 3) == 0) {
+          const float4* q4 = reinterpret_cast<const float4*>(qrow + x0);
+          for (int j = threadIdx.x; j < (len >> 2); j += blockDim.x) {
+            float4 d = D4[j];
+            const float4 qq = __ldg(q4 + j);
+            d.x = resid(d.x, Z, qq.x);
+            d.y = resid(d.y, Z, qq.y);
+            d.z = resid(d.z, Z, qq.z);
+            d.w = resid(d.w, Z, qq.w);
+            D4[j] = d;
+            ln += fx(d.x) + fx(d.y) + fx(d.z) + fx(d.w);
+          }
+        } else {
+          for (int j = threadIdx.x; j < len; j += blockDim.x) {
+            const float dn = resid(D[j], Z, __ldg(qrow + x0 + j));
+            D[j] = dn;
+            ln += fx(dn);
+          }
+        }
+        const unsigned long long Sn = cluster_sum<C>(ln, red, &xs);  // also publishes D
         if (Sn != 0) {
-          for (int j = threadIdx.x; j < len; j += blockDim.x) D[j] = resid(D[j], Z, __ldg(qrow + x0 + j));
           S = Sn;
           Z = z_of(Sn);
+          lt = ln;
+          ++nsteps;
+        } else {
+          // S_j == 0 (impossible in exact arithmetic after a rejection): the
+          // state stays that of step j-1, and so does every later residual.
+          // Rebuild step j-1 from the logits: e, then the nsteps earlier steps.
+          frozen = true;
+          ls = 0;
+          for (int j = threadIdx.x; j < len; j += blockDim.x) D[j] = canon_exp(__fsub_rn(__ldg(prow + x0 + j), m));
+          for (int j = len + threadIdx.x; j < lenp; j += blockDim.x) D[j] = 0.0f;
+          for (int st2 = 0; st2 < nsteps; ++st2) {
+            __syncthreads();
+            const float Zs = s_z[st2];
+            for (int j = threadIdx.x; j < len; j += blockDim.x) D[j] = resid(D[j], Zs, __ldg(qrow + x0 + j));
+          }
+          __syncthreads();
+          for (int j = threadIdx.x; j < len; j += blockDim.x) ls += fx(D[j]);
+          lt = ls;                // this thread's share of S, which is unchanged
           cluster_sync_all<C>();  // D is read across the cluster by the next test
         }
       }
@@ -383,9 +483,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
       } else {
         // terminal sample: smallest x whose fixed-point prefix sum exceeds target
         const unsigned long long target = sample_target(a.uniforms[t].y, S);
-        // this CTA's slice total and the exclusive prefix of the slices before it
-        unsigned long long lt = 0;
-        for (int j = threadIdx.x; j < len; j += blockDim.x) lt += fx(D[j]);
+        // this CTA's slice total (kept from the last pass) and the exclusive
+        // prefix of the slices before it
         lt = block_sum_u64(lt, red);
         unsigned long long before = 0;
         if constexpr (C > 1) {
@@ -415,7 +514,6 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
               acc += red.u[ww];
             }
             s_flag = ww;
-            red.f[0] = 0.0f;
             red.u[0] = acc;  // prefix before warp ww (slot reused after the read above)
           }
           __syncthreads();
@@ -435,7 +533,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
               }
               const unsigned hit = __ballot_sync(0xffffffffu, j < d1 && run + v > tl);
               if (hit) {
-                if (lane == __ffs(hit) - 1) a.ws_s[(size_t)b * a.n_max + u] = x0 + j;
+                if (lane == __ffs(hit) - 1) {
+                  a.ws_s[(size_t)b * a.n_max + u] = x0 + j;
+                  __threadfence();
+                }
                 break;
               }
               run += __shfl_sync(0xffffffffu, v, 31);
@@ -448,9 +549,9 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) verify_kernel(VerifyArgs a)
   }
 
   // ---- ticket: the last CTA of the request runs phase B ----
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();
     const int prev = atomicAdd(&a.ws_ticket[b], 1);
     s_last = prev == n_cta * C - 1;
   }
@@ -556,7 +657,7 @@ inline size_t ws_layout(int B, int n_max, size_t* off_s, size_t* off_t) {
 template <int MODE, int C>
 cudaError_t launch_verify(const VerifyArgs& a, int B, cudaStream_t stream) {
   auto kern = verify_kernel<MODE, C>;
-  const size_t dyn = MODE == 1 ? (size_t)a.slice * sizeof(float) : 0;
+  const size_t dyn = MODE == 1 ? (size_t)((a.slice + 3) & ~3) * sizeof(float) : 0;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -584,16 +685,17 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
   a.ws_s = reinterpret_cast<int32_t*>(ws + off_s);
   a.ws_ticket = reinterpret_cast<int32_t*>(ws + off_t);
   a.W = (a.n_max + 63) / 64;
-  const int C = (a.V + kSlice - 1) / kSlice;
-  // slice: ceil(V / C) rounded up to a multiple of 4 (16-byte aligned slices)
+  // cluster size: slices of kSlice entries, at most 8 CTAs (wider slices beyond)
+  int C = (a.V + kSlice - 1) / kSlice;
+  C = C <= 1 ? 1 : C <= 2 ? 2 : C <= 4 ? 4 : 8;
   a.slice = (((a.V + C - 1) / C) + 3) & ~3;
   if (cudaMemsetAsync(a.ws_ticket, 0, (size_t)B * sizeof(int32_t), stream) != cudaSuccess) return SPEC_ERR_CUDA;
   cudaError_t e;
   switch (C) {
     case 1: e = launch_verify<MODE, 1>(a, B, stream); break;
     case 2: e = launch_verify<MODE, 2>(a, B, stream); break;
-    case 3: case 4: a.slice = (((a.V + 3) / 4) + 3) & ~3; e = launch_verify<MODE, 4>(a, B, stream); break;
-    default: a.slice = (((a.V + 7) / 8) + 3) & ~3; e = launch_verify<MODE, 8>(a, B, stream); break;
+    case 4: e = launch_verify<MODE, 4>(a, B, stream); break;
+    default: e = launch_verify<MODE, 8>(a, B, stream); break;
   }
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
