@@ -154,47 +154,65 @@ __device__ __forceinline__ void cluster_sync_all() {
   else cg::this_cluster().sync();
 }
 
+// Cluster reductions with one cluster barrier each: every CTA publishes its
+// block result in exchange slot `par`, the barrier makes it visible, every CTA
+// reads all C slots.  Slots alternate, so a slot is rewritten only after a
+// later barrier, which no CTA passes before finishing its reads of it.  A
+// final barrier before exit keeps peers' shared memory alive for late reads.
 template <int C>
-__device__ __forceinline__ float cluster_max(float v, Red& red, XSlot* xs) {
+__device__ __forceinline__ float cluster_max(float v, Red& red, XSlot* xs, int& par) {
   v = block_max(v, red);
   if constexpr (C == 1) return v;
   cg::cluster_group cl = cg::this_cluster();
-  if (threadIdx.x == 0) xs->f = v;
+  if (threadIdx.x == 0) xs[par].f = v;
   cl.sync();
   float m = v;
-  for (int r = 0; r < C; ++r) m = fmaxf(m, cl.map_shared_rank(xs, r)->f);
-  cl.sync();
+  for (int r = 0; r < C; ++r) m = fmaxf(m, cl.map_shared_rank(xs + par, r)->f);
+  par ^= 1;
   return m;
 }
 
 template <int C>
-__device__ __forceinline__ unsigned long long cluster_sum(unsigned long long v, Red& red, XSlot* xs) {
+__device__ __forceinline__ unsigned long long cluster_sum(unsigned long long v, Red& red, XSlot* xs, int& par) {
   v = block_sum_u64(v, red);
   if constexpr (C == 1) return v;
   cg::cluster_group cl = cg::this_cluster();
-  if (threadIdx.x == 0) xs->u = v;
+  if (threadIdx.x == 0) xs[par].u = v;
   cl.sync();
   unsigned long long s = 0;
-  for (int r = 0; r < C; ++r) s += cl.map_shared_rank(xs, r)->u;
+  for (int r = 0; r < C; ++r) s += cl.map_shared_rank(xs + par, r)->u;
+  par ^= 1;
+  return s;
+}
+
+// sum over the CTAs of lower rank (exclusive prefix)
+template <int C>
+__device__ __forceinline__ unsigned long long cluster_prefix(unsigned long long v, XSlot* xs, int& par, int rank) {
+  if constexpr (C == 1) return 0ull;
+  cg::cluster_group cl = cg::this_cluster();
+  if (threadIdx.x == 0) xs[par].u = v;
   cl.sync();
+  unsigned long long s = 0;
+  for (int r = 0; r < rank; ++r) s += cl.map_shared_rank(xs + par, r)->u;
+  par ^= 1;
   return s;
 }
 
 template <int C>
-__device__ __forceinline__ void cluster_argmax(float& v, int& i, Red& red, XSlot* xs) {
+__device__ __forceinline__ void cluster_argmax(float& v, int& i, Red& red, XSlot* xs, int& par) {
   block_argmax(v, i, red);
   if constexpr (C == 1) return;
   cg::cluster_group cl = cg::this_cluster();
   if (threadIdx.x == 0) {
-    xs->f = v;
-    xs->i = i;
+    xs[par].f = v;
+    xs[par].i = i;
   }
   cl.sync();
   for (int r = 0; r < C; ++r) {
-    const XSlot* p = cl.map_shared_rank(xs, r);
+    const XSlot* p = cl.map_shared_rank(xs + par, r);
     argmax_combine(v, i, p->f, p->i);
   }
-  cl.sync();
+  par ^= 1;
 }
 
 struct VerifyArgs {
@@ -281,7 +299,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
   extern __shared__ float4 dyn_smem[];
   float* D = reinterpret_cast<float*>(dyn_smem);  // stochastic: the node's weights slice
   __shared__ Red red;
-  __shared__ XSlot xs;
+  __shared__ XSlot xs[2];
   __shared__ int32_t s_kids[SPEC_MAX_NODES];
   __shared__ int s_cnt, s_last, s_flag;
   __shared__ int s_wofs[kVerifyThreads / 32];
@@ -289,9 +307,12 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
   __shared__ __align__(8) uint64_t s_bar;
   __shared__ float s_z[SPEC_MAX_NODES];  // normalisers of the residual steps applied so far
 
+  // grid: x = (request, cluster rank), y = node; nodes near the root (most
+  // children, most residual passes) are dispatched first
   const int rank = (int)(blockIdx.x % C);
-  const int u = (int)(blockIdx.x / C);
-  const int b = blockIdx.y;
+  const int b = (int)(blockIdx.x / C);
+  const int u = blockIdx.y;
+  int par = 0;  // exchange-slot parity of the cluster reductions
   const int off = a.tree_off[b];
   const int n = a.tree_off[b + 1] - off;
   const bool n_ok = n >= 1 && n <= a.n_max;
@@ -344,7 +365,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
           if (v > bv) { bv = v; bi = x; }
         }
       }
-      cluster_argmax<C>(bv, bi, red, &xs);
+      cluster_argmax<C>(bv, bi, red, xs, par);
+      cluster_sync_all<C>();  // peers read this CTA's slot
       if (rank == 0 && threadIdx.x == 0) a.ws_a[(size_t)b * a.n_max + u] = bi == 0x7fffffff ? 0 : bi;
     } else {
       // ---- stochastic: row state of node u ----
@@ -380,7 +402,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
         const float4 v = D4[j];
         lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
       }
-      const float m = cluster_max<C>(lmax, red, &xs);
+      const float m = cluster_max<C>(lmax, red, xs, par);
       unsigned long long ls = 0;
       for (int j = threadIdx.x; j < (lenp >> 2); j += blockDim.x) {
         float4 v = D4[j];
@@ -391,7 +413,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
         D4[j] = v;
         ls += fx(v.x) + fx(v.y) + fx(v.z) + fx(v.w);
       }
-      unsigned long long S = cluster_sum<C>(ls, red, &xs);
+      unsigned long long S = cluster_sum<C>(ls, red, xs, par);
       float Z = z_of(S);
 
       // children of u in increasing index
@@ -448,7 +470,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
             ln += fx(dn);
           }
         }
-        const unsigned long long Sn = cluster_sum<C>(ln, red, &xs);  // also publishes D
+        const unsigned long long Sn = cluster_sum<C>(ln, red, xs, par);  // also publishes D
         if (Sn != 0) {
           S = Sn;
           Z = z_of(Sn);
@@ -486,14 +508,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
         // this CTA's slice total (kept from the last pass) and the exclusive
         // prefix of the slices before it
         lt = block_sum_u64(lt, red);
-        unsigned long long before = 0;
-        if constexpr (C > 1) {
-          cg::cluster_group cl = cg::this_cluster();
-          if (threadIdx.x == 0) xs.u = lt;
-          cl.sync();
-          for (int r = 0; r < rank; ++r) before += cl.map_shared_rank(&xs, r)->u;
-          cl.sync();
-        }
+        const unsigned long long before = cluster_prefix<C>(lt, xs, par, rank);
+        cluster_sync_all<C>();  // peers read this CTA's slot
         if (target >= before && target - before < lt) {
           // the token lies in this slice: per-warp contiguous chunks
           const unsigned long long tl = target - before;
@@ -661,7 +677,7 @@ cudaError_t launch_verify(const VerifyArgs& a, int B, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.n_max * C), (unsigned)B, 1);
+  cfg.gridDim = dim3((unsigned)(B * C), (unsigned)a.n_max, 1);
   cfg.blockDim = dim3(kVerifyThreads, 1, 1);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
@@ -715,7 +731,7 @@ size_t spec_verify_workspace_size(int B, int n_max, int V) {
 
 static spec_status verify_check(int B, int n_max, int V) {
   if (B < 0 || n_max < 0 || V <= 0) return SPEC_ERR_INVALID_ARG;
-  if (n_max > SPEC_MAX_NODES || V > SPEC_MAX_VOCAB || B > 65535) return SPEC_ERR_UNSUPPORTED;
+  if (n_max > SPEC_MAX_NODES || V > SPEC_MAX_VOCAB || B > (1 << 27)) return SPEC_ERR_UNSUPPORTED;
   return SPEC_OK;
 }
 
