@@ -186,6 +186,29 @@ spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_pr
                                         void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
+ * spec_tree_verify_stochastic without a workspace argument (the pages have no
+ * counterpart of this call).  For callers that cannot allocate device memory
+ * at the point where they verify: a host framework that hands the library only
+ * its inputs and outputs, or a latency-critical loop that must not pay the
+ * device-wide synchronisation of cudaMalloc.  Its scratch is a fixed file-scope
+ * device array of about 2.1 MB that every GPU loading the library keeps until
+ * the process exits.
+ *   Limits: B <= 16384 and B * n_max <= 262144; larger batches return
+ *   SPEC_ERR_UNSUPPORTED and launch nothing.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current): make that first call before any stream capture.
+ *   Every call uses the same array, and the call clears what must start at
+ *   zero: calls that overlap on the GPU (different streams, or several host
+ *   threads) race and must be serialised by the caller.
+ *   Arguments, outputs and statuses as in spec_tree_verify_stochastic.
+ */
+spec_status spec_tree_verify_stochastic_noalloc(const float* p_logits, const float* q_probs, const int32_t* tokens,
+                                                const int32_t* parent, const int32_t* tree_off,
+                                                const uint32_t* uniforms, int B, int n_max, int V, int32_t* path,
+                                                int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
+                                                int32_t* status, void* stream);
+
+/*
  * KV commit / rollback.  "SpecInfer Guide", "Depth-First Flattening and KV
  * Cache Reuse" and "PagedKV Allocation with Zero-Copy Pruning": only the
  * accepted path stays.  In place, for every kv-head: slot prefix_len[b] + i

@@ -30,6 +30,7 @@ SIGNATURES = {
     "spec_verify_workspace_size": ([_I, _I, _I], _SZ),
     "spec_tree_verify_greedy": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "spec_tree_verify_stochastic": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
+    "spec_tree_verify_stochastic_noalloc": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "spec_kv_commit": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "spec_philox_uniforms": ([_U64, _U32, _P, _I, _I, _P, _P], _I),
 }
@@ -134,6 +135,13 @@ def spec_tree_verify_stochastic(p_logits, q_probs, tokens, parent, tree_off, uni
         _ptr(p_logits), _ptr(q_probs), _ptr(tokens), _ptr(parent), _ptr(tree_off), _ptr(uniforms), B, n_max, V,
         _ptr(path), _ptr(accept_len), _ptr(emitted), _ptr(n_emitted), _ptr(workspace), ws_bytes, _ptr(status),
         _stream(stream)))
+
+
+def spec_tree_verify_stochastic_noalloc(p_logits, q_probs, tokens, parent, tree_off, uniforms, B, n_max, V, path,
+                                        accept_len, emitted, n_emitted, status, stream=None):
+    _check("spec_tree_verify_stochastic_noalloc", lib().spec_tree_verify_stochastic_noalloc(
+        _ptr(p_logits), _ptr(q_probs), _ptr(tokens), _ptr(parent), _ptr(tree_off), _ptr(uniforms), B, n_max, V,
+        _ptr(path), _ptr(accept_len), _ptr(emitted), _ptr(n_emitted), _ptr(status), _stream(stream)))
 
 
 def spec_kv_commit(k_cache, v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len, path, path_stride,
