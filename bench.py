@@ -47,7 +47,7 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def algorithmic_bytes(w, stats):
+def algorithmic_bytes(w, stats, mode="stochastic"):
     """Per-launch algorithmic bytes of each kernel (formulas of the design)."""
     s = 2 if w.dtype == 1 else 4
     Wd = (w.n_max + 63) // 64
@@ -55,7 +55,7 @@ def algorithmic_bytes(w, stats):
     P = w.prefix_len.tolist()
     attn = sum(2 * w.Hkv * w.D * s * (P[b] + n[b]) + 2 * n[b] * w.Hq * w.D * s + 8 * n[b] * Wd for b in range(w.B))
     internal = stats["internal_nodes"]
-    verify = 4 * w.T * w.V + 4 * w.V * internal
+    verify = 4 * w.T * w.V + (4 * w.V * internal if mode == "stochastic" else 0)
     mask = 4 * w.T + 12 * w.T + 8 * w.T * Wd
     commit = 2 * 2 * w.Hkv * w.D * s * stats["moved_rows"]
     return dict(mask=mask, attention=attn, verify=verify, commit=commit)
@@ -74,27 +74,105 @@ def _tree_stats(w, accept_paths):
     return dict(internal_nodes=internal, moved_rows=moved)
 
 
-class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+class _Cudart:
+    """The CUDA runtime the process already loaded (PyTorch's), for external
+    event records inside captured graphs."""
 
-    def __init__(self, gpu_index):
-        self.idx = gpu_index
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = None
+        for name in ("libcudart.so.13", "libcudart.so", "/usr/local/cuda/lib64/libcudart.so.13"):
+            try:
+                self.lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if self.lib is None:
+            raise RuntimeError("libcudart not found")
+        self.lib.cudaEventCreateWithFlags.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint]
+        self.lib.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.lib.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        self.lib.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+
+    def event(self):
+        e = self.ct.c_void_p()
+        assert self.lib.cudaEventCreateWithFlags(self.ct.byref(e), 0) == 0
+        return e
+
+    def record_external(self, ev, stream):  # cudaEventRecordExternal: a node of the captured graph
+        assert self.lib.cudaEventRecordWithFlags(ev, self.ct.c_void_p(stream.cuda_stream), 1) == 0
+
+    def elapsed_ms(self, a, b):
+        ms = self.ct.c_float()
+        assert self.lib.cudaEventElapsedTime(self.ct.byref(ms), a, b) == 0
+        return ms.value
+
+
+class ClockSampler:
+    """SM clock and clock-event reasons of one GPU, sampled every ~2 ms in a
+    background thread through NVML (read-only queries), with nvidia-smi as a
+    fallback when NVML cannot be loaded."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index):
+        import threading
+        self.dev = device_index
+        self.samples = []
+        self.stop = threading.Event()
+        self.thread = None
         self.proc = None
 
+    def _nvml(self):
+        import ctypes
+        import torch
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        assert nv.nvmlInit_v2() == 0
+        h = ctypes.c_void_p()
+        uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+            assert nv.nvmlDeviceGetHandleByIndex_v2(self.dev, ctypes.byref(h)) == 0
+        return nv, h
+
+    def _run(self):
+        import ctypes
+        nv, h = self.nv, self.h
+        mhz, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop.is_set():
+            ok = nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0  # NVML_CLOCK_SM
+            nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            get_reasons(h, ctypes.byref(rs))
+            if ok:
+                self.samples.append((float(mhz.value), float(mx.value), int(rs.value)))
+            time.sleep(0.002)
+
     def __enter__(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.nv, self.h = self._nvml()
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
         except Exception:
-            self.proc = None
+            self.thread = None
+            try:
+                q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                     "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_power_cap")
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={q}",
+                                              "--format=csv,noheader,nounits", "-lms", "100"],
+                                             stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self.proc = None
         return self
 
     def __exit__(self, *a):
-        self.lines = []
+        self.stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -102,27 +180,22 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            names = [0x8, 0x40, 0x20, 0x4]
+            for l in out.splitlines():
+                f = [x.strip() for x in l.split(",")]
+                try:
+                    r = sum(bit for bit, v in zip(names, f[2:6]) if v.lower().startswith("active"))
+                    self.samples.append((float(f[0]), float(f[1]), r))
+                except (ValueError, IndexError):
+                    continue
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = sorted({name for _, _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(x[0] for x in self.samples),
+                "sm_max_mhz": max(x[1] for x in self.samples), "reasons": reasons, "samples": len(self.samples),
+                "source": "nvml" if self.thread is not None else "nvidia-smi"}
 
 
 def run_cpu_baseline(w, seconds_cap=30.0):
@@ -197,7 +270,7 @@ def bench_gpu(args):
     B_.build()
     S.lib()
     dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream(dev)
+    rt = _Cudart()
 
     sets, passes, works = [], [], []
     for i in range(N_SETS):
@@ -208,49 +281,69 @@ def bench_gpu(args):
         passes.append(VerifyPass(d))
     torch.cuda.synchronize()
 
-    def step(i, ev=None):
-        vp = passes[i % N_SETS]
-        if ev is not None:
-            ev[0].record(stream)
+    def step(vp, evs=None, stream=None):
+        marks = [] if evs is None else evs
+        if marks:
+            rt.record_external(marks[0], stream)
         vp.mask_build()
-        if ev is not None:
-            ev[1].record(stream)
+        if marks:
+            rt.record_external(marks[1], stream)
         vp.attention(args.attn_flags)
-        if ev is not None:
-            ev[2].record(stream)
+        if marks:
+            rt.record_external(marks[2], stream)
         vp.verify(args.mode)
-        if ev is not None:
-            ev[3].record(stream)
+        if marks:
+            rt.record_external(marks[3], stream)
         vp.commit()
-        if ev is not None:
-            ev[4].record(stream)
+        if marks:
+            rt.record_external(marks[4], stream)
 
+    # eager warm-up (first calls set kernel attributes and look up driver entry points)
     for i in range(args.warmup):
-        step(i)
+        step(passes[i % N_SETS])
+    torch.cuda.synchronize()
+
+    # one CUDA graph per (input set, copy); each carries its own stage events
+    cap = torch.cuda.Stream(dev)
+    graphs, gevs = [], []
+    copies = 4
+    for c in range(copies):
+        for i in range(N_SETS):
+            evs = [rt.event() for _ in range(5)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                step(passes[i], evs, torch.cuda.current_stream(dev))
+            graphs.append(g)
+            gevs.append(evs)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    for i in range(args.warmup):
+        graphs[i % len(graphs)].replay()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         t_start.record(stream)
         for i in range(args.steps):
-            step(args.warmup + i, evs[i])
+            graphs[i % len(graphs)].replay()
         t_end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
+    # stage times of the last replay of every graph (inside the timed region)
     stage = {k: [] for k in ("mask", "attention", "verify", "commit")}
-    for e in evs:
+    for gi in range(min(len(graphs), args.steps)):
+        e = gevs[gi]
         for j, k in enumerate(stage):
-            stage[k].append(e[j].elapsed_time(e[j + 1]))
+            stage[k].append(rt.elapsed_ms(e[j], e[j + 1]))
 
     # emitted tokens per step (verify inputs do not change between steps of one set)
     tokens_per_set = [int(p.n_emitted[:p.batch.B].sum()) for p in passes]
     status_ok = all(int(p.status[:p.batch.B].abs().sum()) == 0 for p in passes)
-    tokens = sum(tokens_per_set[(args.warmup + i) % N_SETS] for i in range(args.steps))
+    tokens = sum(tokens_per_set[(i % len(graphs)) % N_SETS] for i in range(args.steps))
     if world > 1:
         t = torch.tensor([elapsed_ms, float(tokens)], dtype=torch.float64, device=dev)
         mx = t.clone()
@@ -260,34 +353,37 @@ def bench_gpu(args):
         elapsed_ms, tokens = float(mx[0]), float(sm[1])
     value = tokens / (elapsed_ms / 1e3)
 
-    # --- e2e through the C ABI with host buffers: H2D of the step's inputs from
-    # pinned memory, the pass, D2H of the emitted tokens; KV cache is resident state.
+    # --- e2e through the C ABI with host buffers: per step, H2D of the step's
+    # inputs from pinned memory, the five calls, D2H of the emitted tokens; the KV
+    # cache is resident state.
     e2e = run_e2e(args, works, sets, passes, stream, dev)
 
     # --- roofline of the dominant kernel
     peak, peak_kind = _peaks()
     w0 = works[0]
     stats = _tree_stats(w0, passes[0].path[:w0.B].tolist())
-    algo = algorithmic_bytes(w0, stats)
+    algo = algorithmic_bytes(w0, stats, args.mode)
     avg = {k: statistics.mean(v) for k, v in stage.items()}
     dom = max(("attention", "verify"), key=lambda k: avg[k])
     kernels = {k: {"ms": avg[k], "bytes": algo[k], "gbs": algo[k] / (avg[k] * 1e-3) / 1e9,
                    "frac_hbm": algo[k] / (avg[k] * 1e-3) / 1e9 / peak} for k in avg}
     achieved = kernels[dom]["gbs"]
     launches_per_step = 4 + (1 if _attn_splits(passes[0]) > 1 else 0)
+    traffic = _profiled_traffic(dom, args.mode)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "verify": args.mode, "input_sets": N_SETS,
                        "l2": "3 rotating input sets of ~205 MB each (inputs larger than L2)",
+                       "launch": "one CUDA graph per step (the five C-ABI calls captured)",
                        "tokens_per_step": tokens / args.steps / max(world, 1), "status_ok": status_ok,
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "clocks": clk.summary(),
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind},
+                         "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind},
             "kernels": kernels}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, _ = run_cpu_baseline(works[0])
@@ -297,6 +393,24 @@ def bench_gpu(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def _profiled_traffic(kernel, mode):
+    """DRAM bytes per launch (read + write) of the dominant kernel from the
+    committed ncu summary, or None when the summary is missing or the kernel
+    source changed since the capture."""
+    import hashlib
+    src = {"attention": "attention_tc.cu", "verify": "verify.cu"}[kernel]
+    path = os.path.join(ROOT, "tree_speculative_verification_spec_gb300", "csrc", src)
+    try:
+        digest = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+        for line in open(os.path.join(ROOT, "profiles", "traffic.md")):
+            f = [x.strip() for x in line.strip().strip("|").split("|")]
+            if len(f) >= 4 and f[0] == kernel and f[1] == mode and f[2] == digest:
+                return float(f[3])
+    except (OSError, ValueError):
+        pass
+    return None
 
 
 def _attn_splits(vp):
@@ -345,7 +459,7 @@ def run_e2e(args, works, sets, passes, stream, dev):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--mode", default="stochastic", choices=["stochastic", "greedy"])

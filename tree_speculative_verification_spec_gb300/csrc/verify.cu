@@ -23,8 +23,13 @@ namespace cg = cooperative_groups;
 
 namespace spectree {
 
-constexpr int kVerifyThreads = 256;
-constexpr int kSlice = 8192;  // vocabulary entries per CTA (wider slices above 8 * kSlice)
+// Stochastic: 128-thread CTAs over 4096-entry slices held in shared memory
+// (up to 8 CTAs per SM).  Greedy streams its slice once: 256-thread CTAs over
+// 16384-entry slices.  Slices widen beyond 8 CTAs per cluster.
+constexpr int kVerifyThreads = 256;  // upper bound of the two block sizes
+template <int MODE> struct VCfg;
+template <> struct VCfg<0> { static constexpr int threads = 256, slice = 16384, min_blocks = 4; };
+template <> struct VCfg<1> { static constexpr int threads = 128, slice = 4096, min_blocks = 8; };
 
 // ---------------------------------------------------------------------------
 // fp32 arithmetic contract of the stochastic verifier.  Every operation is a
@@ -69,6 +74,30 @@ __device__ __forceinline__ unsigned long long fx(float v) {
   if (e == 0) return 0ull;  // zero or subnormal: below 2^-126 * 2^46
   return sh >= 0 ? (m << sh) : (sh > -24 ? (m >> (-sh)) : 0ull);
 }
+// Running sum of FX values, mostly on the FMA pipe: for 0 <= v <= 1,
+// v * 2^46 = A * 2^23 + B with A = trunc(v * 2^23) and B = trunc(frac(v * 2^23) * 2^23);
+// each is read off a round-toward-zero addition of 2^23 (ulp 1 on [2^23, 2^24]).
+// A and B of up to 2^6 * 2^8 terms fit 32 bits; values above 1 take fx().
+struct FxSum {
+  uint32_t a = 0, b = 0;
+  unsigned long long big = 0;
+  __device__ __forceinline__ void add(float v) {
+    if (v <= 1.0f) {
+      const float y1 = __fmul_rn(v, 0x1p23f);
+      const float t = __fadd_rz(y1, 0x1p23f);
+      const float f = __fsub_rn(y1, __fsub_rn(t, 0x1p23f));
+      const float t2 = __fadd_rz(__fmul_rn(f, 0x1p23f), 0x1p23f);
+      a += __float_as_uint(t) - 0x4B000000u;
+      b += __float_as_uint(t2) - 0x4B000000u;
+    } else {
+      big += fx(v);
+    }
+  }
+  __device__ __forceinline__ unsigned long long total() const {
+    return ((unsigned long long)a << 23) + (unsigned long long)b + big;
+  }
+};
+
 __device__ __forceinline__ float z_of(unsigned long long S) { return __fmul_rn(__ull2float_rn(S), 0x1p-46f); }
 
 // floor(U * S / 2^32), exact for U < 2^32, S < 2^64.
@@ -297,7 +326,8 @@ __device__ __forceinline__ bool bulk_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int MODE, int C>
-__global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(VCfg<MODE>::threads, VCfg<MODE>::min_blocks) verify_kernel(VerifyArgs a) {
+  constexpr int NT = VCfg<MODE>::threads;
   extern __shared__ float4 dyn_smem[];
   float* D = reinterpret_cast<float*>(dyn_smem);  // stochastic: the node's weights slice
   __shared__ Red red;
@@ -345,16 +375,16 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
       if ((V & 3) == 0) {
         const float4* p4 = reinterpret_cast<const float4*>(prow);
         const int j0 = x0 >> 2, j1 = x1 >> 2;
-        for (int j = j0 + threadIdx.x; j < j1; j += 4 * kVerifyThreads) {
+        for (int j = j0 + threadIdx.x; j < j1; j += 4 * NT) {
           float4 v[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int jj = j + q * kVerifyThreads;
+            const int jj = j + q * NT;
             v[q] = jj < j1 ? __ldcs(p4 + jj) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
           }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int x = (j + q * kVerifyThreads) << 2;
+            const int x = (j + q * NT) << 2;
             if (v[q].x > bv) { bv = v[q].x; bi = x; }
             if (v[q].y > bv) { bv = v[q].y; bi = x + 1; }
             if (v[q].z > bv) { bv = v[q].z; bi = x + 2; }
@@ -405,7 +435,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
         lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
       }
       const float m = cluster_max<C>(lmax, red, xs, par);
-      unsigned long long ls = 0;
+      FxSum acc;
       for (int j = threadIdx.x; j < (lenp >> 2); j += blockDim.x) {
         float4 v = D4[j];
         v.x = canon_exp(__fsub_rn(v.x, m));
@@ -413,8 +443,12 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
         v.z = canon_exp(__fsub_rn(v.z, m));
         v.w = canon_exp(__fsub_rn(v.w, m));
         D4[j] = v;
-        ls += fx(v.x) + fx(v.y) + fx(v.z) + fx(v.w);
+        acc.add(v.x);
+        acc.add(v.y);
+        acc.add(v.z);
+        acc.add(v.w);
       }
+      unsigned long long ls = acc.total();
       unsigned long long S = cluster_sum<C>(ls, red, xs, par);
       float Z = z_of(S);
 
@@ -455,6 +489,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
         unsigned long long ln = 0;
         if ((V & 3) == 0) {
           const float4* q4 = reinterpret_cast<const float4*>(qrow + x0);
+          FxSum ra;
           for (int j = threadIdx.x; j < (len >> 2); j += blockDim.x) {
             float4 d = D4[j];
             const float4 qq = __ldg(q4 + j);
@@ -463,8 +498,12 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(VerifyArgs a)
             d.z = resid(d.z, Z, qq.z);
             d.w = resid(d.w, Z, qq.w);
             D4[j] = d;
-            ln += fx(d.x) + fx(d.y) + fx(d.z) + fx(d.w);
+            ra.add(d.x);
+            ra.add(d.y);
+            ra.add(d.z);
+            ra.add(d.w);
           }
+          ln = ra.total();
         } else {
           for (int j = threadIdx.x; j < len; j += blockDim.x) {
             const float dn = resid(D[j], Z, __ldg(qrow + x0 + j));
@@ -680,7 +719,7 @@ cudaError_t launch_verify(const VerifyArgs& a, int B, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(B * C), (unsigned)a.n_max, 1);
-  cfg.blockDim = dim3(kVerifyThreads, 1, 1);
+  cfg.blockDim = dim3(VCfg<MODE>::threads, 1, 1);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -704,6 +743,7 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
   a.ws_ticket = reinterpret_cast<int32_t*>(ws + off_t);
   a.W = (a.n_max + 63) / 64;
   // cluster size: slices of kSlice entries, at most 8 CTAs (wider slices beyond)
+  constexpr int kSlice = VCfg<MODE>::slice;
   int C = (a.V + kSlice - 1) / kSlice;
   C = C <= 1 ? 1 : C <= 2 ? 2 : C <= 4 ? 4 : 8;
   a.slice = (((a.V + C - 1) / C) + 3) & ~3;
