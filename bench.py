@@ -255,6 +255,21 @@ def bench_reference(args):
     return 0
 
 
+def aggregate_replicas(elapsed_ms, tokens, device):
+    """Whole-job figures of independent replicas: the slowest rank's time and
+    the tokens of all ranks (no collective touches the data path)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return elapsed_ms, tokens
+    t = torch.tensor([elapsed_ms, tokens], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    sm = t.clone()
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(sm[1])
+
+
 def bench_gpu(args):
     import torch
     import workloads as W
@@ -344,13 +359,7 @@ def bench_gpu(args):
     tokens_per_set = [int(p.n_emitted[:p.batch.B].sum()) for p in passes]
     status_ok = all(int(p.status[:p.batch.B].abs().sum()) == 0 for p in passes)
     tokens = sum(tokens_per_set[(i % len(graphs)) % N_SETS] for i in range(args.steps))
-    if world > 1:
-        t = torch.tensor([elapsed_ms, float(tokens)], dtype=torch.float64, device=dev)
-        mx = t.clone()
-        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
-        sm = t.clone()
-        torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
-        elapsed_ms, tokens = float(mx[0]), float(sm[1])
+    elapsed_ms, tokens = aggregate_replicas(elapsed_ms, float(tokens), dev)
     value = tokens / (elapsed_ms / 1e3)
 
     # --- e2e through the C ABI with host buffers: per step, H2D of the step's
