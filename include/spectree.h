@@ -238,6 +238,15 @@ spec_status spec_kv_commit(void* k_cache, void* v_cache, const int32_t* block_ta
 spec_status spec_philox_uniforms(uint64_t seed, uint32_t round, const int32_t* tree_off, int B, int n_max,
                                  uint32_t* out, void* stream);
 
+/*
+ * Diagnostic of the bounded device waits (no counterpart on the pages): one
+ * small kernel waits on a barrier that nothing ever completes, with a limit of
+ * `polls` polls (1 .. 2^20), the same wait the tensor-core attention roles use
+ * with a limit of 2^25; on expiry it or-s SPEC_DEV_TIMEOUT into status[0] and
+ * returns, leaving the context usable.
+ */
+spec_status spec_selftest_bounded_wait(int32_t* status, uint32_t polls, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

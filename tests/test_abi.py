@@ -2,6 +2,7 @@
 include/spectree.h declares, the binding covers each of them under the same
 name, host-side argument checks return their codes before any launch, and the
 product shares no code with the oracle."""
+import ctypes
 import os
 import re
 import subprocess
@@ -96,6 +97,8 @@ def test_host_argument_checks_return_codes_without_launching(libpath):
     assert L.spec_kv_commit(None, None, None, 4, 12, 4, None, None, 4, None, 1, 2, 64, 1, None, None, None) == \
         S.SPEC_ERR_UNSUPPORTED
     assert L.spec_philox_uniforms(0, 0, None, -1, 4, None, None) == S.SPEC_ERR_INVALID_ARG
+    assert L.spec_selftest_bounded_wait(None, 16, None) == S.SPEC_ERR_INVALID_ARG
+    assert L.spec_selftest_bounded_wait(ctypes.c_void_p(16), 0, None) == S.SPEC_ERR_INVALID_ARG
 
 
 def test_workspace_sizes(libpath):

@@ -419,3 +419,15 @@ def test_full_pass_workload1(mode):
     assert np.array_equal(np_elems(vp.batch.k_cache, w.dtype), k_ref)
     assert np.array_equal(np_elems(vp.batch.v_cache, w.dtype), v_ref)
     assert np.array_equal(vp.new_len.cpu().numpy(), nl_ref)
+
+
+# ---------------------------------------------------------- failure detection ----
+
+def test_bounded_wait_expires_with_a_timeout_status_and_the_context_survives():
+    """A wait on a barrier nothing completes ends after its limit with
+    SPEC_DEV_TIMEOUT; the next call on the same context works normally."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    S.spec_selftest_bounded_wait(st, 4096)
+    torch.cuda.synchronize()
+    assert st.item() == S.SPEC_DEV_TIMEOUT
+    test_philox_parity(0, 0)

@@ -33,6 +33,7 @@ SIGNATURES = {
     "spec_tree_verify_stochastic_noalloc": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "spec_kv_commit": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "spec_philox_uniforms": ([_U64, _U32, _P, _I, _I, _P, _P], _I),
+    "spec_selftest_bounded_wait": ([_P, _U32, _P], _I),
 }
 
 _lib = None
@@ -155,3 +156,8 @@ def spec_kv_commit(k_cache, v_cache, block_table, max_blocks, block_size, num_bl
 def spec_philox_uniforms(seed, round_, tree_off, B, n_max, out, stream=None):
     _check("spec_philox_uniforms", lib().spec_philox_uniforms(
         ctypes.c_uint64(seed), ctypes.c_uint32(round_), _ptr(tree_off), B, n_max, _ptr(out), _stream(stream)))
+
+
+def spec_selftest_bounded_wait(status, polls, stream=None):
+    _check("spec_selftest_bounded_wait", lib().spec_selftest_bounded_wait(_ptr(status), ctypes.c_uint32(polls),
+                                                                            _stream(stream)))

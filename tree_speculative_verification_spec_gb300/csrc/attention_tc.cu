@@ -64,9 +64,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: false when the limit expired or another role gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+// Bounded wait: false when the limit expired (the abort flag is then set) or
+// another role gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 255u && *abort_flag) return false;
   }
@@ -565,6 +567,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Diagnostic of the bounded waits: one CTA waits on an mbarrier that nothing
+// ever arrives on, with a limit of `polls`, exactly as the roles above wait;
+// on expiry it records SPEC_DEV_TIMEOUT and returns.
+__global__ void selftest_wait_kernel(int32_t* status, uint32_t polls) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(&bar, 0, &abort_flag, polls);
+  __syncthreads();
+  if (threadIdx.x == 0 && (!ok || abort_flag)) atomicOr(status, SPEC_DEV_TIMEOUT);
+}
+
 }  // namespace tc
 
 // ---------------------------------------------------------------------------
@@ -632,3 +651,9 @@ cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace spectree
+
+extern "C" spec_status spec_selftest_bounded_wait(int32_t* status, uint32_t polls, void* stream) {
+  if (!status || polls == 0 || polls > (1u << 20)) return SPEC_ERR_INVALID_ARG;
+  spectree::tc::selftest_wait_kernel<<<1, 64, 0, (cudaStream_t)stream>>>(status, polls);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
