@@ -54,24 +54,35 @@ def algorithmic_bytes(w, stats, mode="stochastic"):
     n = (w.tree_off[1:] - w.tree_off[:-1]).tolist()
     P = w.prefix_len.tolist()
     attn = sum(2 * w.Hkv * w.D * s * (P[b] + n[b]) + 2 * n[b] * w.Hq * w.D * s + 8 * n[b] * Wd for b in range(w.B))
-    internal = stats["internal_nodes"]
-    verify = 4 * w.T * w.V + (4 * w.V * internal if mode == "stochastic" else 0)
+    # the walk reads the target row of every node it reaches, and the draft row
+    # of every reached node where a child was rejected
+    verify = 4 * w.V * (stats["walk_rows"] + (stats["rejecting_nodes"] if mode == "stochastic" else 0))
     mask = 4 * w.T + 12 * w.T + 8 * w.T * Wd
     commit = 2 * 2 * w.Hkv * w.D * s * stats["moved_rows"]
     return dict(mask=mask, attention=attn, verify=verify, commit=commit)
 
 
 def _tree_stats(w, accept_paths):
+    """Rows the verifier's walk reads and rows the commit moves, from the
+    accepted paths: every path node's target row; the draft row of a path node
+    whose accepted child is not its first child, or of the last path node when
+    it has children (all of them rejected)."""
     par = w.parent.tolist()
     off = w.tree_off.tolist()
-    internal = 0
-    for b in range(w.B):
-        kids = set(par[off[b] + i] for i in range(1, off[b + 1] - off[b]))
-        internal += len(kids)
-    moved = 0
-    for row in accept_paths:
+    walk_rows = rejecting = moved = 0
+    for b, row in enumerate(accept_paths):
+        n = off[b + 1] - off[b]
+        kids = [[] for _ in range(n)]
+        for c in range(1, n):
+            kids[par[off[b] + c]].append(c)
+        path = [p for p in row if p >= 0]
+        walk_rows += len(path)
+        for i, u in enumerate(path):
+            nxt = path[i + 1] if i + 1 < len(path) else None
+            if kids[u] and (nxt is None or kids[u][0] != nxt):
+                rejecting += 1
         moved += sum(1 for i, p in enumerate(row) if p >= 0 and p != i)
-    return dict(internal_nodes=internal, moved_rows=moved)
+    return dict(walk_rows=walk_rows, rejecting_nodes=rejecting, moved_rows=moved)
 
 
 class _Cudart:

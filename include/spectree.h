@@ -126,7 +126,9 @@ spec_status spec_tree_attention(const void* q, const void* k_cache, const void* 
                                 void* workspace, size_t workspace_bytes, int32_t* status,
                                 uint32_t flags, void* stream);
 
-/* Bytes of workspace the verifiers need. */
+/* Bytes of workspace the verifiers take (a small constant: the walk keeps no
+ * state in global memory; the argument stays so that callers need not change
+ * when a variant needs scratch). */
 size_t spec_verify_workspace_size(int B, int n_max, int V);
 
 /*
@@ -138,21 +140,25 @@ size_t spec_verify_workspace_size(int B, int n_max, int V);
  * The accepted node f is the deepest node whose whole root path follows the
  * argmax chain (ties between equally deep nodes: lowest node index; with
  * distinct sibling tokens this is the walk above).  argmax ties go to the
- * lowest token id.  Logits must be finite.
+ * lowest token id.  Logits must be finite.  One thread-block cluster per
+ * request walks the tree level by level; only rows of nodes on matching
+ * paths are read.
  *   p_logits   float [T][V]
  *   tokens     int32 [T]       draft token of each node (the root's is not used for matching)
- *   parent, tree_off, mask, depth  as produced / consumed by spec_tree_mask_build
+ *   parent, tree_off           as for spec_tree_mask_build
  *   path       int32 [B][n_max] out: accepted nodes root first (local indices), then -1
  *   accept_len int32 [B]       out: number of accepted nodes including the root
  *   emitted    int32 [B][n_max] out: tokens of path[1..] then the correction / bonus token, then -1
  *   n_emitted  int32 [B]       out: = accept_len
- *   workspace  device scratch of spec_verify_workspace_size() bytes (no state between calls)
- *   status     int32 [B]       in/out: or-ed with SPEC_DEV_BAD_TOKEN; a request whose status is
- *                              non-zero after the call has accept_len = n_emitted = 0 and -1 rows.
+ *   workspace  device memory of at least spec_verify_workspace_size() bytes (not read or written)
+ *   status     int32 [B]       in/out: a request whose incoming status is non-zero is skipped;
+ *                              otherwise or-ed with SPEC_DEV_BAD_TREE (invalid parent array or
+ *                              n_b outside [0, n_max]) and SPEC_DEV_BAD_TOKEN; a request whose
+ *                              status is non-zero after the call has accept_len = n_emitted = 0
+ *                              and -1 rows.
  */
 spec_status spec_tree_verify_greedy(const float* p_logits, const int32_t* tokens, const int32_t* parent,
-                                    const int32_t* tree_off, const uint64_t* mask, const int32_t* depth,
-                                    int B, int n_max, int V,
+                                    const int32_t* tree_off, int B, int n_max, int V,
                                     int32_t* path, int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
                                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
@@ -177,7 +183,9 @@ spec_status spec_tree_verify_greedy(const float* p_logits, const int32_t* tokens
  *   q_probs    float [T][V]    row u: the draft distribution the children of u were drawn from
  *   uniforms   uint32 [T][2]   raw random words: [t][0] acceptance word of node t,
  *                              [t][1] sampling word used if the walk stops at node t
- *   other arguments as in spec_tree_verify_greedy (no mask / depth needed)
+ *   other arguments as in spec_tree_verify_greedy.  One cluster per request
+ *   follows the walk: a node's target row is read when the walk reaches it,
+ *   its draft row when one of its children is rejected.
  */
 spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_probs, const int32_t* tokens,
                                         const int32_t* parent, const int32_t* tree_off, const uint32_t* uniforms,
@@ -190,16 +198,13 @@ spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_pr
  * counterpart of this call).  For callers that cannot allocate device memory
  * at the point where they verify: a host framework that hands the library only
  * its inputs and outputs, or a latency-critical loop that must not pay the
- * device-wide synchronisation of cudaMalloc.  Its scratch is a fixed file-scope
- * device array of about 2.1 MB that every GPU loading the library keeps until
- * the process exits.
+ * device-wide synchronisation of cudaMalloc.  It hands the verifier a fixed
+ * file-scope device array as its workspace, which every GPU loading the
+ * library keeps until the process exits.
  *   Limits: B <= 16384 and B * n_max <= 262144; larger batches return
  *   SPEC_ERR_UNSUPPORTED and launch nothing.
  *   The first call on each device looks up the array's device address (with
  *   that device current): make that first call before any stream capture.
- *   Every call uses the same array, and the call clears what must start at
- *   zero: calls that overlap on the GPU (different streams, or several host
- *   threads) race and must be serialised by the caller.
  *   Arguments, outputs and statuses as in spec_tree_verify_stochastic.
  */
 spec_status spec_tree_verify_stochastic_noalloc(const float* p_logits, const float* q_probs, const int32_t* tokens,

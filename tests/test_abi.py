@@ -85,9 +85,9 @@ def test_host_argument_checks_return_codes_without_launching(libpath):
         S.SPEC_ERR_INVALID_ARG
     # verify: vocabulary above 2^17, NULL pointers
     v = [None] * 6
-    assert L.spec_tree_verify_greedy(*v, 1, 4, 200000, None, None, None, None, None, 0, None, None) == \
+    assert L.spec_tree_verify_greedy(*v[:4], 1, 4, 200000, None, None, None, None, None, 0, None, None) == \
         S.SPEC_ERR_UNSUPPORTED
-    assert L.spec_tree_verify_greedy(*v, 1, 4, 1000, None, None, None, None, None, 0, None, None) == \
+    assert L.spec_tree_verify_greedy(*v[:4], 1, 4, 1000, None, None, None, None, None, 0, None, None) == \
         S.SPEC_ERR_INVALID_ARG
     assert L.spec_tree_verify_stochastic(*v, 1, 4, 0, None, None, None, None, None, 0, None, None) == \
         S.SPEC_ERR_INVALID_ARG
@@ -107,8 +107,8 @@ def test_workspace_sizes(libpath):
     # one request with a long prefix needs key splits: room for the partial rows
     one = S.spec_attention_workspace_size(1, 40, 40, 100000, 32, 8, 128)
     assert one >= 2 * 40 * 32 * (128 + 2) * 4
-    v = S.spec_verify_workspace_size(8, 64, 32000)
-    assert v >= 2 * 8 * 64 * 4 + 8 * 4
+    # the walk keeps no state in global memory: a small constant
+    assert S.spec_verify_workspace_size(8, 64, 32000) == S.spec_verify_workspace_size(1, 1024, 131072) >= 16
 
 
 def test_product_and_oracle_share_no_code(libpath):

@@ -28,7 +28,7 @@ SIGNATURES = {
     "spec_tree_attention": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _SZ,
                              _P, _U32, _P], _I),
     "spec_verify_workspace_size": ([_I, _I, _I], _SZ),
-    "spec_tree_verify_greedy": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
+    "spec_tree_verify_greedy": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "spec_tree_verify_stochastic": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "spec_tree_verify_stochastic_noalloc": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "spec_kv_commit": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
@@ -120,11 +120,11 @@ def spec_verify_workspace_size(B, n_max, V):
     return int(lib().spec_verify_workspace_size(B, n_max, V))
 
 
-def spec_tree_verify_greedy(p_logits, tokens, parent, tree_off, mask, depth, B, n_max, V, path, accept_len,
-                            emitted, n_emitted, workspace, status, stream=None):
+def spec_tree_verify_greedy(p_logits, tokens, parent, tree_off, B, n_max, V, path, accept_len, emitted, n_emitted,
+                            workspace, status, stream=None):
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("spec_tree_verify_greedy", lib().spec_tree_verify_greedy(
-        _ptr(p_logits), _ptr(tokens), _ptr(parent), _ptr(tree_off), _ptr(mask), _ptr(depth), B, n_max, V,
+        _ptr(p_logits), _ptr(tokens), _ptr(parent), _ptr(tree_off), B, n_max, V,
         _ptr(path), _ptr(accept_len), _ptr(emitted), _ptr(n_emitted), _ptr(workspace), ws_bytes, _ptr(status),
         _stream(stream)))
 

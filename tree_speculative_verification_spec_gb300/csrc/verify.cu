@@ -1,35 +1,32 @@
-// Token-tree verification, greedy and stochastic, in one launch per call.
+// Token-tree verification, greedy and stochastic: one launch, one
+// thread-block cluster per request, walking the request's tree from the root.
 //
-// Phase A (one thread-block cluster per tree node): the node's target row is
-// streamed once from HBM, split across the C CTAs of the cluster (a slice of
-// at most kSlice vocabulary entries each, held in shared memory for the
-// stochastic verifier); row reductions combine through distributed shared
-// memory.  Greedy: the argmax of the row.  Stochastic: the node decides, by
-// itself, which of its children the walk would accept if it reached the node
-// (the decision depends only on the node's own rows, its children's tokens
-// and their random words), and, when none is accepted, samples the
-// correction / bonus token.
-// Phase B (the last CTA to finish a request, found with an atomic ticket):
-// greedy picks the deepest node whose root path follows the argmax chain;
-// stochastic follows the accepted-child links from the root.  No CTA ever
-// waits for another.
-#include <cooperative_groups.h>
-
+// "SpecInfer Guide", "Greedy Verification Algorithm" and "Stochastic
+// Verification Algorithm": verification starts at the root (the last
+// verified token), tests the children of the current node against the
+// target's row of that node and moves into the accepted child.  Only the
+// rows of nodes the walk reaches are read: the target row of every node on
+// the accepted path, the draft row of a node where a child was rejected.
+//
+// The C CTAs of a cluster split the vocabulary into C slices.  Each row
+// reduction (max, argmax, fixed-point sums, the exclusive prefix of the final
+// sample) is a block reduction followed by one cluster barrier and reads of
+// the peers' exchange slots in distributed shared memory.  Every CTA takes
+// the same decisions: they depend only on cluster-reduced values and on
+// single entries (a child's logit and draft probability) that each CTA reads
+// and evaluates itself.  While a node is processed, the row slices its
+// children would need next are prefetched into L2.  No CTA waits for a CTA of
+// another cluster.
 #include <mutex>
 
 #include "common.cuh"
 
-namespace cg = cooperative_groups;
-
 namespace spectree {
 
-// Stochastic: 128-thread CTAs over 4096-entry slices held in shared memory
-// (up to 8 CTAs per SM).  Greedy streams its slice once: 256-thread CTAs over
-// 16384-entry slices.  Slices widen beyond 8 CTAs per cluster.
-constexpr int kVerifyThreads = 256;  // upper bound of the two block sizes
-template <int MODE> struct VCfg;
-template <> struct VCfg<0> { static constexpr int threads = 256, slice = 16384, min_blocks = 4; };
-template <> struct VCfg<1> { static constexpr int threads = 128, slice = 4096, min_blocks = 8; };
+constexpr int kWalkThreads = 512;
+constexpr int kMaxSlice = 20480;  // stochastic: floats of one CTA's slice (target and draft: 160 KB)
+constexpr int kMaxCluster = 16;   // 16 needs the non-portable cluster size
+constexpr int kTargetCtas = 152;  // one CTA per SM when the batch is small
 
 // ---------------------------------------------------------------------------
 // fp32 arithmetic contract of the stochastic verifier.  Every operation is a
@@ -77,7 +74,8 @@ __device__ __forceinline__ unsigned long long fx(float v) {
 // Running sum of FX values, mostly on the FMA pipe: for 0 <= v <= 1,
 // v * 2^46 = A * 2^23 + B with A = trunc(v * 2^23) and B = trunc(frac(v * 2^23) * 2^23);
 // each is read off a round-toward-zero addition of 2^23 (ulp 1 on [2^23, 2^24]).
-// A and B of up to 2^6 * 2^8 terms fit 32 bits; values above 1 take fx().
+// A and B stay below 2^32 for up to 511 terms (a thread adds at most 48 here);
+// values above 1 take fx().
 struct FxSum {
   uint32_t a = 0, b = 0;
   unsigned long long big = 0;
@@ -107,20 +105,25 @@ __device__ __forceinline__ unsigned long long sample_target(uint32_t U, unsigned
   return hi + (lo >> 32);
 }
 
-// residual step: max(r - q, 0) written as a comparison (no fmax sign-of-zero ambiguity)
+// residual step: max(r - q, 0) written as a comparison (no fmax sign-of-zero
+// ambiguity).  A zero weight (every weight the previous steps clamped) skips
+// the division: +0 / Z is +0 for the finite positive Z, the same value.
 __device__ __forceinline__ float resid(float d, float Z, float q) {
-  const float diff = __fsub_rn(__fdiv_rn(d, Z), q);
+  const float r = d == 0.0f ? 0.0f : __fdiv_rn(d, Z);
+  const float diff = __fsub_rn(r, q);
   return diff > 0.0f ? diff : 0.0f;
 }
 
 // ---------------------------------------------------------------------------
-// Block / cluster reductions
+// Block reductions
 // ---------------------------------------------------------------------------
 
+constexpr int kWarps = kWalkThreads / 32;
+
 struct Red {
-  float f[kVerifyThreads / 32];
-  int i[kVerifyThreads / 32];
-  unsigned long long u[kVerifyThreads / 32];
+  float f[kWarps];
+  int i[kWarps];
+  unsigned long long u[kWarps];
 };
 
 __device__ __forceinline__ float block_max(float v, Red& s) {
@@ -130,7 +133,7 @@ __device__ __forceinline__ float block_max(float v, Red& s) {
   if (l == 0) s.f[w] = v;
   __syncthreads();
   v = s.f[0];
-  for (int k = 1; k < (int)(blockDim.x >> 5); ++k) v = fmaxf(v, s.f[k]);
+  for (int k = 1; k < kWarps; ++k) v = fmaxf(v, s.f[k]);
   return v;
 }
 
@@ -141,7 +144,7 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
   if (l == 0) s.u[w] = v;
   __syncthreads();
   v = 0;
-  for (int k = 0; k < (int)(blockDim.x >> 5); ++k) v += s.u[k];
+  for (int k = 0; k < kWarps; ++k) v += s.u[k];
   return v;
 }
 
@@ -169,82 +172,121 @@ __device__ __forceinline__ void block_argmax(float& v, int& i, Red& s) {
   __syncthreads();
   v = s.f[0];
   i = s.i[0];
-  for (int k = 1; k < (int)(blockDim.x >> 5); ++k) argmax_combine(v, i, s.f[k], s.i[k]);
+  for (int k = 1; k < kWarps; ++k) argmax_combine(v, i, s.f[k], s.i[k]);
 }
 
-// Cluster exchange slots (one per CTA, read by every CTA of the cluster).
-struct XSlot {
-  float f;
-  int i;
-  unsigned long long u;
+// ---------------------------------------------------------------------------
+// Cluster exchange: every CTA pushes one 8-byte value into slot [k & 1][rank]
+// of every CTA of the cluster (st.async to distributed shared memory,
+// completing on the receiver's mbarrier of that slot), then waits on its own
+// mbarrier for the C values of exchange k.  One one-way trip instead of a
+// cluster barrier.  Slot reuse is safe: a CTA pushes exchange k + 2 only after
+// finishing exchange k + 1, which needs every peer's push of k + 1, which each
+// peer makes after reading its slots of exchange k (a block reduction with
+// __syncthreads separates the reads from the next push).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; false on expiry.
+__device__ __forceinline__ bool mbar_wait_bounded(const uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  for (uint32_t i = 0; i < (1u << 26); ++i)
+    if (mbar_try(a, parity)) return true;
+  return false;
+}
+
+struct Exch {
+  uint64_t bar[2];
+  unsigned long long v[2][kMaxCluster];
 };
 
 template <int C>
-__device__ __forceinline__ void cluster_sync_all() {
-  if constexpr (C == 1) __syncthreads();
-  else cg::this_cluster().sync();
+__device__ __forceinline__ const unsigned long long* exchange(unsigned long long val, Exch& ex, int& k, int rank,
+                                                              int32_t* status) {
+  const int s = k & 1;
+  const uint32_t parity = (uint32_t)(k >> 1) & 1u;
+  ++k;
+  if (threadIdx.x == 0) {
+    const uint32_t lbar = smem_addr(&ex.bar[s]), lslot = smem_addr(&ex.v[s][rank]);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(lbar), "r"((uint32_t)(C * 8))
+                 : "memory");
+#pragma unroll
+    for (int r = 0; r < C; ++r) {
+      uint32_t rs, rb;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rs) : "r"(lslot), "r"(r));
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(lbar), "r"(r));
+      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(rs), "l"(val),
+                   "r"(rb)
+                   : "memory");
+    }
+  }
+  if (!mbar_wait_bounded(&ex.bar[s], parity) && threadIdx.x == 0) atomicOr(status, SPEC_DEV_TIMEOUT);
+  return ex.v[s];
 }
 
-// Cluster reductions with one cluster barrier each: every CTA publishes its
-// block result in exchange slot `par`, the barrier makes it visible, every CTA
-// reads all C slots.  Slots alternate, so a slot is rewritten only after a
-// later barrier, which no CTA passes before finishing its reads of it.  A
-// final barrier before exit keeps peers' shared memory alive for late reads.
 template <int C>
-__device__ __forceinline__ float cluster_max(float v, Red& red, XSlot* xs, int& par) {
+__device__ __forceinline__ float cluster_max(float v, Red& red, Exch& ex, int& k, int rank, int32_t* status) {
   v = block_max(v, red);
   if constexpr (C == 1) return v;
-  cg::cluster_group cl = cg::this_cluster();
-  if (threadIdx.x == 0) xs[par].f = v;
-  cl.sync();
-  float m = v;
-  for (int r = 0; r < C; ++r) m = fmaxf(m, cl.map_shared_rank(xs + par, r)->f);
-  par ^= 1;
+  const unsigned long long* x = exchange<C>((unsigned long long)__float_as_uint(v), ex, k, rank, status);
+  float m = __uint_as_float((uint32_t)x[0]);
+#pragma unroll
+  for (int r = 1; r < C; ++r) m = fmaxf(m, __uint_as_float((uint32_t)x[r]));
   return m;
 }
 
+// Cluster total of per-thread values; `cta` receives this CTA's total.
 template <int C>
-__device__ __forceinline__ unsigned long long cluster_sum(unsigned long long v, Red& red, XSlot* xs, int& par) {
+__device__ __forceinline__ unsigned long long cluster_sum(unsigned long long v, Red& red, Exch& ex, int& k, int rank,
+                                                          int32_t* status, unsigned long long& cta) {
   v = block_sum_u64(v, red);
+  cta = v;
   if constexpr (C == 1) return v;
-  cg::cluster_group cl = cg::this_cluster();
-  if (threadIdx.x == 0) xs[par].u = v;
-  cl.sync();
-  unsigned long long s = 0;
-  for (int r = 0; r < C; ++r) s += cl.map_shared_rank(xs + par, r)->u;
-  par ^= 1;
-  return s;
+  const unsigned long long* x = exchange<C>(v, ex, k, rank, status);
+  unsigned long long t = 0;
+#pragma unroll
+  for (int r = 0; r < C; ++r) t += x[r];
+  return t;
 }
 
-// sum over the CTAs of lower rank (exclusive prefix)
+// Exclusive prefix over the ranks below this CTA of a CTA-uniform value.
 template <int C>
-__device__ __forceinline__ unsigned long long cluster_prefix(unsigned long long v, XSlot* xs, int& par, int rank) {
+__device__ __forceinline__ unsigned long long cluster_prefix(unsigned long long v, Exch& ex, int& k, int rank,
+                                                             int32_t* status) {
   if constexpr (C == 1) return 0ull;
-  cg::cluster_group cl = cg::this_cluster();
-  if (threadIdx.x == 0) xs[par].u = v;
-  cl.sync();
-  unsigned long long s = 0;
-  for (int r = 0; r < rank; ++r) s += cl.map_shared_rank(xs + par, r)->u;
-  par ^= 1;
-  return s;
+  __syncthreads();  // every thread has read the slots of the previous exchange
+  const unsigned long long* x = exchange<C>(v, ex, k, rank, status);
+  unsigned long long t = 0;
+  for (int r = 0; r < rank; ++r) t += x[r];
+  return t;
 }
 
 template <int C>
-__device__ __forceinline__ void cluster_argmax(float& v, int& i, Red& red, XSlot* xs, int& par) {
+__device__ __forceinline__ void cluster_argmax(float& v, int& i, Red& red, Exch& ex, int& k, int rank,
+                                               int32_t* status) {
   block_argmax(v, i, red);
   if constexpr (C == 1) return;
-  cg::cluster_group cl = cg::this_cluster();
-  if (threadIdx.x == 0) {
-    xs[par].f = v;
-    xs[par].i = i;
-  }
-  cl.sync();
-  for (int r = 0; r < C; ++r) {
-    const XSlot* p = cl.map_shared_rank(xs + par, r);
-    argmax_combine(v, i, p->f, p->i);
-  }
-  par ^= 1;
+  const unsigned long long x0 = ((unsigned long long)__float_as_uint(v) << 32) | (uint32_t)i;
+  const unsigned long long* x = exchange<C>(x0, ex, k, rank, status);
+#pragma unroll
+  for (int r = 0; r < C; ++r) argmax_combine(v, i, __uint_as_float((uint32_t)(x[r] >> 32)), (int)(uint32_t)x[r]);
 }
+
+// ---------------------------------------------------------------------------
+// Walk helpers
+// ---------------------------------------------------------------------------
 
 struct VerifyArgs {
   const float* p_logits;
@@ -252,23 +294,92 @@ struct VerifyArgs {
   const int32_t* tokens;
   const int32_t* parent;
   const int32_t* tree_off;
-  const uint64_t* mask;
-  const int32_t* depth;
   const uint2* uniforms;
-  int n_max, V, W, slice;
+  int n_max, V, slice;
+  int vec;  // V % 4 == 0 and 16-byte aligned rows: float4 passes, bulk copies, L2 prefetch
   int32_t* path;
   int32_t* accept_len;
   int32_t* emitted;
   int32_t* n_emitted;
   int32_t* status;
-  // workspace
-  int32_t* ws_a;        // [B * n_max]  greedy: argmax / stochastic: accepted child (or -1)
-  int32_t* ws_s;        // [B * n_max]  stochastic: sampled token when no child is accepted
-  int32_t* ws_ticket;   // [B]          zeroed by the host wrapper before the launch
 };
 
-__device__ __forceinline__ void clear_request(const VerifyArgs& a, int b) {
-  for (int i = threadIdx.x; i < a.n_max; i += blockDim.x) {
+struct WalkShared {
+  Red red;
+  Exch ex;
+  uint64_t dbar, qbar;          // stochastic: slice copies of the target and draft rows
+  int32_t par[SPEC_MAX_NODES];  // the request's parent array
+  int32_t tok[SPEC_MAX_NODES];  // the request's tokens
+  int32_t aux[SPEC_MAX_NODES];  // greedy: argmax of frontier nodes; stochastic: the path
+  union {
+    struct {
+      int32_t fr[SPEC_MAX_NODES];   // frontier
+      int32_t nx[SPEC_MAX_NODES];   // next frontier
+      int32_t inf[SPEC_MAX_NODES];  // 1 for frontier nodes
+    } g;
+    struct {
+      int32_t kids[SPEC_MAX_NODES];  // children of the node, increasing
+      float z[SPEC_MAX_NODES];       // normaliser before each residual step at the node
+      float cx[SPEC_MAX_NODES];      // the node's logit at each child's token
+      float cq[SPEC_MAX_NODES];      // the node's draft probability at each child's token
+      uint32_t cu[SPEC_MAX_NODES];   // each child's acceptance word
+    } s;
+  };
+  uint32_t uterm;  // stochastic: the node's sampling word
+  int cnt, flag;
+  unsigned long long wsum[kWarps];
+};
+
+// Ordered compaction by warp 0 of the c in [lo, hi) with pred(c) into out[]
+// (increasing c); every thread gets the count (one __syncthreads).
+template <class Pred>
+__device__ int compact(int lo, int hi, Pred pred, int32_t* out, WalkShared& sh) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int cnt = 0;
+    for (int base = lo; base < hi; base += 32) {
+      const int c = base + lane;
+      const bool is = c < hi && pred(c);
+      const unsigned m = __ballot_sync(0xffffffffu, is);
+      if (is) out[cnt + __popc(m & ((1u << lane) - 1u))] = c;
+      cnt += __popc(m);
+    }
+    if (lane == 0) sh.cnt = cnt;
+  }
+  __syncthreads();
+  return sh.cnt;
+}
+
+// L2 prefetch of [p, p + bytes): 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  if (bytes == 0) return;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Thread 0 starts a bulk copy global -> shared of `bytes` completing on `bar`.
+// The caller has made every earlier access to dst complete (__syncthreads
+// after a proxy fence) and waits with wait_copy before reading dst.
+__device__ __forceinline__ void start_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Bounded wait for a copy; on expiry SPEC_DEV_TIMEOUT is set and the copy is
+// waited for once more (it must land before the buffer is reused).
+__device__ __forceinline__ void wait_copy(uint64_t* bar, uint32_t& phase, int32_t* status) {
+  if (!mbar_wait_bounded(bar, phase)) {
+    if (threadIdx.x == 0) atomicOr(status, SPEC_DEV_TIMEOUT);
+    mbar_wait_bounded(bar, phase);
+  }
+  phase ^= 1u;
+}
+
+__device__ void clear_request(const VerifyArgs& a, int b) {
+  for (int i = threadIdx.x; i < a.n_max; i += kWalkThreads) {
     a.path[(size_t)b * a.n_max + i] = -1;
     a.emitted[(size_t)b * a.n_max + i] = -1;
   }
@@ -278,448 +389,447 @@ __device__ __forceinline__ void clear_request(const VerifyArgs& a, int b) {
   }
 }
 
-// Children of node u (local indices, increasing) into kids[]; returns the
-// count.  Ordered stream compaction: per chunk of blockDim candidates, warp
-// ballots give per-warp counts, thread 0 turns them into offsets.
-__device__ int collect_children(const int32_t* par, int n, int u, int* kids, int* s_cnt, int* s_wofs) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  if (threadIdx.x == 0) *s_cnt = 0;
-  __syncthreads();
-  for (int base = u + 1; base < n; base += blockDim.x) {
-    const int c = base + threadIdx.x;
-    const bool is = c < n && __ldg(par + c) == u;
-    const unsigned m = __ballot_sync(0xffffffffu, is);
-    if (lane == 0) s_wofs[w] = __popc(m);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int acc = *s_cnt;
-      for (int k = 0; k < nw; ++k) {
-        const int x = s_wofs[k];
-        s_wofs[k] = acc;
-        acc += x;
-      }
-      *s_cnt = acc;
-    }
-    __syncthreads();
-    if (is) kids[s_wofs[w] + __popc(m & ((1u << lane) - 1u))] = c;
-    __syncthreads();
-  }
-  return *s_cnt;
-}
-
-// Bulk copy of one row slice (global -> this CTA's shared memory) completing
-// on an mbarrier, and a bounded wait for it.
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ bool bulk_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < (1u << 26); ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
+// ---------------------------------------------------------------------------
+// The walk
+// ---------------------------------------------------------------------------
 
 template <int MODE, int C>
-__global__ void __launch_bounds__(VCfg<MODE>::threads, VCfg<MODE>::min_blocks) verify_kernel(VerifyArgs a) {
-  constexpr int NT = VCfg<MODE>::threads;
+__global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs a) {
   extern __shared__ float4 dyn_smem[];
-  float* D = reinterpret_cast<float*>(dyn_smem);  // stochastic: the node's weights slice
-  __shared__ Red red;
-  __shared__ XSlot xs[2];
-  __shared__ int32_t s_kids[SPEC_MAX_NODES];
-  __shared__ int s_cnt, s_last, s_flag;
-  __shared__ int s_wofs[kVerifyThreads / 32];
-  __shared__ uint64_t s_match[SPEC_MAX_WORDS];
-  __shared__ __align__(8) uint64_t s_bar;
-  __shared__ float s_z[SPEC_MAX_NODES];  // normalisers of the residual steps applied so far
+  __shared__ WalkShared sh;
 
-  // grid: x = (request, cluster rank), y = node; nodes near the root (most
-  // children, most residual passes) are dispatched first
   const int rank = (int)(blockIdx.x % C);
   const int b = (int)(blockIdx.x / C);
-  const int u = blockIdx.y;
-  int par = 0;  // exchange-slot parity of the cluster reductions
   const int off = a.tree_off[b];
   const int n = a.tree_off[b + 1] - off;
-  const bool n_ok = n >= 1 && n <= a.n_max;
-  const int n_cta = n_ok ? n : 1;  // requests without a valid tree still run phase B once
-  if (u >= n_cta) return;
-
-  // Only SPEC_DEV_BAD_TOKEN can change while this kernel runs (other CTAs set
-  // it); ignoring that bit keeps the decision uniform across a cluster.
-  const int st_in = *(volatile int32_t*)&a.status[b];
-  const bool work = n_ok && (st_in & ~SPEC_DEV_BAD_TOKEN) == 0;
   const int V = a.V;
-  const int x0 = rank * a.slice;
-  const int x1 = min(V, x0 + a.slice);
-  const int len = max(0, x1 - x0);
-  const int t = off + u;
+  const int x0 = min(V, rank * a.slice);
+  const int len = min(V, x0 + a.slice) - x0;
+  const bool vec = a.vec != 0;
+  int32_t* status = &a.status[b];
+  int xk = 0;  // exchange counter
+  const int st_in = *(volatile int32_t*)status;
+  const bool may_run = n >= 1 && n <= a.n_max && (st_in & ~(SPEC_DEV_BAD_TOKEN | SPEC_DEV_BAD_TREE)) == 0;
 
-  if (work && rank == 0 && threadIdx.x == 0) {
-    const int tok = a.tokens[t];
-    if (tok < 0 || tok >= V) atomicOr(&a.status[b], SPEC_DEV_BAD_TOKEN);
+  // stochastic: the root's target slice is copied while the inputs are checked
+  float* D = reinterpret_cast<float*>(dyn_smem);  // current weights of this CTA's slice
+  float* Q = D + a.slice;                          // this node's draft slice
+  uint32_t dphase = 0, qphase = 0;
+  const bool root_copy = MODE == 1 && may_run && vec && len > 0;
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.ex.bar[0])) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.ex.bar[1])) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.dbar)) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.qbar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (root_copy) start_copy(D, a.p_logits + (size_t)off * V + x0, (uint32_t)len * 4, &sh.dbar);
+    else if (MODE == 0 && may_run && vec) prefetch_l2(a.p_logits + (size_t)off * V + x0, (uint32_t)len * 4);
   }
-  if (work) {
-    const float* prow = a.p_logits + (size_t)t * V;
-    if constexpr (MODE == 0) {
-      // ---- greedy: argmax of row u, ties to the lowest token id; four
-      // independent 16-byte loads in flight per thread ----
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      if ((V & 3) == 0) {
-        const float4* p4 = reinterpret_cast<const float4*>(prow);
-        const int j0 = x0 >> 2, j1 = x1 >> 2;
-        for (int j = j0 + threadIdx.x; j < j1; j += 4 * NT) {
-          float4 v[4];
+  // Peers push into this CTA's exchange slots only after the cluster barrier
+  // completes (the mbarriers are initialised); it completes while the inputs
+  // are checked.
+  if constexpr (C > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+
+  // The tree and token checks are made by every CTA from the inputs; the only
+  // status bits this kernel sets are those checks' (by rank 0, when every CTA
+  // of the cluster skips the walk), so ignoring them in the incoming status
+  // keeps the decision uniform.
+  int bad = 0;
+  bool skip = (st_in & ~(SPEC_DEV_BAD_TOKEN | SPEC_DEV_BAD_TREE)) != 0;
+  if (!skip) {
+    const int nc = min(max(n, 0), a.n_max);  // nodes whose entries are checked
+    bool bt = false, bp = n < 0 || n > a.n_max;
+    for (int i = threadIdx.x; i < nc; i += kWalkThreads) {
+      const int t = a.tokens[off + i], p = a.parent[off + i];
+      sh.tok[i] = t;
+      sh.par[i] = p;
+      bt |= (unsigned)t >= (unsigned)V;
+      bp |= i == 0 ? p != -1 : (p < 0 || p >= i);
+    }
+    bad = (__syncthreads_or(bt) ? SPEC_DEV_BAD_TOKEN : 0) | (__syncthreads_or(bp) ? SPEC_DEV_BAD_TREE : 0);
+    skip = bad != 0 || n == 0;
+  }
+  if constexpr (C > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  __syncthreads();
+  if (skip) {
+    if (root_copy) wait_copy(&sh.dbar, dphase, status);  // the copy lands before the CTA leaves
+    if (rank == 0) {
+      clear_request(a, b);
+      if (bad && threadIdx.x == 0) atomicOr(status, bad);
+    }
+    return;  // uniform across the cluster; nothing was exchanged
+  }
+  int32_t* out_path = a.path + (size_t)b * a.n_max;
+  int32_t* out_emit = a.emitted + (size_t)b * a.n_max;
+
+  if constexpr (MODE == 0) {
+    // ---------------------------------------------------------------- greedy
+    // Level by level: the frontier holds every node of the current depth whose
+    // root path follows the argmax chain (several when siblings repeat a
+    // token).  Row argmaxes of the frontier, then the next frontier = children
+    // whose token equals their parent's argmax.  The accepted node is the
+    // lowest-index node of the deepest non-empty frontier.
+    int32_t* fr = sh.g.fr;  // frontier
+    int32_t* nx = sh.g.nx;  // next frontier
+    int32_t* inf = sh.g.inf;
+    for (int i = threadIdx.x; i < n; i += kWalkThreads) inf[i] = i == 0;
+    if (threadIdx.x == 0) fr[0] = 0;
+    int nf = 1, depth = 0;
+    __syncthreads();
+    for (;;) {
+      // warp 0: L2 prefetch of the frontier's children's slices
+      if (vec && threadIdx.x < 32)
+        for (int c = 1 + (int)threadIdx.x; c < n; c += 32)
+          if (inf[sh.par[c]]) prefetch_l2(a.p_logits + (size_t)(off + c) * V + x0, (uint32_t)len * 4);
+      for (int i = 0; i < nf; ++i) {
+        const int u = fr[i];
+        const float* prow = a.p_logits + (size_t)(off + u) * V + x0;
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        if (vec) {
+          const float4* p4 = reinterpret_cast<const float4*>(prow);
+          const int n4 = len >> 2;
+          for (int j = threadIdx.x; j < n4; j += 4 * kWalkThreads) {
+            float4 v[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int jj = j + q * NT;
-            v[q] = jj < j1 ? __ldcs(p4 + jj) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-          }
+            for (int q = 0; q < 4; ++q) {
+              const int jj = j + q * kWalkThreads;
+              v[q] = jj < n4 ? __ldcg(p4 + jj) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int x = (j + q * NT) << 2;
-            if (v[q].x > bv) { bv = v[q].x; bi = x; }
-            if (v[q].y > bv) { bv = v[q].y; bi = x + 1; }
-            if (v[q].z > bv) { bv = v[q].z; bi = x + 2; }
-            if (v[q].w > bv) { bv = v[q].w; bi = x + 3; }
+            for (int q = 0; q < 4; ++q) {
+              const int x = x0 + ((j + q * kWalkThreads) << 2);
+              if (v[q].x > bv) { bv = v[q].x; bi = x; }
+              if (v[q].y > bv) { bv = v[q].y; bi = x + 1; }
+              if (v[q].z > bv) { bv = v[q].z; bi = x + 2; }
+              if (v[q].w > bv) { bv = v[q].w; bi = x + 3; }
+            }
+          }
+        } else {
+          for (int j = threadIdx.x; j < len; j += kWalkThreads) {
+            const float v = __ldcg(prow + j);
+            if (v > bv) { bv = v; bi = x0 + j; }
           }
         }
-      } else {
-        for (int x = x0 + threadIdx.x; x < x1; x += blockDim.x) {
-          const float v = __ldcs(prow + x);
-          if (v > bv) { bv = v; bi = x; }
-        }
+        cluster_argmax<C>(bv, bi, sh.red, sh.ex, xk, rank, status);
+        if (threadIdx.x == 0) sh.aux[u] = bi == 0x7fffffff ? 0 : bi;
       }
-      cluster_argmax<C>(bv, bi, red, xs, par);
-      cluster_sync_all<C>();  // peers read this CTA's slot
-      if (rank == 0 && threadIdx.x == 0) a.ws_a[(size_t)b * a.n_max + u] = bi == 0x7fffffff ? 0 : bi;
-    } else {
-      // ---- stochastic: row state of node u ----
-      const float* qrow = a.q_probs + (size_t)t * V;
-      const int lenp = (len + 3) & ~3;  // padded to whole float4 (pad = -inf: weight 0)
-      if ((V & 3) == 0) {
-        // one bulk copy of the slice into shared memory
-        if (threadIdx.x == 0) {
-          asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&s_bar)) : "memory");
-          asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&s_bar)),
-                       "r"((uint32_t)(len * 4))
-                       : "memory");
-          asm volatile(
-              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                  smem_addr(D)),
-              "l"(prow + x0), "r"((uint32_t)(len * 4)), "r"(smem_addr(&s_bar))
-              : "memory");
-        }
-        __syncthreads();
-        if (!bulk_wait(&s_bar, 0)) {
-          if (threadIdx.x == 0) atomicOr(&a.status[b], SPEC_DEV_TIMEOUT);
-          bulk_wait(&s_bar, 0);  // drain before the buffer is touched
-        }
-      } else {
-        for (int j = threadIdx.x; j < len; j += blockDim.x) D[j] = __ldcs(prow + x0 + j);
-      }
-      for (int j = len + threadIdx.x; j < lenp; j += blockDim.x) D[j] = -INFINITY;
       __syncthreads();
-      float4* D4 = reinterpret_cast<float4*>(D);
+      // warp 0: the next frontier in increasing index, and the flags
+      if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int cnt = 0;
+        for (int base = 1; base < n; base += 32) {
+          const int c = base + lane;
+          bool is = false;
+          if (c < n) {
+            const int p = sh.par[c];
+            is = inf[p] && sh.tok[c] == sh.aux[p];
+          }
+          const unsigned m = __ballot_sync(0xffffffffu, is);
+          if (is) nx[cnt + __popc(m & ((1u << lane) - 1u))] = c;
+          cnt += __popc(m);
+        }
+        __syncwarp();
+        if (cnt > 0) {
+          for (int i = lane; i < nf; i += 32) inf[fr[i]] = 0;
+          __syncwarp();
+          for (int i = lane; i < cnt; i += 32) inf[nx[i]] = 1;
+        }
+        if (lane == 0) sh.cnt = cnt;
+      }
+      __syncthreads();
+      const int nn = sh.cnt;
+      if (nn == 0) break;
+      int32_t* t = fr;
+      fr = nx;
+      nx = t;
+      nf = nn;
+      ++depth;
+    }
+    if (rank == 0 && threadIdx.x == 0) {
+      int f = fr[0];
+      for (int i = 1; i < nf; ++i) f = min(f, fr[i]);
+      const int L = depth + 1;
+      out_emit[L - 1] = sh.aux[f];
+      for (int i = L - 1, c = f; i >= 0; --i, c = sh.par[c]) {
+        out_path[i] = c;
+        if (i >= 1) out_emit[i - 1] = sh.tok[c];
+      }
+      a.accept_len[b] = L;
+      a.n_emitted[b] = L;
+      sh.flag = L;
+    }
+    __syncthreads();
+    if (rank == 0) {
+      const int L = sh.flag;
+      for (int i = L + threadIdx.x; i < a.n_max; i += kWalkThreads) {
+        out_path[i] = -1;
+        out_emit[i] = -1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ stochastic
+    // Each thread owns a contiguous range [e0, e1) of the slice (whole float4
+    // when vec), so its fixed-point partial sums are prefix-ordered for the
+    // final sample.
+    float4* D4 = reinterpret_cast<float4*>(D);
+    const float4* Q4 = reinterpret_cast<const float4*>(Q);
+    const int per = vec ? 4 * (((len >> 2) + kWalkThreads - 1) / kWalkThreads) : (len + kWalkThreads - 1) / kWalkThreads;
+    const int e0 = min(len, (int)threadIdx.x * per), e1 = min(len, e0 + per);
+    if (threadIdx.x == 0) sh.aux[0] = 0;
+    int u = 0, L = 1;
+    auto load_target = [&](int node) {
+      const float* src = a.p_logits + (size_t)(off + node) * V + x0;
+      if (vec) {
+        if (len > 0) {
+          if (threadIdx.x == 0) start_copy(D, src, (uint32_t)len * 4, &sh.dbar);
+          wait_copy(&sh.dbar, dphase, status);
+        }
+      } else {
+        for (int j = threadIdx.x; j < len; j += kWalkThreads) D[j] = src[j];
+      }
+      __syncthreads();
+    };
+    if (root_copy) wait_copy(&sh.dbar, dphase, status);
+    else if (!vec) load_target(0);
+    __syncthreads();
+    for (;;) {
+      const float* prow = a.p_logits + (size_t)(off + u) * V;
+      const float* qrow = a.q_probs + (size_t)(off + u) * V;
+      // children of u in increasing index; this node's entries at their tokens;
+      // the draft slice (needed from the first rejection on) and an L2 prefetch
+      // of the children's target slices
+      const int k = compact(u + 1, n, [&](int c) { return sh.par[c] == u; }, sh.s.kids, sh);
+      // loads in flight through the max and exp passes, stored before the sum
+      float rx[2], rq[2];
+      uint32_t ru[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int i = threadIdx.x + r * kWalkThreads;
+        if (i < k) {
+          const int c = sh.s.kids[i];
+          const int t = sh.tok[c];
+          rx[r] = __ldcg(prow + t);
+          rq[r] = __ldcg(qrow + t);
+          ru[r] = a.uniforms[off + c].x;
+          if (vec) prefetch_l2(a.p_logits + (size_t)(off + c) * V + x0, (uint32_t)len * 4);
+        }
+      }
+      const uint32_t uterm = threadIdx.x == 0 ? a.uniforms[off + u].y : 0u;
+      const bool qcopy = k > 0 && vec && len > 0;
+      if (qcopy && threadIdx.x == 0) start_copy(Q, qrow + x0, (uint32_t)len * 4, &sh.qbar);
+      bool qready = !qcopy;
+
+      // C4: m = max, e = E(l - m), S_0 = sum FX(e)
       float lmax = -INFINITY;
-      for (int j = threadIdx.x; j < (lenp >> 2); j += blockDim.x) {
-        const float4 v = D4[j];
-        lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+      if (vec) {
+        for (int j = e0 >> 2; j < (e1 >> 2); ++j) {
+          const float4 v = D4[j];
+          lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+        }
+      } else {
+        for (int j = e0; j < e1; ++j) lmax = fmaxf(lmax, D[j]);
       }
-      const float m = cluster_max<C>(lmax, red, xs, par);
-      FxSum acc;
-      for (int j = threadIdx.x; j < (lenp >> 2); j += blockDim.x) {
-        float4 v = D4[j];
-        v.x = canon_exp(__fsub_rn(v.x, m));
-        v.y = canon_exp(__fsub_rn(v.y, m));
-        v.z = canon_exp(__fsub_rn(v.z, m));
-        v.w = canon_exp(__fsub_rn(v.w, m));
-        D4[j] = v;
-        acc.add(v.x);
-        acc.add(v.y);
-        acc.add(v.z);
-        acc.add(v.w);
+      const float m = cluster_max<C>(lmax, sh.red, sh.ex, xk, rank, status);
+      unsigned long long mp;  // this thread's share of S
+      if (vec) {
+        FxSum acc;
+        for (int j = e0 >> 2; j < (e1 >> 2); ++j) {
+          float4 v = D4[j];
+          v.x = canon_exp(__fsub_rn(v.x, m));
+          v.y = canon_exp(__fsub_rn(v.y, m));
+          v.z = canon_exp(__fsub_rn(v.z, m));
+          v.w = canon_exp(__fsub_rn(v.w, m));
+          D4[j] = v;
+          acc.add(v.x);
+          acc.add(v.y);
+          acc.add(v.z);
+          acc.add(v.w);
+        }
+        mp = acc.total();
+      } else {
+        mp = 0;
+        for (int j = e0; j < e1; ++j) {
+          const float e = canon_exp(__fsub_rn(D[j], m));
+          D[j] = e;
+          mp += fx(e);
+        }
       }
-      unsigned long long ls = acc.total();
-      unsigned long long S = cluster_sum<C>(ls, red, xs, par);
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int i = threadIdx.x + r * kWalkThreads;
+        if (i < k) {
+          sh.s.cx[i] = rx[r];
+          sh.s.cq[i] = rq[r];
+          sh.s.cu[i] = ru[r];
+        }
+      }
+      if (threadIdx.x == 0) sh.uterm = uterm;
+      unsigned long long lt;  // this CTA's share of S (the sum publishes the stores above)
+      unsigned long long S = cluster_sum<C>(mp, sh.red, sh.ex, xk, rank, status, lt);
       float Z = z_of(S);
 
-      // children of u in increasing index
-      const int k = collect_children(a.parent + off, n, u, s_kids, &s_cnt, s_wofs);
-
-      int accepted = -1;
-      bool bad_tok = false;
-      bool frozen = false;      // a zero-sum residual froze the state (see below)
-      int nsteps = 0;           // residual steps applied to D
-      unsigned long long lt = ls;  // this CTA's share of S
+      // C5 / C6: children in increasing index, each against the residual left
+      // by the siblings rejected before it
+      int accepted = -1, nsteps = 0;
+      bool frozen = false;  // a zero-sum residual froze the state
       for (int i = 0; i < k; ++i) {
-        const int c = s_kids[i];
-        const int tok = a.tokens[off + c];
-        if (tok < 0 || tok >= V) {
-          bad_tok = true;
-          break;
-        }
-        // r_j(tok) from the CTA of the cluster that holds tok
-        const int owner = tok / a.slice;
-        float dt;
-        if constexpr (C == 1) {
-          dt = D[tok];
-        } else {
-          dt = cg::this_cluster().map_shared_rank(D, owner)[tok - owner * a.slice];
-        }
-        const float rt = __fdiv_rn(dt, Z);
-        const float qt = qrow[tok];
-        const float ua = __fmul_rn((float)(a.uniforms[off + c].x >> 8), 0x1p-24f);
-        if (__fmul_rn(ua, qt) <= rt) {
+        const int c = sh.s.kids[i];
+        // r_j(t) from this node's logit and draft probability at t: the same
+        // operations the slice passes apply to entry t
+        float d = canon_exp(__fsub_rn(sh.s.cx[i], m));
+        for (int s = 0; s < nsteps; ++s) d = resid(d, sh.s.z[s], sh.s.cq[i]);
+        const float rt = __fdiv_rn(d, Z);
+        const float ua = __fmul_rn((float)(sh.s.cu[i] >> 8), 0x1p-24f);
+        if (__fmul_rn(ua, sh.s.cq[i]) <= rt) {
           accepted = c;
           break;
         }
         if (frozen) continue;  // the next residual would be the same all-zero one
-        // rejection: d <- max(d / Z - q, 0) in place, S <- sum FX(d)
-        s_z[nsteps] = Z;
-        cluster_sync_all<C>();  // every CTA has read D[tok] before it changes
-        unsigned long long ln = 0;
-        if ((V & 3) == 0) {
-          const float4* q4 = reinterpret_cast<const float4*>(qrow + x0);
+        if (!qready) {
+          wait_copy(&sh.qbar, qphase, status);
+          qready = true;
+        }
+        if (threadIdx.x == 0) sh.s.z[nsteps] = Z;  // read only after the exchange below
+        unsigned long long np;
+        if (vec) {
           FxSum ra;
-          for (int j = threadIdx.x; j < (len >> 2); j += blockDim.x) {
-            float4 d = D4[j];
-            const float4 qq = __ldg(q4 + j);
-            d.x = resid(d.x, Z, qq.x);
-            d.y = resid(d.y, Z, qq.y);
-            d.z = resid(d.z, Z, qq.z);
-            d.w = resid(d.w, Z, qq.w);
-            D4[j] = d;
-            ra.add(d.x);
-            ra.add(d.y);
-            ra.add(d.z);
-            ra.add(d.w);
+          for (int j = e0 >> 2; j < (e1 >> 2); ++j) {
+            float4 dv = D4[j];
+            const float4 qq = Q4[j];
+            dv.x = resid(dv.x, Z, qq.x);
+            dv.y = resid(dv.y, Z, qq.y);
+            dv.z = resid(dv.z, Z, qq.z);
+            dv.w = resid(dv.w, Z, qq.w);
+            D4[j] = dv;
+            ra.add(dv.x);
+            ra.add(dv.y);
+            ra.add(dv.z);
+            ra.add(dv.w);
           }
-          ln = ra.total();
+          np = ra.total();
         } else {
-          for (int j = threadIdx.x; j < len; j += blockDim.x) {
+          np = 0;
+          for (int j = e0; j < e1; ++j) {
             const float dn = resid(D[j], Z, __ldg(qrow + x0 + j));
             D[j] = dn;
-            ln += fx(dn);
+            np += fx(dn);
           }
         }
-        const unsigned long long Sn = cluster_sum<C>(ln, red, xs, par);  // also publishes D
+        unsigned long long ltn;
+        const unsigned long long Sn = cluster_sum<C>(np, sh.red, sh.ex, xk, rank, status, ltn);
         if (Sn != 0) {
           S = Sn;
           Z = z_of(Sn);
-          lt = ln;
+          lt = ltn;
+          mp = np;
           ++nsteps;
         } else {
           // S_j == 0 (impossible in exact arithmetic after a rejection): the
           // state stays that of step j-1, and so does every later residual.
           // Rebuild step j-1 from the logits: e, then the nsteps earlier steps.
           frozen = true;
-          ls = 0;
-          for (int j = threadIdx.x; j < len; j += blockDim.x) D[j] = canon_exp(__fsub_rn(__ldg(prow + x0 + j), m));
-          for (int j = len + threadIdx.x; j < lenp; j += blockDim.x) D[j] = 0.0f;
-          for (int st2 = 0; st2 < nsteps; ++st2) {
-            __syncthreads();
-            const float Zs = s_z[st2];
-            for (int j = threadIdx.x; j < len; j += blockDim.x) D[j] = resid(D[j], Zs, __ldg(qrow + x0 + j));
+          for (int j = e0; j < e1; ++j) {
+            float e = canon_exp(__fsub_rn(__ldg(prow + x0 + j), m));
+            const float q = vec ? Q[j] : __ldg(qrow + x0 + j);
+            for (int s = 0; s < nsteps; ++s) e = resid(e, sh.s.z[s], q);
+            D[j] = e;
           }
           __syncthreads();
-          for (int j = threadIdx.x; j < len; j += blockDim.x) ls += fx(D[j]);
-          lt = ls;                // this thread's share of S, which is unchanged
-          cluster_sync_all<C>();  // D is read across the cluster by the next test
         }
       }
-      // A CTA may read a peer's shared memory (D[tok]) right before the loop
-      // ends: no CTA of the cluster leaves before every such read is done.
-      cluster_sync_all<C>();
-      if (bad_tok) {
-        if (rank == 0 && threadIdx.x == 0) atomicOr(&a.status[b], SPEC_DEV_BAD_TOKEN);
-      } else if (accepted >= 0) {
-        if (rank == 0 && threadIdx.x == 0) a.ws_a[(size_t)b * a.n_max + u] = accepted;
-      } else {
-        // terminal sample: smallest x whose fixed-point prefix sum exceeds target
-        const unsigned long long target = sample_target(a.uniforms[t].y, S);
-        // this CTA's slice total (kept from the last pass) and the exclusive
-        // prefix of the slices before it
-        lt = block_sum_u64(lt, red);
-        const unsigned long long before = cluster_prefix<C>(lt, xs, par, rank);
-        cluster_sync_all<C>();  // peers read this CTA's slot
-        if (target >= before && target - before < lt) {
-          // the token lies in this slice: per-warp contiguous chunks
-          const unsigned long long tl = target - before;
-          const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-          const int cw = (len + nw - 1) / nw;
-          const int c0 = min(len, w * cw), c1 = min(len, c0 + cw);
-          unsigned long long wsum = 0;
-          for (int j = c0 + lane; j < c1; j += 32) wsum += fx(D[j]);
-          wsum = warp_sum_u64(wsum);
-          __syncthreads();
-          if (lane == 0) red.u[w] = wsum;
-          __syncthreads();
-          if (threadIdx.x == 0) {
-            unsigned long long acc = 0;
-            int ww = 0;
-            for (; ww < nw; ++ww) {
-              if (tl < acc + red.u[ww]) break;
-              acc += red.u[ww];
-            }
-            s_flag = ww;
-            red.u[0] = acc;  // prefix before warp ww (slot reused after the read above)
-          }
-          __syncthreads();
-          const int ww = s_flag;
-          const unsigned long long acc0 = red.u[0];
-          if (w == ww) {
-            const int d0 = min(len, ww * cw), d1 = min(len, d0 + cw);
-            unsigned long long run = acc0;
-            for (int base = d0; base < d1; base += 32) {
-              const int j = base + lane;
-              unsigned long long v = j < d1 ? fx(D[j]) : 0ull;
-              // inclusive warp scan
+      if (!qready) wait_copy(&sh.qbar, qphase, status);  // Q is rewritten at the next node
+      if (accepted >= 0) {
+        if (threadIdx.x == 0) sh.aux[L] = accepted;
+        ++L;
+        u = accepted;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();  // D and Q are no longer read before the copies overwrite them
+        load_target(u);
+        continue;
+      }
+
+      // C7: sample from the current weights: the smallest x whose fixed-point
+      // prefix sum exceeds floor(U * S / 2^32)
+      const unsigned long long target = sample_target(sh.uterm, S);
+      const unsigned long long before = cluster_prefix<C>(lt, sh.ex, xk, rank, status);
+      if (target >= before && target - before < lt) {
+        // the token lies in this slice: exclusive scan of the threads' shares
+        const unsigned long long tl = target - before;
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        unsigned long long incl = mp;
 #pragma unroll
-              for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += y;
-              }
-              const unsigned hit = __ballot_sync(0xffffffffu, j < d1 && run + v > tl);
-              if (hit) {
-                if (lane == __ffs(hit) - 1) {
-                  a.ws_s[(size_t)b * a.n_max + u] = x0 + j;
-                  __threadfence();
-                }
-                break;
-              }
-              run += __shfl_sync(0xffffffffu, v, 31);
-            }
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (lane == 31) sh.wsum[w] = incl;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          unsigned long long acc = 0;
+          for (int q = 0; q < kWarps; ++q) {
+            const unsigned long long x = sh.wsum[q];
+            sh.wsum[q] = acc;
+            acc += x;
           }
         }
-        if (rank == 0 && threadIdx.x == 0) a.ws_a[(size_t)b * a.n_max + u] = -1;
+        __syncthreads();
+        const unsigned long long excl = sh.wsum[w] + incl - mp;
+        if (tl >= excl && tl - excl < mp) {
+          unsigned long long acc = excl;
+          int x = e1 - 1;
+          for (int j = e0; j < e1; ++j) {
+            acc += fx(D[j]);
+            if (acc > tl) {
+              x = j;
+              break;
+            }
+          }
+          out_emit[L - 1] = x0 + x;
+        }
       }
+      break;
     }
-  }
-
-  // ---- ticket: the last CTA of the request runs phase B ----
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int prev = atomicAdd(&a.ws_ticket[b], 1);
-    s_last = prev == n_cta * C - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  const int st = *(volatile int32_t*)&a.status[b];
-  if (!n_ok || st != 0) {
-    clear_request(a, b);
-    return;
-  }
-  int32_t* path = a.path + (size_t)b * a.n_max;
-  int32_t* emit = a.emitted + (size_t)b * a.n_max;
-  if constexpr (MODE == 0) {
-    // greedy: match bit of v = (v is the root) or tokens[v] == argmax(row parent(v));
-    // a node is ok when every ancestor-or-self matches; pick the deepest ok node.
-    const int W = a.W;
-    for (int w = threadIdx.x; w < W; w += blockDim.x) s_match[w] = 0;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) s_kids[i] = __ldcg(&a.ws_a[(size_t)b * a.n_max + i]);
+    // path, emitted tokens of the accepted nodes, lengths, -1 tails
     __syncthreads();
-    for (int v = threadIdx.x; v < n; v += blockDim.x) {
-      const int p = a.parent[off + v];
-      const bool mt = v == 0 || a.tokens[off + v] == s_kids[p];
-      if (mt) atomicOr(reinterpret_cast<unsigned long long*>(&s_match[v >> 6]), 1ull << (v & 63));
-    }
-    __syncthreads();
-    int best = -1;
-    for (int v = threadIdx.x; v < n; v += blockDim.x) {
-      bool ok = true;
-      for (int w = 0; w < W; ++w) ok &= (a.mask[(size_t)(off + v) * W + w] & ~s_match[w]) == 0;
-      if (ok) best = max(best, (a.depth[off + v] << 11) | (2047 - v));
-    }
-    // block max of the key
-    {
-      int v = best;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-      __syncthreads();
-      if ((threadIdx.x & 31) == 0) red.i[threadIdx.x >> 5] = v;
-      __syncthreads();
+    if (rank == 0) {
+      for (int i = threadIdx.x; i < a.n_max; i += kWalkThreads) {
+        if (i < L) {
+          out_path[i] = sh.aux[i];
+          if (i >= 1) out_emit[i - 1] = sh.tok[sh.aux[i]];
+        } else {
+          out_path[i] = -1;
+          out_emit[i] = -1;
+        }
+      }
       if (threadIdx.x == 0) {
-        int m = red.i[0];
-        for (int k2 = 1; k2 < (int)(blockDim.x >> 5); ++k2) m = max(m, red.i[k2]);
-        s_flag = m;
+        a.accept_len[b] = L;
+        a.n_emitted[b] = L;
       }
-      __syncthreads();
-    }
-    const int f = 2047 - (s_flag & 2047);
-    const int L = (s_flag >> 11) + 1;
-    const uint64_t* frow = a.mask + (size_t)(off + f) * W;
-    for (int v = threadIdx.x; v < a.n_max; v += blockDim.x) {
-      if (v < n && ((frow[v >> 6] >> (v & 63)) & 1ull)) {
-        int idx = 0;
-        for (int w = 0; w < (v >> 6); ++w) idx += __popcll(frow[w]);
-        idx += __popcll(frow[v >> 6] & ((1ull << (v & 63)) - 1ull));
-        path[idx] = v;
-        if (idx >= 1) emit[idx - 1] = a.tokens[off + v];
-      }
-      if (v >= L) {
-        path[v] = -1;
-        emit[v] = -1;
-      }
-    }
-    if (threadIdx.x == 0) {
-      emit[L - 1] = s_kids[f];
-      a.accept_len[b] = L;
-      a.n_emitted[b] = L;
-    }
-  } else {
-    // stochastic: follow the accepted-child links from the root
-    for (int i = threadIdx.x; i < n; i += blockDim.x) s_kids[i] = __ldcg(&a.ws_a[(size_t)b * a.n_max + i]);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int v = 0, L = 1;
-      path[0] = 0;
-      while (s_kids[v] > v && L < n) {  // accepted children have larger indices: the walk ends
-        v = s_kids[v];
-        emit[L - 1] = a.tokens[off + v];
-        path[L++] = v;
-      }
-      emit[L - 1] = __ldcg(&a.ws_s[(size_t)b * a.n_max + v]);
-      s_flag = L;
-      a.accept_len[b] = L;
-      a.n_emitted[b] = L;
-    }
-    __syncthreads();
-    for (int i = s_flag + threadIdx.x; i < a.n_max; i += blockDim.x) {
-      path[i] = -1;
-      emit[i] = -1;
     }
   }
-  if (threadIdx.x == 0) a.ws_ticket[b] = 0;
+  // Exchanges push into the receiver, which waits for every value before it
+  // goes on, so no CTA leaves while a peer may still write into it.
 }
 
-inline size_t ws_layout(int B, int n_max, size_t* off_s, size_t* off_t) {
-  const size_t na = (size_t)B * n_max * sizeof(int32_t);
-  *off_s = (na + 255) & ~(size_t)255;
-  *off_t = (*off_s + na + 255) & ~(size_t)255;
-  return *off_t + (size_t)B * sizeof(int32_t);
-}
+// The walk keeps no state in global memory.  The workspace argument stays in
+// the interface (callers size it with spec_verify_workspace_size).
+constexpr size_t kVerifyWorkspace = 256;
 
 template <int MODE, int C>
-cudaError_t launch_verify(const VerifyArgs& a, int B, cudaStream_t stream) {
-  auto kern = verify_kernel<MODE, C>;
-  const size_t dyn = MODE == 1 ? (size_t)((a.slice + 3) & ~3) * sizeof(float) : 0;
+cudaError_t launch_walk(const VerifyArgs& a, int B, cudaStream_t stream) {
+  auto kern = verify_walk_kernel<MODE, C>;
+  const size_t dyn = MODE == 1 ? 2 * (size_t)a.slice * sizeof(float) : 0;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
+  if (C > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(B * C), (unsigned)a.n_max, 1);
-  cfg.blockDim = dim3(VCfg<MODE>::threads, 1, 1);
+  cfg.gridDim = dim3((unsigned)(B * C), 1, 1);
+  cfg.blockDim = dim3(kWalkThreads, 1, 1);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -732,28 +842,72 @@ cudaError_t launch_verify(const VerifyArgs& a, int B, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+// How many 16-CTA clusters of the walk can be resident at once on the
+// current device (queried once per device and mode; 0 if none).
+template <int MODE>
+int clusters16(size_t dyn) {
+  static int cache[2][128];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = cache[MODE][dev];
+  if (c == 0) {
+    auto kern = verify_walk_kernel<MODE, 16>;
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1, 1);
+    cfg.blockDim = dim3(kWalkThreads, 1, 1);
+    cfg.dynamicSmemBytes = dyn;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+                    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) ==
+                        cudaSuccess &&
+                    cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1;
+    cudaGetLastError();
+    c = ok ? n : -1;
+  }
+  return c > 0 ? c : 0;
+}
+
+// Cluster size: about one CTA per SM when the batch is small (at most 16 CTAs
+// per request), and slices that fit shared memory.
+inline int walk_cluster(int B, int V, int mode, bool allow16) {
+  const int cmax = allow16 ? 16 : 8;
+  int C = 1;
+  while (C < cmax && (long long)B * C * 2 <= kTargetCtas) C *= 2;
+  if (mode == 1)
+    while (C < cmax && (V + C - 1) / C > kMaxSlice) C *= 2;
+  return C;
+}
+
 template <int MODE>
 spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  size_t off_s, off_t;
-  const size_t need = ws_layout(B, a.n_max, &off_s, &off_t);
-  if (!workspace || ws_bytes < need) return SPEC_ERR_WORKSPACE;
-  char* ws = static_cast<char*>(workspace);
-  a.ws_a = reinterpret_cast<int32_t*>(ws);
-  a.ws_s = reinterpret_cast<int32_t*>(ws + off_s);
-  a.ws_ticket = reinterpret_cast<int32_t*>(ws + off_t);
-  a.W = (a.n_max + 63) / 64;
-  // cluster size: slices of kSlice entries, at most 8 CTAs (wider slices beyond)
-  constexpr int kSlice = VCfg<MODE>::slice;
-  int C = (a.V + kSlice - 1) / kSlice;
-  C = C <= 1 ? 1 : C <= 2 ? 2 : C <= 4 ? 4 : 8;
+  if (!workspace || ws_bytes < kVerifyWorkspace) return SPEC_ERR_WORKSPACE;
+  int C = walk_cluster(B, a.V, MODE, false);
+  if (C == 8 && walk_cluster(B, a.V, MODE, true) == 16) {
+    // only when every request's cluster is resident at once: a cluster that
+    // waits for another to finish costs more than the wider slices save
+    const int s16 = (((a.V + 15) / 16) + 3) & ~3;
+    if (clusters16<MODE>(MODE == 1 ? 2 * (size_t)s16 * sizeof(float) : 0) >= B) C = 16;
+  }
   a.slice = (((a.V + C - 1) / C) + 3) & ~3;
-  if (cudaMemsetAsync(a.ws_ticket, 0, (size_t)B * sizeof(int32_t), stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (MODE == 1 && a.slice > kMaxSlice) return SPEC_ERR_UNSUPPORTED;
+  a.vec = (a.V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p_logits) & 15) == 0 &&
+          (MODE == 0 || (reinterpret_cast<uintptr_t>(a.q_probs) & 15) == 0);
   cudaError_t e;
   switch (C) {
-    case 1: e = launch_verify<MODE, 1>(a, B, stream); break;
-    case 2: e = launch_verify<MODE, 2>(a, B, stream); break;
-    case 4: e = launch_verify<MODE, 4>(a, B, stream); break;
-    default: e = launch_verify<MODE, 8>(a, B, stream); break;
+    case 1: e = launch_walk<MODE, 1>(a, B, stream); break;
+    case 2: e = launch_walk<MODE, 2>(a, B, stream); break;
+    case 4: e = launch_walk<MODE, 4>(a, B, stream); break;
+    case 8: e = launch_walk<MODE, 8>(a, B, stream); break;
+    default: e = launch_walk<MODE, 16>(a, B, stream); break;
   }
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -764,7 +918,7 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
 // code must not hand the symbol itself to a kernel: it names a host-side
 // stand-in, so the device address is looked up per device.
 // ---------------------------------------------------------------------------
-constexpr size_t kNoAllocBytes = (size_t)2 * 1024 * 1024 + 64 * 1024 + 512;  // B*n_max <= 2^18, B <= 2^14
+constexpr size_t kNoAllocBytes = kVerifyWorkspace;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 static std::mutex g_noalloc_mutex;
@@ -791,10 +945,10 @@ using namespace spectree;
 extern "C" {
 
 size_t spec_verify_workspace_size(int B, int n_max, int V) {
+  (void)B;
+  (void)n_max;
   (void)V;
-  if (B <= 0 || n_max <= 0) return 256;
-  size_t off_s, off_t;
-  return ws_layout(B, n_max, &off_s, &off_t);
+  return kVerifyWorkspace;
 }
 
 static spec_status verify_check(int B, int n_max, int V) {
@@ -804,23 +958,19 @@ static spec_status verify_check(int B, int n_max, int V) {
 }
 
 spec_status spec_tree_verify_greedy(const float* p_logits, const int32_t* tokens, const int32_t* parent,
-                                    const int32_t* tree_off, const uint64_t* mask, const int32_t* depth, int B,
-                                    int n_max, int V, int32_t* path, int32_t* accept_len, int32_t* emitted,
-                                    int32_t* n_emitted, void* workspace, size_t workspace_bytes, int32_t* status,
-                                    void* stream) {
+                                    const int32_t* tree_off, int B, int n_max, int V, int32_t* path,
+                                    int32_t* accept_len, int32_t* emitted, int32_t* n_emitted, void* workspace,
+                                    size_t workspace_bytes, int32_t* status, void* stream) {
   spec_status s = verify_check(B, n_max, V);
   if (s != SPEC_OK) return s;
   if (B == 0 || n_max == 0) return SPEC_OK;
-  if (!p_logits || !tokens || !parent || !tree_off || !mask || !depth || !path || !accept_len || !emitted ||
-      !n_emitted || !status)
+  if (!p_logits || !tokens || !parent || !tree_off || !path || !accept_len || !emitted || !n_emitted || !status)
     return SPEC_ERR_INVALID_ARG;
   VerifyArgs a = {};
   a.p_logits = p_logits;
   a.tokens = tokens;
   a.parent = parent;
   a.tree_off = tree_off;
-  a.mask = mask;
-  a.depth = depth;
   a.n_max = n_max;
   a.V = V;
   a.path = path;
@@ -875,8 +1025,6 @@ spec_status spec_tree_verify_stochastic_noalloc(const float* p_logits, const flo
   if (s != SPEC_OK) return s;
   if (B == 0 || n_max == 0) return SPEC_OK;
   if (B > (1 << 14) || (long long)B * n_max > (1LL << 18)) return SPEC_ERR_UNSUPPORTED;
-  size_t off_s, off_t;
-  if (ws_layout(B, n_max, &off_s, &off_t) > kNoAllocBytes) return SPEC_ERR_UNSUPPORTED;
   void* ws = noalloc_scratch();
   if (!ws) return SPEC_ERR_CUDA;
   return spec_tree_verify_stochastic(p_logits, q_probs, tokens, parent, tree_off, uniforms, B, n_max, V, path,

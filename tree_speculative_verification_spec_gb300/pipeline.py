@@ -89,8 +89,7 @@ class VerifyPass:
     def verify(self, mode="stochastic", stream=None):
         b = self.batch
         if mode == "greedy":
-            S.spec_tree_verify_greedy(b.p_logits, b.tokens, b.parent, b.tree_off, self.mask, self.depth, b.B,
-                                      b.n_max, b.V, self.path, self.accept_len, self.emitted, self.n_emitted,
+            S.spec_tree_verify_greedy(b.p_logits, b.tokens, b.parent, b.tree_off, b.B, b.n_max, b.V, self.path, self.accept_len, self.emitted, self.n_emitted,
                                       self.verify_ws, self.status, stream)
         else:
             S.spec_tree_verify_stochastic(b.p_logits, b.q_probs, b.tokens, b.parent, b.tree_off, b.uniforms, b.B,
