@@ -307,42 +307,56 @@ def bench_gpu(args):
         passes.append(VerifyPass(d))
     torch.cuda.synchronize()
 
-    def step(vp, evs=None, stream=None):
-        marks = [] if evs is None else evs
-        if marks:
-            rt.record_external(marks[0], stream)
-        vp.mask_build()
-        if marks:
-            rt.record_external(marks[1], stream)
-        vp.attention(args.attn_flags)
-        if marks:
-            rt.record_external(marks[2], stream)
-        vp.verify(args.mode)
-        if marks:
-            rt.record_external(marks[3], stream)
-        vp.commit()
-        if marks:
-            rt.record_external(marks[4], stream)
+    def step(vp, ev=None, stream=None):
+        """One pass; ev maps a stage name to its (before, after) events."""
+        for name, fn in (("mask", vp.mask_build), ("attention", lambda: vp.attention(args.attn_flags)),
+                         ("verify", lambda: vp.verify(args.mode)), ("commit", vp.commit)):
+            if ev and name in ev:
+                rt.record_external(ev[name][0], stream)
+            fn()
+            if ev and name in ev:
+                rt.record_external(ev[name][1], stream)
 
     # eager warm-up (first calls set kernel attributes and look up driver entry points)
     for i in range(args.warmup):
         step(passes[i % N_SETS])
     torch.cuda.synchronize()
 
-    # one CUDA graph per (input set, copy); each carries its own stage events
-    cap = torch.cuda.Stream(dev)
-    graphs, gevs = [], []
-    copies = 4
-    for c in range(copies):
-        for i in range(N_SETS):
-            evs = [rt.event() for _ in range(5)]
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cap):
-                step(passes[i], evs, torch.cuda.current_stream(dev))
-            graphs.append(g)
-            gevs.append(evs)
-    torch.cuda.synchronize()
+    def capture(stages, copies):
+        """CUDA graphs of one pass per (copy, input set), with events around
+        the given stages."""
+        cap = torch.cuda.Stream(dev)
+        gs, es = [], []
+        for c in range(copies):
+            for i in range(N_SETS):
+                ev = {k: (rt.event(), rt.event()) for k in stages}
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    step(passes[i], ev, torch.cuda.current_stream(dev))
+                gs.append(g)
+                es.append(ev)
+        torch.cuda.synchronize()
+        return gs, es
+
     stream = torch.cuda.current_stream(dev)
+    all_stages = ("mask", "attention", "verify", "commit")
+    # every stage timed in instrumented replays outside the timed region; they
+    # pick the dominant kernel
+    igraphs, ievs = capture(all_stages, 1)
+    for r in range(max(args.warmup, 3)):
+        for g in igraphs:
+            g.replay()
+    torch.cuda.synchronize()
+    stage = {k: [] for k in all_stages}
+    for r in range(3):
+        for g, ev in zip(igraphs, ievs):
+            g.replay()
+            torch.cuda.synchronize()
+            for k in all_stages:
+                stage[k].append(rt.elapsed_ms(*ev[k]))
+    dom = max(("attention", "verify"), key=lambda k: statistics.mean(stage[k]))
+    # the timed graphs carry events around the dominant kernel only
+    graphs, gevs = capture((dom,), 4)
     for i in range(args.warmup):
         graphs[i % len(graphs)].replay()
     torch.cuda.synchronize()
@@ -359,12 +373,9 @@ def bench_gpu(args):
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    # stage times of the last replay of every graph (inside the timed region)
-    stage = {k: [] for k in ("mask", "attention", "verify", "commit")}
-    for gi in range(min(len(graphs), args.steps)):
-        e = gevs[gi]
-        for j, k in enumerate(stage):
-            stage[k].append(rt.elapsed_ms(e[j], e[j + 1]))
+    # the dominant kernel's time: last replay of every timed graph (inside the
+    # timed region)
+    stage[dom] = [rt.elapsed_ms(*gevs[gi][dom]) for gi in range(min(len(graphs), args.steps))]
 
     # emitted tokens per step (verify inputs do not change between steps of one set)
     tokens_per_set = [int(p.n_emitted[:p.batch.B].sum()) for p in passes]
@@ -384,7 +395,6 @@ def bench_gpu(args):
     stats = _tree_stats(w0, passes[0].path[:w0.B].tolist())
     algo = algorithmic_bytes(w0, stats, args.mode)
     avg = {k: statistics.mean(v) for k, v in stage.items()}
-    dom = max(("attention", "verify"), key=lambda k: avg[k])
     kernels = {k: {"ms": avg[k], "bytes": algo[k], "gbs": algo[k] / (avg[k] * 1e-3) / 1e9,
                    "frac_hbm": algo[k] / (avg[k] * 1e-3) / 1e9 / peak} for k in avg}
     achieved = kernels[dom]["gbs"]
@@ -397,6 +407,8 @@ def bench_gpu(args):
             "config": {"workload": WORKLOAD, "verify": args.mode, "input_sets": N_SETS,
                        "l2": "3 rotating input sets of ~205 MB each (inputs larger than L2)",
                        "launch": "one CUDA graph per step (the five C-ABI calls captured)",
+                       "kernel_timing": "dominant kernel: CUDA events inside the timed graphs; other stages: "
+                                        "instrumented replays of the same graphs outside the timed region",
                        "tokens_per_step": tokens / args.steps / max(world, 1), "status_ok": status_ok,
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "clocks": clk.summary(),

@@ -6,26 +6,30 @@
 // query head) pairs of one kv-head group, so the K/V stream of the group is
 // shared by all its query heads (GQA) and all its tree nodes.  Per 128-key
 // tile j of the CTA's key range:
-//   S_j = Q K_j^T            tcgen05.mma, A = Q (smem), B = K tile (smem), D in TMEM
-//   P_j = exp2(S_j*c - m)    softmax warps: TMEM -> registers -> bf16 P (smem);
-//                            the ancestor bitmask is applied only on tiles that
+//   S_j = Q K_j^T            tcgen05.mma, A = Q (smem), B = K tile (smem), D in
+//                            tensor-memory slot j % 3
+//   P_j = exp2(S_j*c - m)    softmax warps: TMEM -> registers -> bf16 P written
+//                            back over the first half of S_j's slot; the
+//                            ancestor bitmask is applied only on tiles that
 //                            reach past the prefix
-//   O  += P_j V_j            tcgen05.mma, A = P (smem), B = V tile (smem, MN-major)
+//   O  += P_j V_j            tcgen05.mma, A = P (tensor memory), B = V tile
+//                            (smem, MN-major)
 // K and V tiles arrive by TMA (2-D tensor maps over the paged cache, one box
-// per page or per 128 rows), 128-byte swizzled, into two-stage rings.  S is
-// double-buffered in TMEM so S_{j+1} runs on the tensor core while the
-// softmax warps work on S_j.  O is rescaled only when a row maximum grows by
-// more than 2^8 (the stale maximum is exact for the final normalisation);
-// the rescale happens while the P buffer is anyway waiting for PV_{j-1}.
+// per page or per 128 rows), 128-byte swizzled, into a three-stage K ring and
+// a two-stage V ring.  Three S slots let the tensor core run QK_{j+1} and
+// QK_{j+2} while the softmax works on tile j, and P never leaves tensor
+// memory, so the softmax of consecutive tiles runs back to back.  O is
+// rescaled only when a row maximum grows by more than 2^8 (the stale maximum
+// is exact for the final normalisation), between PV_{j-1} and PV_j.
 //
-// Warp roles (384 threads): warp 0 issues TMA from the start, warp 1 issues
-// MMAs and owns the TMEM allocation, warps 2-11 stage the Q tile, warps 4-11
-// run softmax and the epilogue: two threads per accumulator row (row r ==
-// TMEM lane r, the warp's lane quadrant), each owning one 64-column half of
-// S, P and O; their row maxima meet through shared memory and a 64-thread
-// mbarrier per lane quadrant.  Every mbarrier wait is bounded: on
-// expiry the CTA records SPEC_DEV_TIMEOUT, drains its own copies and MMAs,
-// frees TMEM and returns.
+// Warp roles (384 threads): warp 0 issues the K loads from the start, warp 1
+// issues MMAs and owns the TMEM allocation, warps 2-11 stage the Q tile, then
+// warp 3 issues the V loads and warps 4-11 run softmax and the epilogue: two
+// threads per accumulator row (row r == TMEM lane r, the warp's lane
+// quadrant), each owning one 64-column half of S and O; their row maxima meet
+// through shared memory and a 64-thread mbarrier per lane quadrant.  Every
+// mbarrier wait is bounded: on expiry the CTA records SPEC_DEV_TIMEOUT, drains
+// its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 
 #include "attention.cuh"
@@ -36,7 +40,7 @@ namespace tc {
 
 constexpr int BM = 128;       // rows per CTA (M of the MMA)
 constexpr int BN = 128;       // keys per tile
-constexpr int kThreads = 384;        // warp 0 TMA, warp 1 MMA, warps 2-11 Q load, warps 4-11 softmax
+constexpr int kThreads = 384;        // warp 0 K loads, 1 MMA, 2-11 Q load, then 3 V loads, 4-11 softmax
 constexpr int kSoftmaxThreads = 256;  // two threads per accumulator row
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 25;  // bounded mbarrier polls
@@ -97,6 +101,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// A operand from tensor memory (lane = row, two bf16 per 32-bit column along K).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -154,15 +168,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& ra, float
 
 template <int D>
 struct Layout {
-  static constexpr int DH = D / 64;                 // 128-byte halves of a row
-  static constexpr uint32_t kQ = BM * D * 2;        // Q tile bytes
-  static constexpr uint32_t kKV = BN * D * 2;       // one K (or V) stage
-  static constexpr uint32_t kP = BM * BN * 2;       // P tile
+  static constexpr int DH = D / 64;           // 128-byte halves of a row
+  static constexpr int KST = 2;               // K stages (QK runs up to three tiles ahead of PV)
+  static constexpr int VST = 3;               // V stages (a V stage frees only when its PV completes)
+  static constexpr uint32_t kQ = BM * D * 2;  // Q tile bytes
+  static constexpr uint32_t kKV = BN * D * 2; // one K (or V) stage
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kQ;
-  static constexpr uint32_t kOffV = kQ + 2 * kKV;
-  static constexpr uint32_t kOffP = kQ + 4 * kKV;
-  static constexpr uint32_t kBytes = kOffP + kP;
+  static constexpr uint32_t kOffV = kQ + KST * kKV;
+  static constexpr uint32_t kBytes = kOffV + VST * kKV;
   // one CTA per SM: TMEM is allocated whole (512 columns)
   static constexpr uint32_t kDyn = (kBytes + 1024 < 120 * 1024 ? 120 * 1024 : kBytes + 1024);
 };
@@ -173,6 +187,29 @@ struct TcParams {
   long long rows_total;  // num_blocks * Hkv * block_size (rows of the 2-D cache view)
 };
 
+// TMA of one K or V tile (keys k0 .. k0+BN-1 of kv-head kvh) into dst, one
+// box per page (or per 128 rows); rows past the key range or at a bad block
+// id read the out-of-range row `rows_total` (zero fill).
+template <int D>
+__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap* map, const TcParams& prm, int b,
+                                             int kvh, int k0, int Lk, uint64_t* full, int* bad_block) {
+  const AttnArgs& a = prm.a;
+  const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
+  const int bs = a.block_size, br = prm.box_rows;
+  mbar_expect_tx(full, Layout<D>::kKV);
+  for (int i = 0; i < BN / br; ++i) {
+    const int k = k0 + i * br;
+    int y = (int)prm.rows_total;
+    if (k < Lk) {
+      const int blk = bt[k / bs];
+      if (blk >= 0 && blk < a.num_blocks) y = (int)(((long long)blk * a.Hkv + kvh) * bs + (k % bs));
+      else *bad_block = 1;
+    }
+#pragma unroll
+    for (int h = 0; h < Layout<D>::DH; ++h) tma_load_2d(dst + h * (BN * 128) + i * br * 128, map, h * 64, y, full);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -180,9 +217,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L_ = Layout<D>;
   constexpr int HC = BN / 2;        // score columns per softmax thread
   constexpr int OC = D / 2;         // output columns per softmax thread
+  constexpr int KST = L_::KST, VST = L_::VST;
   const AttnArgs& a = prm.a;
   extern __shared__ uint8_t dyn_raw[];
-  __shared__ uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full, pv_done, q_full,
+  __shared__ uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[3], p_full[3], pv_done[3], q_full,
       drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag, bad_block;
@@ -215,16 +253,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < KST; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < VST; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kSoftmaxThreads);
     }
-    mbar_init(&p_full, kSoftmaxThreads);
-    mbar_init(&pv_done, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], kSoftmaxThreads);
+      mbar_init(&pv_done[i], 1);
+    }
     mbar_init(&q_full, kThreads - 64);
     mbar_init(&drain, 1);
     for (int i = 0; i < 4; ++i) {
@@ -246,97 +287,77 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 256;
+  const uint32_t tS = tmem, tO = tmem + 3 * BN;  // S / P slots 0..2 at 0, 128, 256; O at 384
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ---------------------------------------------------------- K producer
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
-      const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
-      const int bs = a.block_size, br = prm.box_rows;
-      const int nbox = BN / br;
-      int issued = 0;
-      bool ok = true;
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int st = j & 1;
-        const int k0 = k_begin + j * BN;
-        for (int kv = 0; kv < 2 && ok; ++kv) {
-          uint64_t* full = kv == 0 ? &k_full[st] : &v_full[st];
-          uint64_t* empty = kv == 0 ? &k_empty[st] : &v_empty[st];
-          if (j >= 2 && !mbar_wait(empty, ((j >> 1) - 1) & 1, &abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(full, L_::kKV);
-          const CUtensorMap* map = kv == 0 ? &tmap_k : &tmap_v;
-          const uint32_t dst0 = sbase + (kv == 0 ? L_::kOffK : L_::kOffV) + st * L_::kKV;
-          for (int i = 0; i < nbox; ++i) {
-            const int k = k0 + i * br;
-            int y = (int)prm.rows_total;  // out of range: zero fill
-            if (k < Lk) {
-              const int blk = bt[k / bs];
-              if (blk >= 0 && blk < a.num_blocks) y = (int)(((long long)blk * a.Hkv + kvh) * bs + (k % bs));
-              else bad_block = 1;
-            }
-#pragma unroll
-            for (int h = 0; h < L_::DH; ++h) tma_load_2d(dst0 + h * (BN * 128) + i * br * 128, map, h * 64, y, full);
-          }
-        }
-        if (ok) issued = j + 1;
+      // the first K and V tiles go out at once (their stages are free); warp 3
+      // issues the later V tiles once it has staged its part of Q
+      for (int j = 0; j < min(KST, ntiles); ++j)
+        load_kv_tile<D>(sbase + L_::kOffK + j * L_::kKV, &tmap_k, prm, b, kvh, k_begin + j * BN, Lk, &k_full[j],
+                        &bad_block);
+      for (int j = 0; j < min(VST, ntiles); ++j)
+        load_kv_tile<D>(sbase + L_::kOffV + j * L_::kKV, &tmap_v, prm, b, kvh, k_begin + j * BN, Lk, &v_full[j],
+                        &bad_block);
+      int issued = min(KST, ntiles);
+      for (int j = issued; j < ntiles; ++j) {
+        const int st = j % KST;
+        if (j >= KST && !mbar_wait(&k_empty[st], (j / KST - 1) & 1, &abort_flag)) break;
+        load_kv_tile<D>(sbase + L_::kOffK + st * L_::kKV, &tmap_k, prm, b, kvh, k_begin + j * BN, Lk, &k_full[st],
+                        &bad_block);
+        issued = j + 1;
       }
       // drain: every issued load has landed before the CTA can exit
-      for (int j = max(0, issued - 2); j < issued; ++j) {
-        mbar_wait(&k_full[j & 1], (j >> 1) & 1, &abort_flag);
-        mbar_wait(&v_full[j & 1], (j >> 1) & 1, &abort_flag);
-      }
+      for (int j = max(0, issued - KST); j < issued; ++j) mbar_wait(&k_full[j % KST], (j / KST) & 1, &abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // S_j = Q K_j^T into slot j % 3; P_j (bf16) overwrites the first half of
+    // that slot; O += P_j V_j reads A from tensor memory.  Issue order:
+    // QK_0 QK_1 QK_2, then PV_j followed by QK_{j+3} (which reuses P_j's slot;
+    // the tensor pipe executes them in issue order).
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(D, 1);
-      const uint32_t qaddr = sbase + L_::kOffQ, paddr = sbase + L_::kOffP;
+      const uint32_t qaddr = sbase + L_::kOffQ;
       bool ok = mbar_wait(&q_full, 0, &abort_flag);
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&p_full, i & 1, &abort_flag)) return false;
-        if (!mbar_wait(&v_full[i & 1], (i >> 1) & 1, &abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t vaddr = sbase + L_::kOffV + (i & 1) * L_::kKV;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(paddr + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(vaddr + kk * 2048, BN * 128, 1024);
-          umma_bf16(tO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&pv_done);
-        umma_commit(&v_empty[i & 1]);
-        return true;
-      };
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&k_full[st], (j >> 1) & 1, &abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (j >= 2 && !mbar_wait(&s_free[st], ((j >> 1) - 1) & 1, &abort_flag)) {
-          ok = false;
-          break;
-        }
+      auto issue_qk = [&](int j) -> bool {
+        const int st = j % KST;
+        if (!mbar_wait(&k_full[st], (j / KST) & 1, &abort_flag)) return false;
         tc_fence_after();
         const uint32_t kaddr = sbase + L_::kOffK + st * L_::kKV;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
           const uint32_t ob = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-          umma_bf16(tS + st * BN, smem_desc_sw128(qaddr + o, 16, 1024), smem_desc_sw128(kaddr + ob, 16, 1024),
+          umma_bf16(tS + (j % 3) * BN, smem_desc_sw128(qaddr + o, 16, 1024), smem_desc_sw128(kaddr + ob, 16, 1024),
                     idesc_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[st]);
+        umma_commit(&s_full[j % 3]);
         umma_commit(&k_empty[st]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        return true;
+      };
+      for (int j = 0; j < min(3, ntiles) && ok; ++j) ok = issue_qk(j);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        if (!mbar_wait(&p_full[j % 3], (j / 3) & 1, &abort_flag) ||
+            !mbar_wait(&v_full[j % VST], (j / VST) & 1, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vaddr = sbase + L_::kOffV + (j % VST) * L_::kKV;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = smem_desc_sw128(vaddr + kk * 2048, BN * 128, 1024);
+          umma_bf16_ts(tO, tS + (j % 3) * BN + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&pv_done[j % 3]);
+        umma_commit(&v_empty[j % VST]);
+        if (j + 3 < ntiles) ok = issue_qk(j + 3);
       }
-      if (ok) issue_pv(ntiles - 1);
       // drain: every issued MMA has completed before TMEM is freed
       umma_commit(&drain);
       mbar_wait(&drain, 0, &abort_flag);
@@ -372,7 +393,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       mbar_arrive(&q_full);
     }
-    if (warp >= 4) {
+    if (warp == 3) {
+      // ------------------------------------------------------- V producer
+      if (lane == 0) {
+        int issued = min(VST, ntiles);
+        for (int j = issued; j < ntiles; ++j) {
+          const int st = j % VST;
+          if (j >= VST && !mbar_wait(&v_empty[st], (j / VST - 1) & 1, &abort_flag)) break;
+          load_kv_tile<D>(sbase + L_::kOffV + st * L_::kKV, &tmap_v, prm, b, kvh, k_begin + j * BN, Lk, &v_full[st],
+                          &bad_block);
+          issued = j + 1;
+        }
+        for (int j = max(0, issued - VST); j < issued; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, &abort_flag);
+      }
+    } else if (warp >= 4) {
       // -------------------------------------------------- softmax + epilogue
       // two threads per accumulator row: column half `half` of S, P and O
       const int quad = warp & 3, half = (warp - 4) >> 2;
@@ -391,10 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         return __all_sync(0xffffffffu, w);
       };
       for (int j = 0; j < ntiles && ok; ++j) {
-        const int st = j & 1;
+        const uint32_t sl = tS + (j % 3) * BN;  // this tile's S / P slot
         const int k0 = k_begin + j * BN;
         const int c0 = k0 + half * HC;  // first key of this thread's columns
-        if (!wait_warp(&s_full[st], (j >> 1) & 1)) {
+        if (!wait_warp(&s_full[j % 3], (j / 3) & 1)) {
           ok = false;
           break;
         }
@@ -403,36 +437,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < HC / 32; ++c) {
           uint32_t v[32];
-          tmem_ld32(tS + st * BN + half * HC + c * 32 + lane_off, v);
+          tmem_ld32(sl + half * HC + c * 32 + lane_off, v);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]) * c2;
         }
-        tc_fence_before();
-        mbar_arrive(&s_free[st]);
 
         // visibility: the tile reaches past the prefix (tree tail) or the range end
         const bool plain = (c0 + HC <= k_end) && (c0 + HC <= P);
         if (!plain) {
-#pragma unroll
-          for (int c = 0; c < HC / 32; ++c) {
-            uint32_t vis = 0;
-            for (int e = 0; e < 32; ++e) {
-              const int k = c0 + c * 32 + e;
-              bool vk = k < k_end;
-              if (vk && k >= P) vk = (mrow[(k - P) >> 6] >> ((k - P) & 63)) & 1ull;
-              vis |= (uint32_t)vk << e;
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (!((vis >> e) & 1u)) x[c * 32 + e] = -INFINITY;
+          // bit e of vis: key c0 + e is visible (in range, and a prefix key or
+          // an ancestor-or-self tree node); the tree bits come from at most two
+          // mask words
+          const int i0 = c0 - P;               // tree index of key c0 (may be < 0)
+          const int lo = i0 > 0 ? i0 : 0;      // first tree index among the 64 keys
+          uint64_t win = 0;                    // bit t: tree node lo + t
+          if (lo < a.W * 64) {
+            const int w = lo >> 6, sh = lo & 63;
+            win = mrow[w] >> sh;
+            if (sh != 0 && w + 1 < a.W) win |= mrow[w + 1] << (64 - sh);
           }
+          const int pre = lo - i0;             // keys before the tree: always visible
+          uint64_t vis = pre >= 64 ? ~0ull : ((win << pre) | ((1ull << pre) - 1ull));
+          const int inr = k_end - c0;          // keys below the range end
+          if (inr < 64) vis &= inr <= 0 ? 0ull : ((1ull << inr) - 1ull);
+#pragma unroll
+          for (int e = 0; e < HC; ++e)
+            if (!((vis >> e) & 1ull)) x[e] = -INFINITY;
         }
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int e = 0; e < HC; ++e) mx[e & 3] = fmaxf(mx[e & 3], x[e]);
         float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        // combine with the partner thread (same row, other column half)
+        // combine with the partner thread (same row, other column half); after
+        // this exchange both halves have read S_j, so P_j may overwrite it
         xchg[j & 1][half][r] = mloc;
         mbar_arrive(&xbar[j & 1][quad]);
         if (!wait_warp(&xbar[j & 1][quad], (j >> 1) & 1)) {
@@ -450,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 4; ++i) lpart[i] *= factor;
           m_used = mtile;
         }
-        // P (bf16) for this thread's 64 columns; sums from the fp32 values
+        // P (bf16) for this thread's 64 keys, packed in pairs: key k of the tile
+        // at column k / 2 of the slot; sums from the fp32 values
         uint32_t pk[HC / 2];
         const float mneg = -m_used;
 #pragma unroll
@@ -464,58 +503,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        if (j >= 1) {
-          if (!wait_warp(&pv_done, (j - 1) & 1)) {
+        // O holds PV_{j-1} once that MMA completes; PV_j waits for this tile's P
+        if (__any_sync(0xffffffffu, rescale)) {
+          if (!wait_warp(&pv_done[(j - 1) % 3], ((j - 1) / 3) & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, rescale)) {
-            const float f = rescale ? factor : 1.0f;
+          const float f = rescale ? factor : 1.0f;
 #pragma unroll
-            for (int c = 0; c < OC / 32; ++c) {
-              uint32_t v[32];
-              tmem_ld32(tO + half * OC + c * 32 + lane_off, v);
-              tmem_wait_ld();
+          for (int c = 0; c < OC / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tO + half * OC + c * 32 + lane_off, v);
+            tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
-              tmem_st32(tO + half * OC + c * 32 + lane_off, v);
-            }
-            tmem_wait_st();
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
+            tmem_st32(tO + half * OC + c * 32 + lane_off, v);
           }
         }
         // a tile reaching past the key range: zero its V rows there (no stale
         // values, possibly non-finite, may meet a zero probability)
         if (k0 + BN > k_end) {
-          if (!wait_warp(&v_full[st], (j >> 1) & 1)) {
+          if (!wait_warp(&v_full[j % VST], (j / VST) & 1)) {
             ok = false;
             break;
           }
           const int zr = k_end - k0;
-          uint8_t* vst = smem + L_::kOffV + st * L_::kKV;
+          uint8_t* vst = smem + L_::kOffV + (j % VST) * L_::kKV;
           const int sidx = threadIdx.x - 128;
           for (int idx = sidx; idx < (BN - zr) * L_::DH * 8; idx += kSoftmaxThreads) {
             const int rr = zr + idx / (L_::DH * 8), rest = idx % (L_::DH * 8);
             *reinterpret_cast<uint4*>(vst + (rest >> 3) * (BN * 128) + rr * 128 + ((rest & 7) << 4)) =
                 make_uint4(0, 0, 0, 0);
           }
+          fence_async_smem();
         }
-        // P half `half` holds keys [64*half, 64*half + 64): 8 swizzled 16-byte chunks
-        uint8_t* prow = smem + L_::kOffP + half * (BM * 128) + r * 128;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
-              make_uint4(pk[cc * 4], pk[cc * 4 + 1], pk[cc * 4 + 2], pk[cc * 4 + 3]);
-        fence_async_smem();
+        tmem_st32(sl + half * (HC / 2) + lane_off, pk);
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full);
+        mbar_arrive(&p_full[j % 3]);
       }
       // epilogue: this thread's half of the O row
       lfin[half][r] = (lpart[0] + lpart[1]) + (lpart[2] + lpart[3]);
       mbar_arrive(&lbar[quad]);
       ok = ok && wait_warp(&lbar[quad], 0);
       const float lsum = lfin[0][r] + lfin[1][r];
-      if (ok && wait_warp(&pv_done, (ntiles - 1) & 1)) {
+      if (ok && wait_warp(&pv_done[(ntiles - 1) % 3], ((ntiles - 1) / 3) & 1)) {
         tc_fence_after();
         const size_t orow = (size_t)t * a.Hq + kvh * g + (valid ? row % g : 0);
         const float inv = 1.0f / lsum;

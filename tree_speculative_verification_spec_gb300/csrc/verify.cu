@@ -24,7 +24,7 @@
 namespace spectree {
 
 constexpr int kWalkThreads = 512;
-constexpr int kMaxSlice = 20480;  // stochastic: floats of one CTA's slice (target and draft: 160 KB)
+constexpr int kMaxSlice = 16384;  // stochastic: floats of one CTA's slice (target, two draft: 192 KB)
 constexpr int kMaxCluster = 16;   // 16 needs the non-portable cluster size
 constexpr int kTargetCtas = 152;  // one CTA per SM when the batch is small
 
@@ -110,6 +110,29 @@ __device__ __forceinline__ unsigned long long sample_target(uint32_t U, unsigned
 // the division: +0 / Z is +0 for the finite positive Z, the same value.
 __device__ __forceinline__ float resid(float d, float Z, float q) {
   const float r = d == 0.0f ? 0.0f : __fdiv_rn(d, Z);
+  const float diff = __fsub_rn(r, q);
+  return diff > 0.0f ? diff : 0.0f;
+}
+
+// d / Z rounded to nearest even for the weights of a residual pass, by
+// Markstein's division theorem: with y = RN(1/Z) and q = RN(d * y), the
+// remainder r = d - q * Z is exact in one FMA and RN(q + r * y) = RN(d / Z),
+// as long as nothing underflows or overflows.  Here Z in [2^-46, 2^17] and the
+// fast path takes d in [2^-100, 1], so every quantity is a normal number;
+// other d take the IEEE division.  Bit-identical to resid().
+__device__ __noinline__ float div_ieee(float d, float Z) { return __fdiv_rn(d, Z); }
+
+__device__ __forceinline__ float resid_y(float d, float Z, float y, float q) {
+  float r;
+  if (d >= 0x1p-100f && d <= 1.0f) {
+    const float q0 = __fmul_rn(d, y);
+    const float rem = fmaf(-q0, Z, d);
+    r = fmaf(rem, y, q0);
+  } else if (d == 0.0f) {
+    r = 0.0f;
+  } else {
+    r = div_ieee(d, Z);  // a call: never evaluated speculatively
+  }
   const float diff = __fsub_rn(r, q);
   return diff > 0.0f ? diff : 0.0f;
 }
@@ -307,7 +330,7 @@ struct VerifyArgs {
 struct WalkShared {
   Red red;
   Exch ex;
-  uint64_t dbar, qbar;          // stochastic: slice copies of the target and draft rows
+  uint64_t dbar, qbar[2];       // stochastic: slice copies of the target and draft rows
   int32_t par[SPEC_MAX_NODES];  // the request's parent array
   int32_t tok[SPEC_MAX_NODES];  // the request's tokens
   int32_t aux[SPEC_MAX_NODES];  // greedy: argmax of frontier nodes; stochastic: the path
@@ -378,6 +401,14 @@ __device__ __forceinline__ void wait_copy(uint64_t* bar, uint32_t& phase, int32_
   phase ^= 1u;
 }
 
+// Wait for the draft copy into buffer i (bit i of the phase and pending masks).
+__device__ __forceinline__ void wait_draft(WalkShared& sh, int i, uint32_t& phase, uint32_t& pend, int32_t* status) {
+  uint32_t p = (phase >> i) & 1u;
+  wait_copy(&sh.qbar[i], p, status);
+  phase ^= 1u << i;
+  pend &= ~(1u << i);
+}
+
 __device__ void clear_request(const VerifyArgs& a, int b) {
   for (int i = threadIdx.x; i < a.n_max; i += kWalkThreads) {
     a.path[(size_t)b * a.n_max + i] = -1;
@@ -413,14 +444,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
 
   // stochastic: the root's target slice is copied while the inputs are checked
   float* D = reinterpret_cast<float*>(dyn_smem);  // current weights of this CTA's slice
-  float* Q = D + a.slice;                          // this node's draft slice
-  uint32_t dphase = 0, qphase = 0;
+  float* Qb = D + a.slice;                         // draft slices, alternating per node
+  uint32_t dphase = 0;
+  uint32_t qphase = 0, qpend = 0;  // per draft buffer i (bit i): phase, copy not yet waited for
   const bool root_copy = MODE == 1 && may_run && vec && len > 0;
   if (threadIdx.x == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.ex.bar[0])) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.ex.bar[1])) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.dbar)) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.qbar)) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.qbar[0])) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.qbar[1])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (root_copy) start_copy(D, a.p_logits + (size_t)off * V + x0, (uint32_t)len * 4, &sh.dbar);
     else if (MODE == 0 && may_run && vec) prefetch_l2(a.p_logits + (size_t)off * V + x0, (uint32_t)len * 4);
@@ -574,7 +607,6 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
     // when vec), so its fixed-point partial sums are prefix-ordered for the
     // final sample.
     float4* D4 = reinterpret_cast<float4*>(D);
-    const float4* Q4 = reinterpret_cast<const float4*>(Q);
     const int per = vec ? 4 * (((len >> 2) + kWalkThreads - 1) / kWalkThreads) : (len + kWalkThreads - 1) / kWalkThreads;
     const int e0 = min(len, (int)threadIdx.x * per), e1 = min(len, e0 + per);
     if (threadIdx.x == 0) sh.aux[0] = 0;
@@ -617,9 +649,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         }
       }
       const uint32_t uterm = threadIdx.x == 0 ? a.uniforms[off + u].y : 0u;
-      const bool qcopy = k > 0 && vec && len > 0;
-      if (qcopy && threadIdx.x == 0) start_copy(Q, qrow + x0, (uint32_t)len * 4, &sh.qbar);
-      bool qready = !qcopy;
+      // the draft slice into the buffer of this node's parity; its previous copy
+      // (two nodes back) was waited for here or at a rejection
+      const int qb = (L - 1) & 1;
+      float* Q = Qb + qb * a.slice;
+      const float4* Q4 = reinterpret_cast<const float4*>(Q);
+      if (qpend & (1u << qb)) wait_draft(sh, qb, qphase, qpend, status);
+      if (k > 0 && vec && len > 0) {
+        if (threadIdx.x == 0) start_copy(Q, qrow + x0, (uint32_t)len * 4, &sh.qbar[qb]);
+        qpend |= 1u << qb;
+      }
 
       // C4: m = max, e = E(l - m), S_0 = sum FX(e)
       float lmax = -INFINITY;
@@ -687,21 +726,19 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           break;
         }
         if (frozen) continue;  // the next residual would be the same all-zero one
-        if (!qready) {
-          wait_copy(&sh.qbar, qphase, status);
-          qready = true;
-        }
+        if (qpend & (1u << qb)) wait_draft(sh, qb, qphase, qpend, status);
         if (threadIdx.x == 0) sh.s.z[nsteps] = Z;  // read only after the exchange below
         unsigned long long np;
         if (vec) {
+          const float y = __frcp_rn(Z);
           FxSum ra;
           for (int j = e0 >> 2; j < (e1 >> 2); ++j) {
             float4 dv = D4[j];
             const float4 qq = Q4[j];
-            dv.x = resid(dv.x, Z, qq.x);
-            dv.y = resid(dv.y, Z, qq.y);
-            dv.z = resid(dv.z, Z, qq.z);
-            dv.w = resid(dv.w, Z, qq.w);
+            dv.x = resid_y(dv.x, Z, y, qq.x);
+            dv.y = resid_y(dv.y, Z, y, qq.y);
+            dv.z = resid_y(dv.z, Z, y, qq.z);
+            dv.w = resid_y(dv.w, Z, y, qq.w);
             D4[j] = dv;
             ra.add(dv.x);
             ra.add(dv.y);
@@ -739,7 +776,6 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           __syncthreads();
         }
       }
-      if (!qready) wait_copy(&sh.qbar, qphase, status);  // Q is rewritten at the next node
       if (accepted >= 0) {
         if (threadIdx.x == 0) sh.aux[L] = accepted;
         ++L;
@@ -791,6 +827,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
       }
       break;
     }
+    // no copy may land after the CTA has left
+    if (qpend & 1u) wait_draft(sh, 0, qphase, qpend, status);
+    if (qpend & 2u) wait_draft(sh, 1, qphase, qpend, status);
     // path, emitted tokens of the accepted nodes, lengths, -1 tails
     __syncthreads();
     if (rank == 0) {
@@ -820,7 +859,7 @@ constexpr size_t kVerifyWorkspace = 256;
 template <int MODE, int C>
 cudaError_t launch_walk(const VerifyArgs& a, int B, cudaStream_t stream) {
   auto kern = verify_walk_kernel<MODE, C>;
-  const size_t dyn = MODE == 1 ? 2 * (size_t)a.slice * sizeof(float) : 0;
+  const size_t dyn = MODE == 1 ? 3 * (size_t)a.slice * sizeof(float) : 0;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
   if (C > 8) {
@@ -895,7 +934,7 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
     // only when every request's cluster is resident at once: a cluster that
     // waits for another to finish costs more than the wider slices save
     const int s16 = (((a.V + 15) / 16) + 3) & ~3;
-    if (clusters16<MODE>(MODE == 1 ? 2 * (size_t)s16 * sizeof(float) : 0) >= B) C = 16;
+    if (clusters16<MODE>(MODE == 1 ? 3 * (size_t)s16 * sizeof(float) : 0) >= B) C = 16;
   }
   a.slice = (((a.V + C - 1) / C) + 3) & ~3;
   if (MODE == 1 && a.slice > kMaxSlice) return SPEC_ERR_UNSUPPORTED;
