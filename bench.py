@@ -62,6 +62,28 @@ def algorithmic_bytes(w, stats, mode="stochastic"):
     return dict(mask=mask, attention=attn, verify=verify, commit=commit)
 
 
+def attention_flops(w):
+    """4 * D * Hq * sum over nodes u of (P_b + depth(u) + 1): every unmasked key."""
+    par = w.parent.tolist()
+    off = w.tree_off.tolist()
+    total = 0
+    for b in range(w.B):
+        depth = {}
+        for i in range(off[b + 1] - off[b]):
+            p = par[off[b] + i]
+            depth[i] = 0 if p < 0 else depth[p] + 1
+            total += int(w.prefix_len[b]) + depth[i] + 1
+    return 4 * w.D * w.Hq * total
+
+
+def _bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def _tree_stats(w, accept_paths):
     """Rows the verifier's walk reads and rows the commit moves, from the
     accepted paths: every path node's target row; the draft row of a path node
@@ -83,41 +105,6 @@ def _tree_stats(w, accept_paths):
                 rejecting += 1
         moved += sum(1 for i, p in enumerate(row) if p >= 0 and p != i)
     return dict(walk_rows=walk_rows, rejecting_nodes=rejecting, moved_rows=moved)
-
-
-class _Cudart:
-    """The CUDA runtime the process already loaded (PyTorch's), for external
-    event records inside captured graphs."""
-
-    def __init__(self):
-        import ctypes
-        self.ct = ctypes
-        self.lib = None
-        for name in ("libcudart.so.13", "libcudart.so", "/usr/local/cuda/lib64/libcudart.so.13"):
-            try:
-                self.lib = ctypes.CDLL(name)
-                break
-            except OSError:
-                continue
-        if self.lib is None:
-            raise RuntimeError("libcudart not found")
-        self.lib.cudaEventCreateWithFlags.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint]
-        self.lib.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
-        self.lib.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
-        self.lib.cudaEventDestroy.argtypes = [ctypes.c_void_p]
-
-    def event(self):
-        e = self.ct.c_void_p()
-        assert self.lib.cudaEventCreateWithFlags(self.ct.byref(e), 0) == 0
-        return e
-
-    def record_external(self, ev, stream):  # cudaEventRecordExternal: a node of the captured graph
-        assert self.lib.cudaEventRecordWithFlags(ev, self.ct.c_void_p(stream.cuda_stream), 1) == 0
-
-    def elapsed_ms(self, a, b):
-        ms = self.ct.c_float()
-        assert self.lib.cudaEventElapsedTime(self.ct.byref(ms), a, b) == 0
-        return ms.value
 
 
 class ClockSampler:
@@ -296,7 +283,6 @@ def bench_gpu(args):
     B_.build()
     S.lib()
     dev = torch.device("cuda", local)
-    rt = _Cudart()
 
     sets, passes, works = [], [], []
     for i in range(N_SETS):
@@ -307,80 +293,67 @@ def bench_gpu(args):
         passes.append(VerifyPass(d))
     torch.cuda.synchronize()
 
-    def step(vp, ev=None, stream=None):
-        """One pass; ev maps a stage name to its (before, after) events."""
+    stages = ("mask", "attention", "verify", "commit")
+
+    def step(vp, skip=None):
+        """One pass (optionally without one stage, for the differential timing)."""
         for name, fn in (("mask", vp.mask_build), ("attention", lambda: vp.attention(args.attn_flags)),
                          ("verify", lambda: vp.verify(args.mode)), ("commit", vp.commit)):
-            if ev and name in ev:
-                rt.record_external(ev[name][0], stream)
-            fn()
-            if ev and name in ev:
-                rt.record_external(ev[name][1], stream)
+            if name != skip:
+                fn()
 
     # eager warm-up (first calls set kernel attributes and look up driver entry points)
     for i in range(args.warmup):
         step(passes[i % N_SETS])
     torch.cuda.synchronize()
 
-    def capture(stages, copies):
-        """CUDA graphs of one pass per (copy, input set), with events around
-        the given stages."""
+    def capture(skip=None):
+        """One CUDA graph of one pass per input set (no event nodes inside)."""
         cap = torch.cuda.Stream(dev)
-        gs, es = [], []
-        for c in range(copies):
-            for i in range(N_SETS):
-                ev = {k: (rt.event(), rt.event()) for k in stages}
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=cap):
-                    step(passes[i], ev, torch.cuda.current_stream(dev))
-                gs.append(g)
-                es.append(ev)
+        gs = []
+        for i in range(N_SETS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                step(passes[i], skip)
+            gs.append(g)
         torch.cuda.synchronize()
-        return gs, es
+        return gs
 
     stream = torch.cuda.current_stream(dev)
-    all_stages = ("mask", "attention", "verify", "commit")
-    # every stage timed in instrumented replays outside the timed region; they
-    # pick the dominant kernel
-    igraphs, ievs = capture(all_stages, 1)
-    for r in range(max(args.warmup, 3)):
-        for g in igraphs:
-            g.replay()
-    torch.cuda.synchronize()
-    stage = {k: [] for k in all_stages}
-    for r in range(3):
-        for g, ev in zip(igraphs, ievs):
-            g.replay()
-            torch.cuda.synchronize()
-            for k in all_stages:
-                stage[k].append(rt.elapsed_ms(*ev[k]))
-    dom = max(("attention", "verify"), key=lambda k: statistics.mean(stage[k]))
-    # the timed graphs carry events around the dominant kernel only
-    graphs, gevs = capture((dom,), 4)
-    for i in range(args.warmup):
-        graphs[i % len(graphs)].replay()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+
+    def timed(graphs):
+        """K replays bracketed by CUDA events on the replay stream (barrier and
+        synchronize on both sides); returns milliseconds."""
+        for i in range(args.warmup):
+            graphs[i % N_SETS].replay()
         torch.cuda.synchronize()
-        t_start.record(stream)
+        if world > 1:
+            torch.distributed.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
         for i in range(args.steps):
-            graphs[i % len(graphs)].replay()
-        t_end.record(stream)
+            graphs[i % N_SETS].replay()
+        b.record(stream)
         torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    # the dominant kernel's time: last replay of every timed graph (inside the
-    # timed region)
-    stage[dom] = [rt.elapsed_ms(*gevs[gi][dom]) for gi in range(min(len(graphs), args.steps))]
+        if world > 1:
+            torch.distributed.barrier()
+        return a.elapsed_time(b)
+
+    graphs = capture()
+    with ClockSampler(local) as clk:
+        elapsed_ms = timed(graphs)
+    # per-kernel launch durations: the same K steps without that kernel, timed
+    # the same way right after; duration = (full - without) / K
+    stage = {}
+    for k in stages:
+        stage[k] = max(0.0, (elapsed_ms - timed(capture(skip=k))) / args.steps)
+    dom = max(("attention", "verify"), key=lambda k: stage[k])
 
     # emitted tokens per step (verify inputs do not change between steps of one set)
     tokens_per_set = [int(p.n_emitted[:p.batch.B].sum()) for p in passes]
     status_ok = all(int(p.status[:p.batch.B].abs().sum()) == 0 for p in passes)
-    tokens = sum(tokens_per_set[(i % len(graphs)) % N_SETS] for i in range(args.steps))
+    tokens = sum(tokens_per_set[i % N_SETS] for i in range(args.steps))
     elapsed_ms, tokens = aggregate_replicas(elapsed_ms, float(tokens), dev)
     value = tokens / (elapsed_ms / 1e3)
 
@@ -394,9 +367,21 @@ def bench_gpu(args):
     w0 = works[0]
     stats = _tree_stats(w0, passes[0].path[:w0.B].tolist())
     algo = algorithmic_bytes(w0, stats, args.mode)
-    avg = {k: statistics.mean(v) for k, v in stage.items()}
-    kernels = {k: {"ms": avg[k], "bytes": algo[k], "gbs": algo[k] / (avg[k] * 1e-3) / 1e9,
-                   "frac_hbm": algo[k] / (avg[k] * 1e-3) / 1e9 / peak} for k in avg}
+    avg = stage
+    kernels = {k: {"ms": avg[k], "bytes": algo[k], "gbs": algo[k] / (avg[k] * 1e-3) / 1e9 if avg[k] > 0 else None,
+                   "frac_hbm": algo[k] / (avg[k] * 1e-3) / 1e9 / peak if avg[k] > 0 else None} for k in avg}
+    # the pages' per-unit formulas for the two big kernels: attention flops
+    # (unmasked keys only) and the verifier's full-row byte count
+    flops = attention_flops(w0)
+    t_attn = avg["attention"]
+    kernels["attention"]["tflops"] = flops / (t_attn * 1e-3) / 1e12 if t_attn > 0 else None
+    kernels["attention"]["frac_tensor_burst"] = (kernels["attention"]["tflops"] / _bf16_peak()
+                                                 if t_attn > 0 else None)
+    n_int = sum(1 for b in range(w0.B) for u in range(int(w0.tree_off[b]), int(w0.tree_off[b + 1]))
+                if any(int(w0.parent[c]) == u - int(w0.tree_off[b]) for c in range(u + 1, int(w0.tree_off[b + 1]))))
+    full_rows = 4 * w0.V * (w0.T + (n_int if args.mode == "stochastic" else 0))
+    kernels["verify"]["bytes_all_rows"] = full_rows
+    kernels["verify"]["gbs_all_rows"] = full_rows / (avg["verify"] * 1e-3) / 1e9 if avg["verify"] > 0 else None
     achieved = kernels[dom]["gbs"]
     launches_per_step = 4 + (1 if _attn_splits(passes[0]) > 1 else 0)
     traffic = _profiled_traffic(dom, args.mode)
@@ -406,9 +391,9 @@ def bench_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "verify": args.mode, "input_sets": N_SETS,
                        "l2": "3 rotating input sets of ~205 MB each (inputs larger than L2)",
-                       "launch": "one CUDA graph per step (the five C-ABI calls captured)",
-                       "kernel_timing": "dominant kernel: CUDA events inside the timed graphs; other stages: "
-                                        "instrumented replays of the same graphs outside the timed region",
+                       "launch": "one CUDA graph per step (the C-ABI calls of the pass captured, no event nodes)",
+                       "kernel_timing": "per kernel: (K timed steps - the same K steps without that kernel) / K, "
+                                        "each run bracketed by CUDA events on the replay stream",
                        "tokens_per_step": tokens / args.steps / max(world, 1), "status_ok": status_ok,
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "clocks": clk.summary(),

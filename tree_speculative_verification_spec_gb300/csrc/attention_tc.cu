@@ -7,29 +7,32 @@
 // shared by all its query heads (GQA) and all its tree nodes.  Per 128-key
 // tile j of the CTA's key range:
 //   S_j = Q K_j^T            tcgen05.mma, A = Q (smem), B = K tile (smem), D in
-//                            tensor-memory slot j % 3
+//                            tensor-memory slot j % 2
 //   P_j = exp2(S_j*c - m)    softmax warps: TMEM -> registers -> bf16 P written
-//                            back over the first half of S_j's slot; the
+//                            back over the S columns each thread read; the
 //                            ancestor bitmask is applied only on tiles that
 //                            reach past the prefix
-//   O  += P_j V_j            tcgen05.mma, A = P (tensor memory), B = V tile
-//                            (smem, MN-major)
+//   O_h += P_j,h V_j,h       tcgen05.mma, A = P (tensor memory), B = V tile
+//                            (smem, MN-major), h = the key half of the tile
+// The two 64-key halves of every tile run separate online softmaxes with
+// separate accumulators O_0 and O_1 (two threads per row, one per half, each
+// with its own running maximum and sum), so the two threads of a row never
+// wait for each other inside the loop; the epilogue merges the halves:
+// O = (2^(m0-m) O_0 + 2^(m1-m) O_1) / (2^(m0-m) l_0 + 2^(m1-m) l_1).
+// Tensor memory: S/P slots 0 and 1 (128 columns each), O_0 and O_1 (D each).
 // K and V tiles arrive by TMA (2-D tensor maps over the paged cache, one box
 // per page or per 128 rows), 128-byte swizzled, into a three-stage K ring and
-// a two-stage V ring.  Three S slots let the tensor core run QK_{j+1} and
-// QK_{j+2} while the softmax works on tile j, and P never leaves tensor
-// memory, so the softmax of consecutive tiles runs back to back.  O is
-// rescaled only when a row maximum grows by more than 2^8 (the stale maximum
-// is exact for the final normalisation), between PV_{j-1} and PV_j.
+// a two-stage V ring.  While the softmax works on tile j the tensor core runs
+// PV_{j-1} and QK_{j+1}.  O_h is rescaled only when the half's maximum grows
+// by more than 2^8 (the stale maximum is exact for the final normalisation).
 //
-// Warp roles (384 threads): warp 0 issues the K loads from the start, warp 1
-// issues MMAs and owns the TMEM allocation, warps 2-11 stage the Q tile, then
-// warp 3 issues the V loads and warps 4-11 run softmax and the epilogue: two
-// threads per accumulator row (row r == TMEM lane r, the warp's lane
-// quadrant), each owning one 64-column half of S and O; their row maxima meet
-// through shared memory and a 64-thread mbarrier per lane quadrant.  Every
-// mbarrier wait is bounded: on expiry the CTA records SPEC_DEV_TIMEOUT, drains
-// its own copies and MMAs, frees TMEM and returns.
+// Warp roles (384 threads): warps 0 and 2 issue the K and V loads from the
+// start, warp 1 issues MMAs and owns the TMEM allocation, warps 3-11 stage the
+// Q tile, then warps 4-11 run softmax and the epilogue
+// (row r == TMEM lane r, the warp's lane quadrant; warps 4-7 take key half 0,
+// warps 8-11 key half 1).  Every mbarrier wait is bounded: on expiry the CTA
+// records SPEC_DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and
+// returns.
 #include <cuda.h>
 
 #include "attention.cuh"
@@ -159,6 +162,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (three-input form of max.f32, sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& ra, float& rb) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   ra = __low2float(h);
@@ -169,8 +179,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& ra, float
 template <int D>
 struct Layout {
   static constexpr int DH = D / 64;           // 128-byte halves of a row
-  static constexpr int KST = 2;               // K stages (QK runs up to three tiles ahead of PV)
-  static constexpr int VST = 3;               // V stages (a V stage frees only when its PV completes)
+  static constexpr int KST = 3;               // K stages: a K load goes out three tiles before its QK
+  static constexpr int VST = 2;               // V stages: a V load goes out two tiles before its PV
   static constexpr uint32_t kQ = BM * D * 2;  // Q tile bytes
   static constexpr uint32_t kKV = BN * D * 2; // one K (or V) stage
   static constexpr uint32_t kOffQ = 0;
@@ -187,27 +197,56 @@ struct TcParams {
   long long rows_total;  // num_blocks * Hkv * block_size (rows of the 2-D cache view)
 };
 
-// TMA of one K or V tile (keys k0 .. k0+BN-1 of kv-head kvh) into dst, one
-// box per page (or per 128 rows); rows past the key range or at a bad block
-// id read the out-of-range row `rows_total` (zero fill).
-template <int D>
-__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap* map, const TcParams& prm, int b,
-                                             int kvh, int k0, int Lk, uint64_t* full, int* bad_block) {
+// Row of the 2-D cache view where the TMA box starting at key k of kv-head
+// kvh begins; keys past the key range or at a bad block id read the
+// out-of-range row `rows_total` (zero fill).
+__device__ __forceinline__ int kv_box_row(const TcParams& prm, const int32_t* bt, int kvh, int k, int Lk,
+                                          int* bad_block) {
   const AttnArgs& a = prm.a;
-  const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
-  const int bs = a.block_size, br = prm.box_rows;
-  mbar_expect_tx(full, Layout<D>::kKV);
-  for (int i = 0; i < BN / br; ++i) {
-    const int k = k0 + i * br;
-    int y = (int)prm.rows_total;
-    if (k < Lk) {
-      const int blk = bt[k / bs];
-      if (blk >= 0 && blk < a.num_blocks) y = (int)(((long long)blk * a.Hkv + kvh) * bs + (k % bs));
-      else *bad_block = 1;
-    }
-#pragma unroll
-    for (int h = 0; h < Layout<D>::DH; ++h) tma_load_2d(dst + h * (BN * 128) + i * br * 128, map, h * 64, y, full);
+  int y = (int)prm.rows_total;
+  if (k < Lk) {
+    const int blk = __ldg(bt + k / a.block_size);
+    if (blk >= 0 && blk < a.num_blocks) y = (int)(((long long)blk * a.Hkv + kvh) * a.block_size + (k % a.block_size));
+    else *bad_block = 1;
   }
+  return y;
+}
+
+// One producer warp streams the K (or V) tiles of the CTA's key range through
+// a ring of NST stages: lane i issues the TMA boxes of page (or 128-row
+// piece) i of each tile.  The block-table entries of tile j + 1 are loaded
+// while the warp waits for tile j's stage, so no dependent global load sits
+// between a stage becoming free and its copy going out.
+template <int D, int NST>
+__device__ __forceinline__ void produce_ring(uint32_t ring, const CUtensorMap* map, const TcParams& prm, int b, int kvh,
+                                             int k_begin, int Lk, int ntiles, uint64_t* full, uint64_t* empty,
+                                             int* bad_block, volatile int* abort_flag) {
+  const AttnArgs& a = prm.a;
+  const int lane = threadIdx.x & 31;
+  const int br = prm.box_rows, nb = BN / br;  // boxes per tile (1 .. 16)
+  const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
+  int y_next = lane < nb ? kv_box_row(prm, bt, kvh, k_begin + lane * br, Lk, bad_block) : 0;
+  int issued = 0;
+  for (int j = 0; j < ntiles; ++j) {
+    const int st = j % NST;
+    const int y = y_next;
+    if (j + 1 < ntiles && lane < nb) y_next = kv_box_row(prm, bt, kvh, k_begin + (j + 1) * BN + lane * br, Lk, bad_block);
+    bool go = true;
+    if (lane == 0 && j >= NST) go = mbar_wait(&empty[st], (j / NST - 1) & 1, abort_flag);
+    go = __shfl_sync(0xffffffffu, go, 0);
+    if (!go) break;
+    if (lane == 0) mbar_expect_tx(&full[st], Layout<D>::kKV);
+    __syncwarp();
+    if (lane < nb) {
+      const uint32_t dst = ring + st * Layout<D>::kKV + lane * br * 128;
+#pragma unroll
+      for (int h = 0; h < Layout<D>::DH; ++h) tma_load_2d(dst + h * (BN * 128), map, h * 64, y, &full[st]);
+    }
+    issued = j + 1;
+  }
+  // drain: every issued load has landed before the CTA can exit
+  if (lane == 0)
+    for (int j = max(0, issued - NST); j < issued; ++j) mbar_wait(&full[j % NST], (j / NST) & 1, abort_flag);
 }
 
 template <int D>
@@ -220,13 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int KST = L_::KST, VST = L_::VST;
   const AttnArgs& a = prm.a;
   extern __shared__ uint8_t dyn_raw[];
-  __shared__ uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[3], p_full[3], pv_done[3], q_full,
+  __shared__ uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2], p_full[2], pv_done[2], q_full,
       drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag, bad_block;
-  __shared__ float xchg[2][2][BM];  // [tile parity][column half][row]: partial row maxima
-  __shared__ float lfin[2][BM];     // final partial row sums
-  __shared__ uint64_t xbar[2][4], lbar[4];  // pair exchanges per lane quadrant (bounded waits)
+  __shared__ float mfin[2][BM], lfin[2][BM];  // [key half][row]: final maximum and sum of each half
+  __shared__ uint64_t lbar[4];                 // their exchange, per lane quadrant (bounded waits)
 
   const int mt = blockIdx.x, split = blockIdx.y;
   const int b = blockIdx.z / a.Hkv, kvh = blockIdx.z % a.Hkv;
@@ -261,18 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kSoftmaxThreads);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(&q_full, kThreads - 64);
+    mbar_init(&q_full, kThreads - 96);
     mbar_init(&drain, 1);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&xbar[0][i], 64);
-      mbar_init(&xbar[1][i], 64);
-      mbar_init(&lbar[i], 64);
-    }
+    for (int i = 0; i < 4; ++i) mbar_init(&lbar[i], 64);
     abort_flag = 0;
     bad_block = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -287,38 +321,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 3 * BN;  // S / P slots 0..2 at 0, 128, 256; O at 384
+  const uint32_t tS = tmem, tO = tmem + 2 * BN;  // S / P slots 0, 1 at 0, 128; O_0 at 256, O_1 at 256 + D
 
   if (warp == 0) {
     // ---------------------------------------------------------- K producer
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
-      // the first K and V tiles go out at once (their stages are free); warp 3
-      // issues the later V tiles once it has staged its part of Q
-      for (int j = 0; j < min(KST, ntiles); ++j)
-        load_kv_tile<D>(sbase + L_::kOffK + j * L_::kKV, &tmap_k, prm, b, kvh, k_begin + j * BN, Lk, &k_full[j],
-                        &bad_block);
-      for (int j = 0; j < min(VST, ntiles); ++j)
-        load_kv_tile<D>(sbase + L_::kOffV + j * L_::kKV, &tmap_v, prm, b, kvh, k_begin + j * BN, Lk, &v_full[j],
-                        &bad_block);
-      int issued = min(KST, ntiles);
-      for (int j = issued; j < ntiles; ++j) {
-        const int st = j % KST;
-        if (j >= KST && !mbar_wait(&k_empty[st], (j / KST - 1) & 1, &abort_flag)) break;
-        load_kv_tile<D>(sbase + L_::kOffK + st * L_::kKV, &tmap_k, prm, b, kvh, k_begin + j * BN, Lk, &k_full[st],
-                        &bad_block);
-        issued = j + 1;
-      }
-      // drain: every issued load has landed before the CTA can exit
-      for (int j = max(0, issued - KST); j < issued; ++j) mbar_wait(&k_full[j % KST], (j / KST) & 1, &abort_flag);
     }
+    produce_ring<D, KST>(sbase + L_::kOffK, &tmap_k, prm, b, kvh, k_begin, Lk, ntiles, k_full, k_empty, &bad_block,
+                         &abort_flag);
+  } else if (warp == 2) {
+    // ---------------------------------------------------------- V producer
+    produce_ring<D, VST>(sbase + L_::kOffV, &tmap_v, prm, b, kvh, k_begin, Lk, ntiles, v_full, v_empty, &bad_block,
+                         &abort_flag);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // S_j = Q K_j^T into slot j % 3; P_j (bf16) overwrites the first half of
-    // that slot; O += P_j V_j reads A from tensor memory.  Issue order:
-    // QK_0 QK_1 QK_2, then PV_j followed by QK_{j+3} (which reuses P_j's slot;
-    // the tensor pipe executes them in issue order).
+    // S_j = Q K_j^T into slot j % 2; P_j (bf16) overwrites part of that slot;
+    // O_h += P_j,h V_j,h reads A from tensor memory.  Issue order: QK_0 QK_1,
+    // then PV_j followed by QK_{j+2} (which reuses P_j's slot; the tensor pipe
+    // executes them in issue order).
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(D, 1);
@@ -333,47 +355,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
           const uint32_t ob = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-          umma_bf16(tS + (j % 3) * BN, smem_desc_sw128(qaddr + o, 16, 1024), smem_desc_sw128(kaddr + ob, 16, 1024),
+          umma_bf16(tS + (j & 1) * BN, smem_desc_sw128(qaddr + o, 16, 1024), smem_desc_sw128(kaddr + ob, 16, 1024),
                     idesc_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[j % 3]);
+        umma_commit(&s_full[j & 1]);
         umma_commit(&k_empty[st]);
         return true;
       };
-      for (int j = 0; j < min(3, ntiles) && ok; ++j) ok = issue_qk(j);
+      for (int j = 0; j < min(2, ntiles) && ok; ++j) ok = issue_qk(j);
       for (int j = 0; j < ntiles && ok; ++j) {
-        if (!mbar_wait(&p_full[j % 3], (j / 3) & 1, &abort_flag) ||
+        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, &abort_flag) ||
             !mbar_wait(&v_full[j % VST], (j / VST) & 1, &abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t vaddr = sbase + L_::kOffV + (j % VST) * L_::kKV;
+        // key half h: P at columns h*64 .. h*64+31 of the slot (two keys per
+        // column), V rows h*64 .. h*64+63, accumulator O_h
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(vaddr + kk * 2048, BN * 128, 1024);
-          umma_bf16_ts(tO, tS + (j % 3) * BN + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int kk = 0; kk < HC / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(vaddr + (h * (HC / 16) + kk) * 2048, BN * 128, 1024);
+            umma_bf16_ts(tO + h * D, tS + (j & 1) * BN + h * HC + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
         }
-        umma_commit(&pv_done[j % 3]);
+        umma_commit(&pv_done[j & 1]);
         umma_commit(&v_empty[j % VST]);
-        if (j + 3 < ntiles) ok = issue_qk(j + 3);
+        if (j + 2 < ntiles) ok = issue_qk(j + 2);
       }
       // drain: every issued MMA has completed before TMEM is freed
       umma_commit(&drain);
       mbar_wait(&drain, 0, &abort_flag);
     }
   } else {
-    // ------------------------------------------------ Q tile (warps 2..11)
+    // ------------------------------------------------ Q tile (warps 3..11)
     // row r = (node r / g, head kvh*g + r % g); rows past the group are zero
     {
       const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
       constexpr int CPR = D / 8;  // 16-byte chunks per row
-      constexpr int NT = kThreads - 64;
+      constexpr int NT = kThreads - 96;
       constexpr int NQ = (BM * CPR + NT - 1) / NT;  // chunks per thread: all loads first
       uint4 v[NQ];
 #pragma unroll
       for (int i = 0; i < NQ; ++i) {
-        const int c = threadIdx.x - 64 + i * NT;
+        const int c = threadIdx.x - 96 + i * NT;
         const int r = c / CPR, ch = c % CPR;
         const int row = mt * BM + r;
         v[i] = make_uint4(0, 0, 0, 0);
@@ -384,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int i = 0; i < NQ; ++i) {
-        const int c = threadIdx.x - 64 + i * NT;
+        const int c = threadIdx.x - 96 + i * NT;
         if (c >= BM * CPR) break;
         const int r = c / CPR, ch = c % CPR;
         const int h = ch >> 3, cc = ch & 7;
@@ -393,31 +420,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       mbar_arrive(&q_full);
     }
-    if (warp == 3) {
-      // ------------------------------------------------------- V producer
-      if (lane == 0) {
-        int issued = min(VST, ntiles);
-        for (int j = issued; j < ntiles; ++j) {
-          const int st = j % VST;
-          if (j >= VST && !mbar_wait(&v_empty[st], (j / VST - 1) & 1, &abort_flag)) break;
-          load_kv_tile<D>(sbase + L_::kOffV + st * L_::kKV, &tmap_v, prm, b, kvh, k_begin + j * BN, Lk, &v_full[st],
-                          &bad_block);
-          issued = j + 1;
-        }
-        for (int j = max(0, issued - VST); j < issued; ++j) mbar_wait(&v_full[j % VST], (j / VST) & 1, &abort_flag);
-      }
-    } else if (warp >= 4) {
+    if (warp >= 4) {
       // -------------------------------------------------- softmax + epilogue
-      // two threads per accumulator row: column half `half` of S, P and O
+      // key half `half` of every tile: its own running maximum m_used (log2
+      // units), sum and accumulator O_half
       const int quad = warp & 3, half = (warp - 4) >> 2;
       const int r = quad * 32 + lane;  // accumulator row == TMEM lane
       const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+      const uint32_t tOh = tO + half * D;
       const int row = mt * BM + r;
       const bool valid = row < R;
       const int t = valid ? off + row / g : off;
       const uint64_t* mrow = a.mask + (size_t)t * a.W;
       const float c2 = a.scale_log2;
-      float m_used = -INFINITY, lpart[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const float2 c22 = make_float2(c2, c2);
+      float m_used = -INFINITY;
+      float2 lacc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
       bool ok = true;
       // tcgen05.ld / st are warp-collective: every decision before one is warp-uniform
       auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -425,22 +443,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         return __all_sync(0xffffffffu, w);
       };
       for (int j = 0; j < ntiles && ok; ++j) {
-        const uint32_t sl = tS + (j % 3) * BN;  // this tile's S / P slot
+        const uint32_t sl = tS + (j & 1) * BN + half * HC;  // this thread's S columns (and P target)
         const int k0 = k_begin + j * BN;
         const int c0 = k0 + half * HC;  // first key of this thread's columns
-        if (!wait_warp(&s_full[j % 3], (j / 3) & 1)) {
+        if (!wait_warp(&s_full[j & 1], (j >> 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float x[HC];
-#pragma unroll
-        for (int c = 0; c < HC / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(sl + half * HC + c * 32 + lane_off, v);
+        float x[HC];  // raw scores q.k
+        {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(sl + lane_off, v0);
+          tmem_ld32(sl + 32 + lane_off, v1);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]) * c2;
+          for (int e = 0; e < 32; ++e) {
+            x[e] = __uint_as_float(v0[e]);
+            x[32 + e] = __uint_as_float(v1[e]);
+          }
         }
 
         // visibility: the tile reaches past the prefix (tree tail) or the range end
@@ -465,60 +486,63 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < HC; ++e)
             if (!((vis >> e) & 1ull)) x[e] = -INFINITY;
         }
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float mx[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-        for (int e = 0; e < HC; ++e) mx[e & 3] = fmaxf(mx[e & 3], x[e]);
-        float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        // combine with the partner thread (same row, other column half); after
-        // this exchange both halves have read S_j, so P_j may overwrite it
-        xchg[j & 1][half][r] = mloc;
-        mbar_arrive(&xbar[j & 1][quad]);
-        if (!wait_warp(&xbar[j & 1][quad], (j >> 1) & 1)) {
-          ok = false;
-          break;
+        for (int e = 4; e < HC; e += 8) {
+          mx[0] = fmax3(mx[0], x[e], x[e + 1]);
+          mx[1] = fmax3(mx[1], x[e + 2], x[e + 3]);
+          if (e + 4 < HC) {
+            mx[2] = fmax3(mx[2], x[e + 4], x[e + 5]);
+            mx[3] = fmax3(mx[3], x[e + 6], x[e + 7]);
+          }
         }
-        const float mtile = valid ? fmaxf(mloc, xchg[j & 1][half ^ 1][r]) : -INFINITY;
+        // the scale is positive: max(c * s) = c * max(s)
+        const float mtile = valid ? fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * c2 : -INFINITY;
 
         float factor = 1.0f;
         bool rescale = false;
         if (mtile > m_used + kRescaleLog2) {
-          rescale = j > 0;
+          rescale = j > 0 && m_used != -INFINITY;
           factor = fast_exp2(m_used - mtile);  // 0 when m_used = -inf
-#pragma unroll
-          for (int i = 0; i < 4; ++i) lpart[i] *= factor;
+          lacc[0].x *= factor;
+          lacc[0].y *= factor;
+          lacc[1].x *= factor;
+          lacc[1].y *= factor;
           m_used = mtile;
         }
-        // P (bf16) for this thread's 64 keys, packed in pairs: key k of the tile
-        // at column k / 2 of the slot; sums from the fp32 values
+        // P (bf16) for this thread's 64 keys, packed in pairs: key k of the half
+        // at column k / 2 of this thread's columns; sums from the fp32 values
         uint32_t pk[HC / 2];
-        const float mneg = -m_used;
+        if (m_used != -INFINITY) {
+          const float2 mneg = make_float2(-m_used, -m_used);
 #pragma unroll
-        for (int e = 0; e < HC; e += 2) {
-          float p0 = 0.0f, p1 = 0.0f;
-          if (valid && m_used != -INFINITY) {
-            p0 = fast_exp2(x[e] + mneg);  // -inf gives 0
-            p1 = fast_exp2(x[e + 1] + mneg);
+          for (int e = 0; e < HC; e += 2) {
+            const float2 arg = __ffma2_rn(make_float2(x[e], x[e + 1]), c22, mneg);  // -inf gives 0 below
+            const float2 pe = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+            lacc[(e >> 1) & 1] = __fadd2_rn(lacc[(e >> 1) & 1], pe);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(pe.x, pe.y);
+            pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          lpart[(e >> 1) & 3] += p0 + p1;
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          pk[e >> 1] = *reinterpret_cast<uint32_t*>(&h2);
+        } else {
+#pragma unroll
+          for (int e = 0; e < HC / 2; ++e) pk[e] = 0u;
         }
-        // O holds PV_{j-1} once that MMA completes; PV_j waits for this tile's P
+        // O_half holds PV_{j-1} once that MMA completes; PV_j waits for this tile's P
         if (__any_sync(0xffffffffu, rescale)) {
-          if (!wait_warp(&pv_done[(j - 1) % 3], ((j - 1) / 3) & 1)) {
+          if (!wait_warp(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const float f = rescale ? factor : 1.0f;
 #pragma unroll
-          for (int c = 0; c < OC / 32; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t v[32];
-            tmem_ld32(tO + half * OC + c * 32 + lane_off, v);
+            tmem_ld32(tOh + c * 32 + lane_off, v);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
-            tmem_st32(tO + half * OC + c * 32 + lane_off, v);
+            tmem_st32(tOh + c * 32 + lane_off, v);
           }
         }
         // a tile reaching past the key range: zero its V rows there (no stale
@@ -538,50 +562,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_async_smem();
         }
-        tmem_st32(sl + half * (HC / 2) + lane_off, pk);
+        tmem_st32(sl + lane_off, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full[j % 3]);
+        mbar_arrive(&p_full[j & 1]);
       }
-      // epilogue: this thread's half of the O row
-      lfin[half][r] = (lpart[0] + lpart[1]) + (lpart[2] + lpart[3]);
+      // epilogue: merge the halves; this thread writes output columns
+      // half*D/2 .. half*D/2 + D/2 - 1 of its row
+      mfin[half][r] = m_used;
+      lfin[half][r] = (lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y);
       mbar_arrive(&lbar[quad]);
       ok = ok && wait_warp(&lbar[quad], 0);
-      const float lsum = lfin[0][r] + lfin[1][r];
-      if (ok && wait_warp(&pv_done[(ntiles - 1) % 3], ((ntiles - 1) / 3) & 1)) {
+      const float m0 = mfin[0][r], m1 = mfin[1][r];
+      const float mrow_max = fmaxf(m0, m1);
+      const float f0 = m0 == -INFINITY ? 0.0f : fast_exp2(m0 - mrow_max);
+      const float f1 = m1 == -INFINITY ? 0.0f : fast_exp2(m1 - mrow_max);
+      const float lsum = lfin[0][r] * f0 + lfin[1][r] * f1;
+      if (ok && wait_warp(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
         tc_fence_after();
         const size_t orow = (size_t)t * a.Hq + kvh * g + (valid ? row % g : 0);
         const float inv = 1.0f / lsum;
+        const float2 w0 = a.splits == 1 ? make_float2(f0 * inv, f0 * inv) : make_float2(f0, f0);
+        const float2 w1 = a.splits == 1 ? make_float2(f1 * inv, f1 * inv) : make_float2(f1, f1);
 #pragma unroll
         for (int c = 0; c < OC / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO + half * OC + c * 32 + lane_off, v);
+          const int col = half * OC + c * 32;
+          uint32_t u0[32], u1[32];
+          tmem_ld32(tO + col + lane_off, u0);
+          tmem_ld32(tO + D + col + lane_off, u1);
           tmem_wait_ld();
           if (!valid) continue;
-          const int col = half * OC + c * 32;
+          float o[32];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 y = __ffma2_rn(make_float2(__uint_as_float(u0[e]), __uint_as_float(u0[e + 1])), w0,
+                                        __fmul2_rn(make_float2(__uint_as_float(u1[e]), __uint_as_float(u1[e + 1])), w1));
+            o[e] = y.x;
+            o[e + 1] = y.y;
+          }
           if (a.splits == 1) {
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + orow * D + col;
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
               float d0, d1;
               uint4 w;
-              w.x = pack_bf16(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv, d0, d1);
-              w.y = pack_bf16(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv, d0, d1);
-              w.z = pack_bf16(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv, d0, d1);
-              w.w = pack_bf16(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv, d0, d1);
+              w.x = pack_bf16(o[e], o[e + 1], d0, d1);
+              w.y = pack_bf16(o[e + 2], o[e + 3], d0, d1);
+              w.z = pack_bf16(o[e + 4], o[e + 5], d0, d1);
+              w.w = pack_bf16(o[e + 6], o[e + 7], d0, d1);
               *reinterpret_cast<uint4*>(out + e) = w;
             }
           } else {
             float* wo = a.ws_o + ((size_t)split * a.T * a.Hq + orow) * D + col;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(wo + e) = make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                                               __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(wo + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
           }
         }
         if (valid && a.splits > 1 && half == 0) {
           float* wml = a.ws_ml + ((size_t)split * a.T * a.Hq + orow) * 2;
-          wml[0] = m_used;
+          wml[0] = mrow_max;
           wml[1] = lsum;
         }
       }
