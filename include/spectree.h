@@ -70,7 +70,12 @@ typedef int32_t spec_status;
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 
 /* spec_tree_attention flags */
-#define SPEC_ATTN_AUTO 0u       /* tcgen05 tensor-core path for bf16 when a KV group has >= 64 query rows */
+/* SPEC_ATTN_AUTO: the tcgen05 tensor-core path for every bf16 call (a KV group
+ * with fewer than 128 query rows runs in a zero-padded 128-row tile: the path
+ * is bound by the K/V stream, and on GB300 the padded tile streams K/V at
+ * 5.3 TB/s for 36-row groups where the CUDA-core kernel reaches 0.22 TB/s);
+ * the CUDA-core path for fp32. */
+#define SPEC_ATTN_AUTO 0u
 #define SPEC_ATTN_CUDA_CORE 1u  /* force the CUDA-core path */
 #define SPEC_ATTN_TCGEN05 2u    /* force the tcgen05 path (bf16 only) */
 

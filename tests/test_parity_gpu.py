@@ -2,6 +2,8 @@
 on the same seeded inputs.  Bit-exact for masks, depths, uniforms, paths,
 emitted tokens, commit results and status words; attention within max-abs
 1e-5 (fp32) or 2e-2 + 1e-2 |ref| (bf16 inputs)."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -28,6 +30,17 @@ def _built():
 def _pass(w, **kw):
     vp = VerifyPass(DeviceBatch.from_workload(w, **kw))
     return vp
+
+
+@functools.lru_cache(maxsize=None)
+def _workload(which, **kw):
+    """Full-size workloads, generated once per test session (read-only here)."""
+    return W.make_config(which, **kw)
+
+
+# sweep points of the linear-vs-tree workload: (K, B, tree, alpha)
+SWEEP_POINTS = [(1, 4, "chain", 0.1), (4, 16, "chain", 0.3), (8, 64, "chain", 0.5), (8, 64, "random", 0.3),
+                (3, 256, "random", 0.1)]
 
 
 # ------------------------------------------------------------------ mask ----
@@ -188,11 +201,11 @@ def test_verify_empty_requests():
         assert got["accept_len"].tolist() == [0, ref["accept_len"][1], 0, 0, ref["accept_len"][4]]
 
 
-@pytest.mark.parametrize("which", [0, 1, 2])
+@pytest.mark.parametrize("which", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("mode", ["greedy", "stochastic"])
 def test_verify_parity_workloads(which, mode):
-    """The pages' workloads at full size (configs 0, 1, 2)."""
-    w = W.make_config(which)
+    """The pages' workloads at full size (configs 0-3; 4 = its default sweep point)."""
+    w = _workload(which)
     ref = oracle_greedy(w) if mode == "greedy" else oracle_stochastic(w)
     got = _gpu_verify(w, mode)
     _assert_verify_equal(got, ref, w.B)
@@ -325,11 +338,11 @@ def _sampled_rows(w, k, seed):
     return np.sort(g.choice(w.T * w.Hq, size=min(k, w.T * w.Hq), replace=False)).astype(np.int64)
 
 
-@pytest.mark.parametrize("which", [1, 2, 3])
+@pytest.mark.parametrize("which", [1, 2, 3, 4])
 def test_attention_parity_workloads_sampled(which):
     """Full-size workloads (launch configuration of the benchmark) checked on
     sampled (node, head) rows the oracle computes one by one."""
-    w = W.make_config(which)
+    w = _workload(which)
     rows = _sampled_rows(w, 96, which)
     ref, _, s_ref = oracle_attention(w, rows=rows)
     got, st = _gpu_attention(w)
@@ -337,6 +350,24 @@ def test_attention_parity_workloads_sampled(which):
     ref32 = (ref.astype(np.uint32) << 16).view(np.float32).reshape(-1, w.D)[rows]
     g = got.reshape(-1, w.D)[rows]
     assert attn_tolerance_ok(g, ref32, w.dtype).all(), float(np.abs(g - ref32).max())
+
+
+@pytest.mark.parametrize("point", SWEEP_POINTS, ids=lambda p: f"{p[2]}_K{p[0]}_B{p[1]}_a{p[3]}")
+def test_sweep_points_parity(point):
+    """Linear-vs-tree sweep points (chains and random trees of K+1 nodes, small
+    query-row groups on the padded tensor-core tile): sampled attention rows,
+    greedy and stochastic verification exact."""
+    K, B, tree, alpha = point
+    w = W.config4(K=K, B=B, tree=tree, alpha=alpha)
+    rows = _sampled_rows(w, 48, K * 1000 + B)
+    ref, _, s_ref = oracle_attention(w, rows=rows)
+    got, st = _gpu_attention(w)
+    assert (st[:w.B] == 0).all() and (s_ref == 0).all()
+    ref32 = (ref.astype(np.uint32) << 16).view(np.float32).reshape(-1, w.D)[rows]
+    assert attn_tolerance_ok(got.reshape(-1, w.D)[rows], ref32, w.dtype).all()
+    for mode in ("greedy", "stochastic"):
+        ref_v = oracle_greedy(w) if mode == "greedy" else oracle_stochastic(w)
+        _assert_verify_equal(_gpu_verify(w, mode), ref_v, w.B)
 
 
 # ---------------------------------------------------------------- commit ----
@@ -419,6 +450,32 @@ def test_full_pass_workload1(mode):
     assert np.array_equal(np_elems(vp.batch.k_cache, w.dtype), k_ref)
     assert np.array_equal(np_elems(vp.batch.v_cache, w.dtype), v_ref)
     assert np.array_equal(vp.new_len.cpu().numpy(), nl_ref)
+
+
+def test_full_pass_workload3_greedy_then_commit():
+    """The batched-serving workload as specified: 64 requests on 16-token pages
+    with a random block table, greedy verification, then the KV commit: mask,
+    verify, commit and new lengths exact, attention on sampled rows."""
+    w = _workload(3)
+    ref_m = oracle_mask(w)
+    ref_v = oracle_greedy(w)
+    rows = _sampled_rows(w, 64, 33)
+    ref_a, _, _ = oracle_attention(w, rows=rows)
+    k_ref, v_ref, nl_ref, st_ref = _oracle_commit(w, ref_v)
+    vp = _pass(w)
+    vp.run("greedy")
+    torch.cuda.synchronize()
+    assert np.array_equal(vp.mask.cpu().numpy().view(np.uint64), ref_m[0])
+    for k in ("path", "accept_len", "emitted", "n_emitted"):
+        assert np.array_equal(getattr(vp, k).cpu().numpy(), ref_v[k]), k
+    assert (ref_v["accept_len"] > 1).sum() > 0
+    got = out_as_f32(vp.out, w.dtype).reshape(-1, w.D)[rows]
+    ref32 = (ref_a.astype(np.uint32) << 16).view(np.float32).reshape(-1, w.D)[rows]
+    assert attn_tolerance_ok(got, ref32, w.dtype).all()
+    assert np.array_equal(np_elems(vp.batch.k_cache, w.dtype), k_ref)
+    assert np.array_equal(np_elems(vp.batch.v_cache, w.dtype), v_ref)
+    assert np.array_equal(vp.new_len.cpu().numpy(), nl_ref)
+    assert np.array_equal(vp.status.cpu().numpy()[:w.B], st_ref)
 
 
 # ---------------------------------------------------------- failure detection ----

@@ -254,7 +254,10 @@ AttnPlan attention_plan(int B, int n_max, int max_prefix, int Hq, int Hkv, int D
   const int rows_max = n_max * g;
   p.use_tc = false;
   if (bf16 && flags != SPEC_ATTN_CUDA_CORE && attention_tc_enabled(D)) {
-    p.use_tc = (flags == SPEC_ATTN_TCGEN05) || rows_max >= 64;
+    // every bf16 group, padded to 128 rows when smaller: the K/V stream, not
+    // the MMA, bounds small groups, and the tensor-core kernel streams it at
+    // near HBM rate where the CUDA-core kernel does not
+    p.use_tc = true;
   }
   p.row_tile = p.use_tc ? 128 : kCcRows;
   const long long units = (long long)B * Hkv * ((rows_max + p.row_tile - 1) / p.row_tile);

@@ -342,21 +342,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // then PV_j followed by QK_{j+2} (which reuses P_j's slot; the tensor pipe
     // executes them in issue order).
     if (lane == 0) {
+      // Descriptors are computed once: a 128B-swizzled descriptor holds the
+      // address >> 4 in its low 14 bits, and every operand offset below keeps
+      // that field under 2^14 (shared addresses < 256 KB), so an operand at
+      // base + off has descriptor desc(base) + (off >> 4).
       constexpr uint32_t idesc_qk = idesc_bf16(BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(D, 1);
-      const uint32_t qaddr = sbase + L_::kOffQ;
+      const uint64_t qdesc = smem_desc_sw128(sbase + L_::kOffQ, 16, 1024);
+      const uint64_t kdesc0 = smem_desc_sw128(sbase + L_::kOffK, 16, 1024);
+      const uint64_t vdesc0 = smem_desc_sw128(sbase + L_::kOffV, BN * 128, 1024);
       bool ok = mbar_wait(&q_full, 0, &abort_flag);
       auto issue_qk = [&](int j) -> bool {
         const int st = j % KST;
         if (!mbar_wait(&k_full[st], (j / KST) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t kaddr = sbase + L_::kOffK + st * L_::kKV;
+        const uint64_t kdesc = kdesc0 + (uint64_t)(st * (L_::kKV >> 4));
+        const uint32_t d = tS + (j & 1) * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          const uint32_t ob = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-          umma_bf16(tS + (j & 1) * BN, smem_desc_sw128(qaddr + o, 16, 1024), smem_desc_sw128(kaddr + ob, 16, 1024),
-                    idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t o = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t ob = ((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4;
+          umma_bf16(d, qdesc + o, kdesc + ob, idesc_qk, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[j & 1]);
         umma_commit(&k_empty[st]);
@@ -370,16 +376,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t vaddr = sbase + L_::kOffV + (j % VST) * L_::kKV;
+        const uint64_t vdesc = vdesc0 + (uint64_t)((j % VST) * (L_::kKV >> 4));
+        const uint32_t pa = tS + (j & 1) * BN;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
         // key half h: P at columns h*64 .. h*64+31 of the slot (two keys per
         // column), V rows h*64 .. h*64+63, accumulator O_h
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int kk = 0; kk < HC / 16; ++kk) {
-            const uint64_t bd = smem_desc_sw128(vaddr + (h * (HC / 16) + kk) * 2048, BN * 128, 1024);
-            umma_bf16_ts(tO + h * D, tS + (j & 1) * BN + h * HC + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < HC / 16; ++kk)
+            umma_bf16_ts(tO + h * D, pa + h * HC + kk * 8, vdesc + (uint64_t)(((h * (HC / 16) + kk) * 2048) >> 4),
+                         idesc_pv, kk > 0 ? 1u : acc0);
         }
         umma_commit(&pv_done[j & 1]);
         umma_commit(&v_empty[j % VST]);

@@ -91,11 +91,40 @@ def _randint(gen, lo, hi):
     return int(gen.integers(lo, hi))
 
 
+_CHUNK = 1 << 24  # elements per independently seeded stream of a large normal fill
+_PARALLEL_MIN = 1 << 26  # fills at least this large use the chunked streams
+
+
 def _normal(gen, shape, var, dtype=torch.float32):
-    x = torch.from_numpy(gen.standard_normal(shape, dtype=np.float32))
-    if var != 1.0:
-        x.mul_(float(np.sqrt(var)))
-    return x.to(dtype)
+    """N(0, var) samples.  Tensors of 2^26 elements or more (the GB-sized
+    caches of the serving and sweep workloads) are filled in fixed chunks of
+    2^24 elements, chunk i from its own PCG64 stream seeded by a draw of `gen`,
+    on a thread pool: the values depend only on `gen`'s state, not on the
+    threads.  Smaller tensors are drawn from `gen` directly."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    if n < _PARALLEL_MIN:
+        x = torch.from_numpy(gen.standard_normal(shape, dtype=np.float32))
+        if var != 1.0:
+            x.mul_(float(np.sqrt(var)))
+        return x.to(dtype)
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+    seeds = gen.integers(0, 2**63, nchunks)
+    out = torch.empty(n, dtype=dtype)
+    sd = float(np.sqrt(var))
+
+    def fill(i):
+        lo, hi = i * _CHUNK, min(n, (i + 1) * _CHUNK)
+        x = torch.from_numpy(np.random.Generator(np.random.PCG64(int(seeds[i]))).standard_normal(hi - lo,
+                                                                                                dtype=np.float32))
+        if var != 1.0:
+            x.mul_(sd)
+        out[lo:hi] = x.to(dtype)
+
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        list(ex.map(fill, range(nchunks)))
+    return out.view(shape)
 
 
 def random_parent_tree(n, gen):
