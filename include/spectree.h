@@ -131,6 +131,35 @@ spec_status spec_tree_attention(const void* q, const void* k_cache, const void* 
                                 void* workspace, size_t workspace_bytes, int32_t* status,
                                 uint32_t flags, void* stream);
 
+/*
+ * spec_tree_attention without a workspace argument (the pages have no
+ * counterpart of this call).  Some callers cannot allocate device memory where
+ * they run attention: a host framework that passes the library only the
+ * tensors it owns, or a serving loop whose graphs are captured once and must
+ * not pay cudaMalloc's device-wide synchronisation per shape.  When the plan
+ * splits a long key range over several CTAs (long prefixes, few requests), the
+ * splits' partial outputs need scratch; this call keeps it in one fixed
+ * file-scope device array of SPEC_ATTN_NOALLOC_BYTES, which every GPU that
+ * loads the library holds until the process exits.  It calls no allocator.
+ *   Limit: the plan's scratch for this shape, dtype and flags (at most
+ *   spec_attention_workspace_size()) must fit in SPEC_ATTN_NOALLOC_BYTES;
+ *   otherwise SPEC_ERR_UNSUPPORTED and nothing is launched.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   with that device current; make that first call before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the last call's
+ *   contents.  Nothing in it must start at zero (a call writes every partial
+ *   it reads back), but calls whose kernels overlap on the GPU race: serialise
+ *   them (one stream per device).
+ *   Other arguments, outputs and statuses as in spec_tree_attention.
+ */
+#define SPEC_ATTN_NOALLOC_BYTES (16u << 20)
+spec_status spec_tree_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_table, int max_blocks, int block_size, int num_blocks,
+                                        const int32_t* prefix_len, const int32_t* tree_off, const uint64_t* mask,
+                                        int B, int T, int n_max, int max_prefix, int Hq, int Hkv, int D,
+                                        spec_dtype dtype, float scale, void* out, int32_t* status, uint32_t flags,
+                                        void* stream);
+
 /* Bytes of workspace the verifiers take (a small constant: the walk keeps no
  * state in global memory; the argument stays so that callers need not change
  * when a variant needs scratch). */
@@ -197,26 +226,6 @@ spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_pr
                                         int B, int n_max, int V,
                                         int32_t* path, int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
                                         void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
-
-/*
- * spec_tree_verify_stochastic without a workspace argument (the pages have no
- * counterpart of this call).  For callers that cannot allocate device memory
- * at the point where they verify: a host framework that hands the library only
- * its inputs and outputs, or a latency-critical loop that must not pay the
- * device-wide synchronisation of cudaMalloc.  It hands the verifier a fixed
- * file-scope device array as its workspace, which every GPU loading the
- * library keeps until the process exits.
- *   Limits: B <= 16384 and B * n_max <= 262144; larger batches return
- *   SPEC_ERR_UNSUPPORTED and launch nothing.
- *   The first call on each device looks up the array's device address (with
- *   that device current): make that first call before any stream capture.
- *   Arguments, outputs and statuses as in spec_tree_verify_stochastic.
- */
-spec_status spec_tree_verify_stochastic_noalloc(const float* p_logits, const float* q_probs, const int32_t* tokens,
-                                                const int32_t* parent, const int32_t* tree_off,
-                                                const uint32_t* uniforms, int B, int n_max, int V, int32_t* path,
-                                                int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
-                                                int32_t* status, void* stream);
 
 /*
  * KV commit / rollback.  "SpecInfer Guide", "Depth-First Flattening and KV

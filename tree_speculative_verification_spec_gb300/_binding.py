@@ -16,6 +16,7 @@ SPEC_DEV_BAD_TREE, SPEC_DEV_BAD_TOKEN, SPEC_DEV_CAPACITY, SPEC_DEV_TIMEOUT = 1, 
 SPEC_DEV_BAD_BLOCK, SPEC_DEV_BAD_PATH = 16, 32
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_ATTN_AUTO, SPEC_ATTN_CUDA_CORE, SPEC_ATTN_TCGEN05 = 0, 1, 2
+SPEC_ATTN_NOALLOC_BYTES = 16 << 20  # scratch of spec_tree_attention_noalloc
 
 # C signatures (argument ctypes, return ctype) of every exported entry point
 _P, _I, _U32, _U64, _SZ, _F = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_size_t,
@@ -27,10 +28,11 @@ SIGNATURES = {
     "spec_attention_workspace_size": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
     "spec_tree_attention": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _SZ,
                              _P, _U32, _P], _I),
+    "spec_tree_attention_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P,
+                                     _P, _U32, _P], _I),
     "spec_verify_workspace_size": ([_I, _I, _I], _SZ),
     "spec_tree_verify_greedy": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "spec_tree_verify_stochastic": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
-    "spec_tree_verify_stochastic_noalloc": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "spec_kv_commit": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "spec_philox_uniforms": ([_U64, _U32, _P, _I, _I, _P, _P], _I),
     "spec_selftest_bounded_wait": ([_P, _U32, _P], _I),
@@ -116,6 +118,15 @@ def spec_tree_attention(q, k_cache, v_cache, block_table, max_blocks, block_size
         float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), flags, _stream(stream)))
 
 
+def spec_tree_attention_noalloc(q, k_cache, v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len,
+                                tree_off, mask, B, T, n_max, max_prefix, Hq, Hkv, D, scale, out, status,
+                                flags=SPEC_ATTN_AUTO, stream=None):
+    _check("spec_tree_attention_noalloc", lib().spec_tree_attention_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_blocks, block_size, num_blocks,
+        _ptr(prefix_len), _ptr(tree_off), _ptr(mask), B, T, n_max, max_prefix, Hq, Hkv, D, _dtype_code(q),
+        float(scale), _ptr(out), _ptr(status), flags, _stream(stream)))
+
+
 def spec_verify_workspace_size(B, n_max, V):
     return int(lib().spec_verify_workspace_size(B, n_max, V))
 
@@ -136,13 +147,6 @@ def spec_tree_verify_stochastic(p_logits, q_probs, tokens, parent, tree_off, uni
         _ptr(p_logits), _ptr(q_probs), _ptr(tokens), _ptr(parent), _ptr(tree_off), _ptr(uniforms), B, n_max, V,
         _ptr(path), _ptr(accept_len), _ptr(emitted), _ptr(n_emitted), _ptr(workspace), ws_bytes, _ptr(status),
         _stream(stream)))
-
-
-def spec_tree_verify_stochastic_noalloc(p_logits, q_probs, tokens, parent, tree_off, uniforms, B, n_max, V, path,
-                                        accept_len, emitted, n_emitted, status, stream=None):
-    _check("spec_tree_verify_stochastic_noalloc", lib().spec_tree_verify_stochastic_noalloc(
-        _ptr(p_logits), _ptr(q_probs), _ptr(tokens), _ptr(parent), _ptr(tree_off), _ptr(uniforms), B, n_max, V,
-        _ptr(path), _ptr(accept_len), _ptr(emitted), _ptr(n_emitted), _ptr(status), _stream(stream)))
 
 
 def spec_kv_commit(k_cache, v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len, path, path_stride,

@@ -8,6 +8,8 @@
 // K/V tile staged in shared memory serves every query head of the group.
 // Online softmax in the log2 domain; split-KV partials (unnormalised output,
 // running max, running sum) are merged by attn_combine_kernel.
+#include <mutex>
+
 #include "attention.cuh"
 
 #include <algorithm>
@@ -296,6 +298,31 @@ size_t attention_ws_bytes(const AttnPlan& p, int T, int Hq, int D) {
   return ((o + 255) & ~(size_t)255) + ml;
 }
 
+// ---------------------------------------------------------------------------
+// Scratch of spec_tree_attention_noalloc: one file-scope device array (every
+// GPU that loads the library holds it until the process exits).  In host code
+// the symbol names a host-side stand-in, so kernels get the device address,
+// looked up once per device with that device current.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_attn_scratch[SPEC_ATTN_NOALLOC_BYTES];
+
+static std::mutex g_attn_scratch_mutex;
+static void* g_attn_scratch_ptr[128];
+
+// Device address of the scratch array on the current device; NULL when the
+// lookup fails.
+static void* attn_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(g_attn_scratch_mutex);
+  if (!g_attn_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess) return nullptr;
+    g_attn_scratch_ptr[dev] = p;
+  }
+  return g_attn_scratch_ptr[dev];
+}
+
 }  // namespace spectree
 
 using namespace spectree;
@@ -379,6 +406,30 @@ spec_status spec_tree_attention(const void* q, const void* k_cache, const void* 
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
   }
   return SPEC_OK;
+}
+
+// Attention without a workspace argument: the split-KV partials live in the
+// library's fixed scratch array.  The shape checks the plan needs come first;
+// spec_tree_attention then checks everything else and launches.
+spec_status spec_tree_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_table, int max_blocks, int block_size, int num_blocks,
+                                        const int32_t* prefix_len, const int32_t* tree_off, const uint64_t* mask,
+                                        int B, int T, int n_max, int max_prefix, int Hq, int Hkv, int D,
+                                        spec_dtype dtype, float scale, void* out, int32_t* status, uint32_t flags,
+                                        void* stream) {
+  if (B < 0 || T < 0 || n_max < 0 || max_prefix < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (flags > SPEC_ATTN_TCGEN05) return SPEC_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
+  const AttnPlan plan = attention_plan(B, n_max, max_prefix, Hq, Hkv, D, dtype == SPEC_BF16, flags);
+  const size_t need = attention_ws_bytes(plan, T, Hq, D);
+  if (need > (size_t)SPEC_ATTN_NOALLOC_BYTES) return SPEC_ERR_UNSUPPORTED;
+  void* ws = attn_scratch();
+  if (!ws) return SPEC_ERR_CUDA;
+  return spec_tree_attention(q, k_cache, v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len,
+                             tree_off, mask, B, T, n_max, max_prefix, Hq, Hkv, D, dtype, scale, out, ws,
+                             (size_t)SPEC_ATTN_NOALLOC_BYTES, status, flags, stream);
 }
 
 }  // extern "C"

@@ -951,32 +951,6 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
-// ---------------------------------------------------------------------------
-// Scratch of spec_tree_verify_stochastic_noalloc: a file-scope device array
-// (every GPU that loads the library holds it until the process exits).  Host
-// code must not hand the symbol itself to a kernel: it names a host-side
-// stand-in, so the device address is looked up per device.
-// ---------------------------------------------------------------------------
-constexpr size_t kNoAllocBytes = kVerifyWorkspace;
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
-
-static std::mutex g_noalloc_mutex;
-static void* g_noalloc_ptr[128];
-
-// Device address of the scratch array on the current device, looked up once
-// per device; NULL if the lookup failed.
-static void* noalloc_scratch() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_noalloc_ptr[dev] = p;
-  }
-  return g_noalloc_ptr[dev];
-}
-
 }  // namespace spectree
 
 using namespace spectree;
@@ -1048,26 +1022,5 @@ spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_pr
   return verify_dispatch<1>(a, B, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
-
-// Stochastic verification without a workspace argument: for callers that
-// cannot allocate device memory when they verify (a host framework that hands
-// the library only its inputs and outputs, or a latency-critical loop that
-// must not pay cudaMalloc's implicit device synchronisation).  The scratch is
-// a fixed device array shared by every call: concurrent calls on different
-// streams race, and the first call on each device looks up its address.
-spec_status spec_tree_verify_stochastic_noalloc(const float* p_logits, const float* q_probs, const int32_t* tokens,
-                                                const int32_t* parent, const int32_t* tree_off,
-                                                const uint32_t* uniforms, int B, int n_max, int V, int32_t* path,
-                                                int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
-                                                int32_t* status, void* stream) {
-  spec_status s = verify_check(B, n_max, V);
-  if (s != SPEC_OK) return s;
-  if (B == 0 || n_max == 0) return SPEC_OK;
-  if (B > (1 << 14) || (long long)B * n_max > (1LL << 18)) return SPEC_ERR_UNSUPPORTED;
-  void* ws = noalloc_scratch();
-  if (!ws) return SPEC_ERR_CUDA;
-  return spec_tree_verify_stochastic(p_logits, q_probs, tokens, parent, tree_off, uniforms, B, n_max, V, path,
-                                     accept_len, emitted, n_emitted, ws, kNoAllocBytes, status, stream);
-}
 
 }  // extern "C"
