@@ -249,6 +249,29 @@ __device__ __forceinline__ void produce_ring(uint32_t ring, const CUtensorMap* m
     for (int j = max(0, issued - NST); j < issued; ++j) mbar_wait(&full[j % NST], (j / NST) & 1, abort_flag);
 }
 
+// Requests in decreasing key count (prefix + tree nodes; ties by index): the
+// CTAs of grid slot z run the z-th longest request, so the longest K/V
+// streams start in the first wave instead of trailing in the last.  Every CTA
+// ranks the candidates itself from prefix_len and tree_off (O(B^2 / threads)
+// comparisons on a shared copy); batches above kOrderMax keep their order.
+constexpr int kOrderMax = 256;
+__device__ __forceinline__ int request_by_length(const AttnArgs& a, int slot) {
+  if (a.B < 2 || a.B > kOrderMax) return slot;
+  __shared__ int len[kOrderMax];
+  __shared__ int pick;
+  for (int i = threadIdx.x; i < a.B; i += blockDim.x) len[i] = a.prefix_len[i] + (a.tree_off[i + 1] - a.tree_off[i]);
+  if (threadIdx.x == 0) pick = slot;
+  __syncthreads();
+  for (int c = threadIdx.x; c < a.B; c += blockDim.x) {
+    const int L = len[c];
+    int rank = 0;
+    for (int j = 0; j < a.B; ++j) rank += (len[j] > L) || (len[j] == L && j < c);
+    if (rank == slot) pick = c;
+  }
+  __syncthreads();
+  return pick;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -267,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t lbar[4];                 // their exchange, per lane quadrant (bounded waits)
 
   const int mt = blockIdx.x, split = blockIdx.y;
-  const int b = blockIdx.z / a.Hkv, kvh = blockIdx.z % a.Hkv;
+  const int kvh = blockIdx.z % a.Hkv;
+  const int b = request_by_length(a, blockIdx.z / a.Hkv);
   const int off = a.tree_off[b];
   const int n = a.tree_off[b + 1] - off;
   const int P = a.prefix_len[b];
