@@ -241,19 +241,20 @@ __device__ __forceinline__ const unsigned long long* exchange(unsigned long long
   const int s = k & 1;
   const uint32_t parity = (uint32_t)(k >> 1) & 1u;
   ++k;
-  if (threadIdx.x == 0) {
+  // lane r of warp 0 pushes to rank r; a push that lands before this CTA's
+  // expect_tx only drives the transaction count below zero for a moment: the
+  // phase cannot complete before the local arrive below.
+  if (threadIdx.x < C) {
     const uint32_t lbar = smem_addr(&ex.bar[s]), lslot = smem_addr(&ex.v[s][rank]);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(lbar), "r"((uint32_t)(C * 8))
-                 : "memory");
-#pragma unroll
-    for (int r = 0; r < C; ++r) {
-      uint32_t rs, rb;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rs) : "r"(lslot), "r"(r));
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(lbar), "r"(r));
-      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(rs), "l"(val),
-                   "r"(rb)
+    if (threadIdx.x == 0)
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(lbar), "r"((uint32_t)(C * 8))
                    : "memory");
-    }
+    uint32_t rs, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rs) : "r"(lslot), "r"((uint32_t)threadIdx.x));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(lbar), "r"((uint32_t)threadIdx.x));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(rs), "l"(val),
+                 "r"(rb)
+                 : "memory");
   }
   if (!mbar_wait_bounded(&ex.bar[s], parity) && threadIdx.x == 0) atomicOr(status, SPEC_DEV_TIMEOUT);
   return ex.v[s];
@@ -603,12 +604,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
     }
   } else {
     // ------------------------------------------------------------ stochastic
-    // Each thread owns a contiguous range [e0, e1) of the slice (whole float4
-    // when vec), so its fixed-point partial sums are prefix-ordered for the
-    // final sample.
+    // The passes over the slice are warp-interleaved (thread t takes entries
+    // t, t + threads, ..., whole float4 when vec): consecutive lanes touch
+    // consecutive shared-memory words.  The fixed-point sums are exact, so
+    // their order does not matter; only the final sample scans in index order.
     float4* D4 = reinterpret_cast<float4*>(D);
-    const int per = vec ? 4 * (((len >> 2) + kWalkThreads - 1) / kWalkThreads) : (len + kWalkThreads - 1) / kWalkThreads;
-    const int e0 = min(len, (int)threadIdx.x * per), e1 = min(len, e0 + per);
+    const int len4 = len >> 2;
     if (threadIdx.x == 0) sh.aux[0] = 0;
     int u = 0, L = 1;
     auto load_target = [&](int node) {
@@ -663,18 +664,19 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
       // C4: m = max, e = E(l - m), S_0 = sum FX(e)
       float lmax = -INFINITY;
       if (vec) {
-        for (int j = e0 >> 2; j < (e1 >> 2); ++j) {
+#pragma unroll 4
+        for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
           const float4 v = D4[j];
           lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
         }
       } else {
-        for (int j = e0; j < e1; ++j) lmax = fmaxf(lmax, D[j]);
+        for (int j = threadIdx.x; j < len; j += kWalkThreads) lmax = fmaxf(lmax, D[j]);
       }
       const float m = cluster_max<C>(lmax, sh.red, sh.ex, xk, rank, status);
       unsigned long long mp;  // this thread's share of S
       if (vec) {
         FxSum acc;
-        for (int j = e0 >> 2; j < (e1 >> 2); ++j) {
+        for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
           float4 v = D4[j];
           v.x = canon_exp(__fsub_rn(v.x, m));
           v.y = canon_exp(__fsub_rn(v.y, m));
@@ -689,7 +691,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         mp = acc.total();
       } else {
         mp = 0;
-        for (int j = e0; j < e1; ++j) {
+        for (int j = threadIdx.x; j < len; j += kWalkThreads) {
           const float e = canon_exp(__fsub_rn(D[j], m));
           D[j] = e;
           mp += fx(e);
@@ -732,7 +734,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         if (vec) {
           const float y = __frcp_rn(Z);
           FxSum ra;
-          for (int j = e0 >> 2; j < (e1 >> 2); ++j) {
+          for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
             float4 dv = D4[j];
             const float4 qq = Q4[j];
             dv.x = resid_y(dv.x, Z, y, qq.x);
@@ -748,7 +750,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           np = ra.total();
         } else {
           np = 0;
-          for (int j = e0; j < e1; ++j) {
+          for (int j = threadIdx.x; j < len; j += kWalkThreads) {
             const float dn = resid(D[j], Z, __ldg(qrow + x0 + j));
             D[j] = dn;
             np += fx(dn);
@@ -767,7 +769,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           // state stays that of step j-1, and so does every later residual.
           // Rebuild step j-1 from the logits: e, then the nsteps earlier steps.
           frozen = true;
-          for (int j = e0; j < e1; ++j) {
+          for (int j = threadIdx.x; j < len; j += kWalkThreads) {
             float e = canon_exp(__fsub_rn(__ldg(prow + x0 + j), m));
             const float q = vec ? Q[j] : __ldg(qrow + x0 + j);
             for (int s = 0; s < nsteps; ++s) e = resid(e, sh.s.z[s], q);
@@ -791,38 +793,37 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
       const unsigned long long target = sample_target(sh.uterm, S);
       const unsigned long long before = cluster_prefix<C>(lt, sh.ex, xk, rank, status);
       if (target >= before && target - before < lt) {
-        // the token lies in this slice: exclusive scan of the threads' shares
+        // The token lies in this slice.  Warp w owns the contiguous chunk
+        // [w * cs, (w + 1) * cs): chunk totals (any order), their exclusive
+        // prefix in warp order, then the one warp whose chunk holds the target
+        // scans it in index order, 32 entries per round.
         const unsigned long long tl = target - before;
         const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        unsigned long long incl = mp;
+        const int cs = (len + kWarps - 1) / kWarps;
+        const int c0 = min(len, w * cs), c1 = min(len, c0 + cs);
+        unsigned long long wt = 0;
+        for (int j = c0 + lane; j < c1; j += 32) wt += fx(D[j]);
+        wt = warp_sum_u64(wt);
+        if (lane == 0) sh.wsum[w] = wt;
+        __syncthreads();
+        unsigned long long run = 0;
+        for (int q = 0; q < w; ++q) run += sh.wsum[q];
+        if (tl >= run && tl - run < wt) {  // warp-uniform: exactly one warp
+          for (int base = c0; base < c1; base += 32) {
+            const int j = base + lane;
+            unsigned long long incl = j < c1 ? fx(D[j]) : 0ull;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        if (lane == 31) sh.wsum[w] = incl;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          unsigned long long acc = 0;
-          for (int q = 0; q < kWarps; ++q) {
-            const unsigned long long x = sh.wsum[q];
-            sh.wsum[q] = acc;
-            acc += x;
-          }
-        }
-        __syncthreads();
-        const unsigned long long excl = sh.wsum[w] + incl - mp;
-        if (tl >= excl && tl - excl < mp) {
-          unsigned long long acc = excl;
-          int x = e1 - 1;
-          for (int j = e0; j < e1; ++j) {
-            acc += fx(D[j]);
-            if (acc > tl) {
-              x = j;
+            for (int o = 1; o < 32; o <<= 1) {
+              const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, j < c1 && run + incl > tl);
+            if (hit) {
+              if (lane == __ffs(hit) - 1) out_emit[L - 1] = x0 + j;
               break;
             }
+            run += __shfl_sync(0xffffffffu, incl, 31);
           }
-          out_emit[L - 1] = x0 + x;
         }
       }
       break;
