@@ -26,9 +26,33 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tree-verify tokens/s"
 UNIT = "tokens/s"
-WORKLOAD = ("Llama-style decode layer: B=8, 32 query / 8 KV heads, head_dim 128, bf16, prefix 2048, 64-node "
-            "expansion trees (4,2,2,1,1,1,1,1) per request, V=32000, stochastic verification, KV commit")
-N_SETS = 3
+# --workload: 1 is the default line; the others give the same contract line for
+# the wide-ensemble tree, the batched-serving and one linear-vs-tree sweep point
+WORKLOADS = {
+    1: dict(desc="Llama-style decode layer: B=8, 32 query / 8 KV heads, head_dim 128, bf16, prefix 2048, 64-node "
+                 "expansion trees (4,2,2,1,1,1,1,1) per request, V=32000, stochastic verification, KV commit",
+            mode="stochastic", sets=3),
+    2: dict(desc="wide ensemble tree: B=1, 64 query / 8 KV heads, head_dim 128, bf16, prefix 8192, 256-node merge "
+                 "of 4 random depth-8 trees, V=128256, stochastic verification, KV commit",
+            mode="stochastic", sets=3),
+    3: dict(desc="batched serving: B=64, 32 query / 8 KV heads, head_dim 128, bf16, 16-token pages, random block "
+                 "table, prefix U[256,16384], trees U[8,64] nodes, V=32000, greedy verification, KV commit",
+            mode="greedy", sets=1),
+    4: dict(desc="linear-vs-tree sweep point: chains of K+1=9 nodes, B=64, 32 query / 8 KV heads, head_dim 128, bf16, "
+                 "prefix 4096, V=32000, draft = 0.7 p + 0.3 r, stochastic verification, KV commit",
+            mode="stochastic", sets=1),
+}
+
+
+def make_workload(which, seed_base, i):
+    import workloads as W
+    if which == 1:
+        return W.config1(seed=1001 + seed_base + i)
+    if which == 2:
+        return W.config2(seed=1002 + seed_base + i)
+    if which == 3:
+        return W.config3(seed=1003 + seed_base + i)
+    return W.config4(K=8, B=64, tree="chain", alpha=0.3, seed=1004 + seed_base + i)
 
 
 def _dist():
@@ -196,9 +220,9 @@ class ClockSampler:
                 "source": "nvml" if self.thread is not None else "nvidia-smi"}
 
 
-def run_cpu_baseline(w, seconds_cap=30.0):
+def run_cpu_baseline(w, mode="stochastic"):
     """The oracle as it stands (plain C, one thread) on a bounded sample of the
-    same workload: request 0's full pass (mask, attention, stochastic verify,
+    same workload: request 0's full pass (mask, attention, verify in `mode`,
     commit).  Returns (tokens/s, sample description, seconds)."""
     import numpy as np
     import torch
@@ -210,19 +234,24 @@ def run_cpu_baseline(w, seconds_cap=30.0):
 
     def bits(t):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    # a one-request cache: the pages request 0 owns, renumbered 0..nblk-1
     nblk = int((w.prefix_len[b] + (hi - lo) + w.block_size - 1) // w.block_size)
-    bt = w.block_table[b:b + 1, :nblk].contiguous()
-    # a one-request view of the same cache (the blocks this request owns)
+    pages = w.block_table[b, :nblk].long()
+    kc, vc = bits(w.k_cache[pages]), bits(w.v_cache[pages])
+    bt = np.arange(nblk, dtype=np.int32)[None, :]
     t0 = time.perf_counter()
     par = w.parent[lo:hi].numpy()
     toff = np.array([0, hi - lo], np.int32)
     O.mask_build(par, toff, w.n_max)
-    O.tree_attention(bits(w.q[lo:hi]), bits(w.k_cache), bits(w.v_cache), bt.numpy(), w.block_size,
-                     w.prefix_len[b:b + 1].numpy(), toff, par, w.n_max, w.Hq, w.Hkv, w.D, w.dtype, w.scale)
-    r = O.verify_stochastic(w.p_logits[lo:hi].numpy(), w.q_probs[lo:hi].numpy(), w.tokens[lo:hi].numpy(), par, toff,
-                            w.uniforms[lo:hi].numpy().view(np.uint32), w.n_max)
-    O.kv_commit(bits(w.k_cache), bits(w.v_cache), bt.numpy(), w.block_size, w.prefix_len[b:b + 1].numpy(),
-                r["path"], r["accept_len"], w.Hkv, w.D, w.dtype, np.zeros(1, np.int32))
+    O.tree_attention(bits(w.q[lo:hi]), kc, vc, bt, w.block_size, w.prefix_len[b:b + 1].numpy(), toff, par, w.n_max,
+                     w.Hq, w.Hkv, w.D, w.dtype, w.scale)
+    if mode == "greedy":
+        r = O.verify_greedy(w.p_logits[lo:hi].numpy(), w.tokens[lo:hi].numpy(), par, toff, w.n_max)
+    else:
+        r = O.verify_stochastic(w.p_logits[lo:hi].numpy(), w.q_probs[lo:hi].numpy(), w.tokens[lo:hi].numpy(), par,
+                                toff, w.uniforms[lo:hi].numpy().view(np.uint32), w.n_max)
+    O.kv_commit(kc, vc, bt, w.block_size, w.prefix_len[b:b + 1].numpy(), r["path"], r["accept_len"], w.Hkv, w.D,
+                w.dtype, np.zeros(1, np.int32))
     dt = time.perf_counter() - t0
     tokens = int(r["n_emitted"][0])
     return tokens / dt, f"request 0 of the batch (1 of {w.B}): full pass in the oracle, {dt:.2f} s", dt
@@ -233,11 +262,11 @@ def bench_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return 0
-    import workloads as W
-    w = W.config1()
+    wl = WORKLOADS[args.workload]
+    w = make_workload(args.workload, 0, 0)
     times, toks = [], 0
     for i in range(args.warmup + args.steps):
-        v, sample, dt = run_cpu_baseline(w)
+        v, sample, dt = run_cpu_baseline(w, args.mode)
         if i >= args.warmup:
             times.append(dt)
             toks = v * dt
@@ -246,7 +275,7 @@ def bench_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": sample},
+            "config": {"workload": wl["desc"], "sample": sample},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -284,9 +313,11 @@ def bench_gpu(args):
     S.lib()
     dev = torch.device("cuda", local)
 
+    wl = WORKLOADS[args.workload]
+    n_sets = wl["sets"]
     sets, passes, works = [], [], []
-    for i in range(N_SETS):
-        w = W.config1(seed=1001 + 97 * rank + i)
+    for i in range(n_sets):
+        w = make_workload(args.workload, 97 * rank, i)
         works.append(w)
         d = DeviceBatch.from_workload(w, device=dev)
         sets.append(d)
@@ -304,14 +335,14 @@ def bench_gpu(args):
 
     # eager warm-up (first calls set kernel attributes and look up driver entry points)
     for i in range(args.warmup):
-        step(passes[i % N_SETS])
+        step(passes[i % n_sets])
     torch.cuda.synchronize()
 
     def capture(skip=None):
         """One CUDA graph of one pass per input set (no event nodes inside)."""
         cap = torch.cuda.Stream(dev)
         gs = []
-        for i in range(N_SETS):
+        for i in range(n_sets):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
                 step(passes[i], skip)
@@ -325,7 +356,7 @@ def bench_gpu(args):
         """K replays bracketed by CUDA events on the replay stream (barrier and
         synchronize on both sides); returns milliseconds."""
         for i in range(args.warmup):
-            graphs[i % N_SETS].replay()
+            graphs[i % n_sets].replay()
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
@@ -333,7 +364,7 @@ def bench_gpu(args):
         torch.cuda.synchronize()
         a.record(stream)
         for i in range(args.steps):
-            graphs[i % N_SETS].replay()
+            graphs[i % n_sets].replay()
         b.record(stream)
         torch.cuda.synchronize()
         if world > 1:
@@ -353,14 +384,14 @@ def bench_gpu(args):
     # emitted tokens per step (verify inputs do not change between steps of one set)
     tokens_per_set = [int(p.n_emitted[:p.batch.B].sum()) for p in passes]
     status_ok = all(int(p.status[:p.batch.B].abs().sum()) == 0 for p in passes)
-    tokens = sum(tokens_per_set[i % N_SETS] for i in range(args.steps))
+    tokens = sum(tokens_per_set[i % n_sets] for i in range(args.steps))
     elapsed_ms, tokens = aggregate_replicas(elapsed_ms, float(tokens), dev)
     value = tokens / (elapsed_ms / 1e3)
 
     # --- e2e through the C ABI with host buffers: per step, H2D of the step's
     # inputs from pinned memory, the five calls, D2H of the emitted tokens; the KV
     # cache is resident state.
-    e2e = run_e2e(args, works, sets, passes, stream, dev)
+    e2e = run_e2e(args, works, sets, passes, stream, dev, n_sets)
 
     # --- roofline of the dominant kernel
     peak, peak_kind = _peaks()
@@ -389,8 +420,9 @@ def bench_gpu(args):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "verify": args.mode, "input_sets": N_SETS,
-                       "l2": "3 rotating input sets of ~205 MB each (inputs larger than L2)",
+            "config": {"workload": wl["desc"], "verify": args.mode, "input_sets": n_sets,
+                       "l2": (f"{n_sets} rotating input sets of {_set_mb(works[0]):.0f} MB each (inputs larger than L2)"
+                              if n_sets > 1 else f"one input set of {_set_mb(works[0]):.0f} MB (larger than L2)"),
                        "launch": "one CUDA graph per step (the C-ABI calls of the pass captured, no event nodes)",
                        "kernel_timing": "per kernel: (K timed steps - the same K steps without that kernel) / K, "
                                         "each run bracketed by CUDA events on the replay stream",
@@ -403,7 +435,7 @@ def bench_gpu(args):
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind},
             "kernels": kernels}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, _ = run_cpu_baseline(works[0])
+        v, sample, _ = run_cpu_baseline(works[0], args.mode)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -436,7 +468,13 @@ def _attn_splits(vp):
     return 2 if S.spec_attention_workspace_size(b.B, b.T, b.n_max, b.max_prefix, b.Hq, b.Hkv, b.D) > 256 else 1
 
 
-def run_e2e(args, works, sets, passes, stream, dev):
+def _set_mb(w):
+    """Bytes one pass reads from its input set (cache, queries, rows), in MB."""
+    ts = (w.k_cache, w.v_cache, w.q, w.p_logits, w.q_probs)
+    return sum(t.numel() * t.element_size() for t in ts) / 1e6
+
+
+def run_e2e(args, works, sets, passes, stream, dev, n_sets):
     import torch
     steps = max(3, args.steps)
     host = []
@@ -450,7 +488,7 @@ def run_e2e(args, works, sets, passes, stream, dev):
     d2h = out_tok[0].numel() * 4 + out_n[0].numel() * 4
 
     def e2e_step(i):
-        j = i % N_SETS
+        j = i % n_sets
         d, vp, h = sets[j], passes[j], host[j]
         for k, t in h.items():
             getattr(d, k).copy_(t, non_blocking=True)
@@ -468,7 +506,7 @@ def run_e2e(args, works, sets, passes, stream, dev):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
-    toks = sum(int(out_n[i % N_SETS].sum()) for i in range(steps))
+    toks = sum(int(out_n[i % n_sets].sum()) for i in range(steps))
     return {"value": toks / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms / steps}
 
@@ -479,12 +517,15 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--mode", default="stochastic", choices=["stochastic", "greedy"])
+    ap.add_argument("--mode", default=None, choices=["stochastic", "greedy"])
+    ap.add_argument("--workload", type=int, default=1, choices=sorted(WORKLOADS))
     ap.add_argument("--attn-flags", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.mode is None:
+        args.mode = WORKLOADS[args.workload]["mode"]
     if args.impl == "reference":
         return bench_reference(args)
     return bench_gpu(args)
