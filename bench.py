@@ -415,7 +415,7 @@ def bench_gpu(args):
     kernels["verify"]["gbs_all_rows"] = full_rows / (avg["verify"] * 1e-3) / 1e9 if avg["verify"] > 0 else None
     achieved = kernels[dom]["gbs"]
     launches_per_step = 4 + (1 if _attn_splits(passes[0]) > 1 else 0)
-    traffic = _profiled_traffic(dom, args.mode)
+    traffic = _profiled_traffic(dom, args.mode, args.workload)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
@@ -444,7 +444,7 @@ def bench_gpu(args):
     return 0
 
 
-def _profiled_traffic(kernel, mode):
+def _profiled_traffic(kernel, mode, workload=1):
     """DRAM bytes per launch (read + write) of the dominant kernel from the
     committed ncu summary, or None when the summary is missing or the kernel
     source changed since the capture."""
@@ -455,8 +455,8 @@ def _profiled_traffic(kernel, mode):
         digest = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
         for line in open(os.path.join(ROOT, "profiles", "traffic.md")):
             f = [x.strip() for x in line.strip().strip("|").split("|")]
-            if len(f) >= 4 and f[0] == kernel and f[1] == mode and f[2] == digest:
-                return float(f[3])
+            if len(f) >= 5 and f[0] == kernel and f[1] == str(workload) and f[2] == mode and f[3] == digest:
+                return float(f[4])
     except (OSError, ValueError):
         pass
     return None
