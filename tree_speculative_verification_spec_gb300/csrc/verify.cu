@@ -137,6 +137,61 @@ __device__ __forceinline__ float resid_y(float d, float Z, float y, float q) {
   return diff > 0.0f ? diff : 0.0f;
 }
 
+// Two entries at once: the same single IEEE operations on the f32x2 pipe
+// (fma.f32x2 is two fused multiply-adds; a - b is a + (-b)), so each lane is
+// bit-identical to the scalar functions above.
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+
+__device__ __forceinline__ float2 canon_exp2(float2 x) {
+  const float2 t = __fmul2_rn(x, f2(0x1.715476p+0f));
+  const float2 big = __fadd2_rn(t, f2(12582912.0f));
+  const float2 n = __fadd2_rn(big, f2(-12582912.0f));
+  const int nx = __float_as_int(big.x) - 0x4B400000, ny = __float_as_int(big.y) - 0x4B400000;
+  const float2 nn = neg2(n);
+  float2 r = __ffma2_rn(nn, f2(0x1.62e4p-1f), x);
+  r = __ffma2_rn(nn, f2(0x1.7f7d1cp-20f), r);
+  float2 p = f2(0x1.a01a02p-13f);
+  p = __ffma2_rn(p, r, f2(0x1.6c16c2p-10f));
+  p = __ffma2_rn(p, r, f2(0x1.111112p-7f));
+  p = __ffma2_rn(p, r, f2(0x1.555556p-5f));
+  p = __ffma2_rn(p, r, f2(0x1.555556p-3f));
+  p = __ffma2_rn(p, r, f2(0.5f));
+  p = __ffma2_rn(p, r, f2(1.0f));
+  p = __ffma2_rn(p, r, f2(1.0f));
+  // below -87 (or NaN) the scale bits are meaningless: the result is selected away
+  float2 e = __fmul2_rn(p, make_float2(__int_as_float((nx + 127) << 23), __int_as_float((ny + 127) << 23)));
+  e.x = x.x >= -87.0f ? e.x : 0.0f;
+  e.y = x.y >= -87.0f ? e.y : 0.0f;
+  return e;
+}
+
+__device__ __forceinline__ void fx_add2(FxSum& acc, float2 v) {
+  if (v.x <= 1.0f && v.y <= 1.0f) {
+    const float2 y1 = __fmul2_rn(v, f2(0x1p23f));
+    const float2 t = __fadd2_rz(y1, f2(0x1p23f));
+    const float2 f = __fadd2_rn(y1, neg2(__fadd2_rn(t, f2(-0x1p23f))));
+    const float2 t2 = __fadd2_rz(__fmul2_rn(f, f2(0x1p23f)), f2(0x1p23f));
+    acc.a += (__float_as_uint(t.x) - 0x4B000000u) + (__float_as_uint(t.y) - 0x4B000000u);
+    acc.b += (__float_as_uint(t2.x) - 0x4B000000u) + (__float_as_uint(t2.y) - 0x4B000000u);
+  } else {
+    acc.add(v.x);
+    acc.add(v.y);
+  }
+}
+
+__device__ __forceinline__ float2 resid_y2(float2 d, float Z, float y, float2 q) {
+  float2 r;
+  if (d.x >= 0x1p-100f && d.x <= 1.0f && d.y >= 0x1p-100f && d.y <= 1.0f) {
+    const float2 q0 = __fmul2_rn(d, f2(y));
+    const float2 rem = __ffma2_rn(neg2(q0), f2(Z), d);
+    r = __ffma2_rn(rem, f2(y), q0);
+    const float2 diff = __fadd2_rn(r, neg2(q));
+    return make_float2(diff.x > 0.0f ? diff.x : 0.0f, diff.y > 0.0f ? diff.y : 0.0f);
+  }
+  return make_float2(resid_y(d.x, Z, y, q.x), resid_y(d.y, Z, y, q.y));
+}
+
 // ---------------------------------------------------------------------------
 // Block reductions
 // ---------------------------------------------------------------------------
@@ -677,16 +732,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
       if (vec) {
         FxSum acc;
         for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
-          float4 v = D4[j];
-          v.x = canon_exp(__fsub_rn(v.x, m));
-          v.y = canon_exp(__fsub_rn(v.y, m));
-          v.z = canon_exp(__fsub_rn(v.z, m));
-          v.w = canon_exp(__fsub_rn(v.w, m));
-          D4[j] = v;
-          acc.add(v.x);
-          acc.add(v.y);
-          acc.add(v.z);
-          acc.add(v.w);
+          const float4 v = D4[j];
+          const float2 lo = canon_exp2(__fadd2_rn(make_float2(v.x, v.y), f2(-m)));
+          const float2 hi = canon_exp2(__fadd2_rn(make_float2(v.z, v.w), f2(-m)));
+          D4[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          fx_add2(acc, lo);
+          fx_add2(acc, hi);
         }
         mp = acc.total();
       } else {
@@ -735,17 +786,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           const float y = __frcp_rn(Z);
           FxSum ra;
           for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
-            float4 dv = D4[j];
+            const float4 dv = D4[j];
             const float4 qq = Q4[j];
-            dv.x = resid_y(dv.x, Z, y, qq.x);
-            dv.y = resid_y(dv.y, Z, y, qq.y);
-            dv.z = resid_y(dv.z, Z, y, qq.z);
-            dv.w = resid_y(dv.w, Z, y, qq.w);
-            D4[j] = dv;
-            ra.add(dv.x);
-            ra.add(dv.y);
-            ra.add(dv.z);
-            ra.add(dv.w);
+            const float2 lo = resid_y2(make_float2(dv.x, dv.y), Z, y, make_float2(qq.x, qq.y));
+            const float2 hi = resid_y2(make_float2(dv.z, dv.w), Z, y, make_float2(qq.z, qq.w));
+            D4[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            fx_add2(ra, lo);
+            fx_add2(ra, hi);
           }
           np = ra.total();
         } else {
