@@ -414,7 +414,7 @@ def bench_gpu(args):
     kernels["verify"]["bytes_all_rows"] = full_rows
     kernels["verify"]["gbs_all_rows"] = full_rows / (avg["verify"] * 1e-3) / 1e9 if avg["verify"] > 0 else None
     achieved = kernels[dom]["gbs"]
-    launches_per_step = 4 + (1 if _attn_splits(passes[0]) > 1 else 0)
+    launches_per_step = 4 + (1 if _attn_splits(passes[0]) > 1 else 0) + (1 if _verify_uses_stats(w0, args.mode) else 0)
     traffic = _profiled_traffic(dom, args.mode, args.workload)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -460,6 +460,21 @@ def _profiled_traffic(kernel, mode, workload=1):
     except (OSError, ValueError):
         pass
     return None
+
+
+def _verify_uses_stats(w, mode):
+    """Whether the stochastic verifier launches its row-statistics kernel: the
+    library does when the walk gets at most two CTAs per request (its cluster
+    size: about one CTA per SM over the batch, wide enough for 16384-entry
+    vocabulary slices)."""
+    if mode != "stochastic":
+        return False
+    C = 1
+    while C < 8 and w.B * C * 2 <= 152:
+        C *= 2
+    while C < 8 and (w.V + C - 1) // C > 16384:
+        C *= 2
+    return C <= 2
 
 
 def _attn_splits(vp):

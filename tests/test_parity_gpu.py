@@ -370,6 +370,29 @@ def test_sweep_points_parity(point):
         _assert_verify_equal(_gpu_verify(w, mode), ref_v, w.B)
 
 
+@pytest.mark.parametrize("tree", ["chain", "random"])
+def test_stochastic_with_and_without_row_statistics(tree):
+    """Large batches verify with precomputed row statistics (a workspace of
+    spec_verify_workspace_size bytes); a 256-byte workspace makes the walk
+    compute them itself.  Both equal the oracle bit for bit."""
+    w = W.config4(K=6, B=80, tree=tree, alpha=0.4, prefix=16)
+    ref = oracle_stochastic(w)
+    d = DeviceBatch.from_workload(w)
+    full = S.spec_verify_workspace_size(d.B, d.n_max, d.V)
+    assert full > 256
+    for ws_bytes in (full, 256):
+        i32 = dict(dtype=torch.int32, device="cuda")
+        path, emit = torch.full((d.B, d.n_max), 7, **i32), torch.full((d.B, d.n_max), 7, **i32)
+        alen, nem, st = torch.zeros(d.B, **i32), torch.zeros(d.B, **i32), torch.zeros(d.B, **i32)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        S.spec_tree_verify_stochastic(d.p_logits, d.q_probs, d.tokens, d.parent, d.tree_off, d.uniforms, d.B,
+                                      d.n_max, d.V, path, alen, emit, nem, ws, st)
+        torch.cuda.synchronize()
+        got = dict(path=path.cpu().numpy(), accept_len=alen.cpu().numpy(), emitted=emit.cpu().numpy(),
+                   n_emitted=nem.cpu().numpy(), status=st.cpu().numpy())
+        _assert_verify_equal(got, ref, w.B)
+
+
 # ---------------------------------------------------------------- commit ----
 
 def _oracle_commit(w, ref_v):

@@ -17,6 +17,7 @@
 // and evaluates itself.  While a node is processed, the row slices its
 // children would need next are prefetched into L2.  No CTA waits for a CTA of
 // another cluster.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -93,6 +94,12 @@ struct FxSum {
   }
   __device__ __forceinline__ unsigned long long total() const {
     return ((unsigned long long)a << 23) + (unsigned long long)b + big;
+  }
+  // moves A and B into the 64-bit total (callers adding more than 511 terms)
+  __device__ __forceinline__ void flush() {
+    big = total();
+    a = 0;
+    b = 0;
   }
 };
 
@@ -367,6 +374,14 @@ __device__ __forceinline__ void cluster_argmax(float& v, int& i, Red& red, Exch&
 // Walk helpers
 // ---------------------------------------------------------------------------
 
+// Row statistics of one node's target row under the arithmetic contract:
+// m = max l and S = sum FX(E(l - m)) (exact).
+struct RowStats {
+  float m;
+  uint32_t pad;
+  unsigned long long S;
+};
+
 struct VerifyArgs {
   const float* p_logits;
   const float* q_probs;
@@ -381,6 +396,7 @@ struct VerifyArgs {
   int32_t* emitted;
   int32_t* n_emitted;
   int32_t* status;
+  const RowStats* stats;  // stochastic: every node's row statistics, or null (the walk computes them)
 };
 
 struct WalkShared {
@@ -473,6 +489,75 @@ __device__ void clear_request(const VerifyArgs& a, int b) {
   if (threadIdx.x == 0) {
     a.accept_len[b] = 0;
     a.n_emitted[b] = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Row statistics of every node, one CTA per (request, node), data-parallel
+// over the whole GPU: for large batches the walk then enters an accepted node
+// with a few shared-memory reads instead of two passes over the node's row.
+// The same contract operations as the walk's own passes, so m and S are
+// bit-identical to what the walk would compute.  256 threads per CTA, so that
+// several rows are resident per SM and one row's loads overlap another's
+// arithmetic; the second pass reads the row again from L2.
+// ---------------------------------------------------------------------------
+constexpr int kStatsThreads = 256;
+constexpr int kStatsWarps = kStatsThreads / 32;
+
+__global__ void __launch_bounds__(kStatsThreads) row_stats_kernel(VerifyArgs a, RowStats* stats) {
+  __shared__ float smax[kStatsWarps];
+  __shared__ unsigned long long ssum[kStatsWarps];
+  const int b = blockIdx.x / a.n_max, u = blockIdx.x % a.n_max;
+  const int off = a.tree_off[b];
+  const int n = a.tree_off[b + 1] - off;
+  if (n < 1 || n > a.n_max || u >= n) return;  // uniform across the CTA
+  const int V = a.V, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* row = a.p_logits + (size_t)(off + u) * V;
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  float lmax = -INFINITY;
+  if (a.vec) {
+#pragma unroll 4
+    for (int j = threadIdx.x; j < (V >> 2); j += kStatsThreads) {
+      const float4 v = __ldg(r4 + j);
+      lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+    }
+  } else {
+    for (int j = threadIdx.x; j < V; j += kStatsThreads) lmax = fmaxf(lmax, __ldg(row + j));
+  }
+  lmax = warp_max_f(lmax);
+  if (lane == 0) smax[w] = lmax;
+  __syncthreads();
+  float m = smax[0];
+#pragma unroll
+  for (int k = 1; k < kStatsWarps; ++k) m = fmaxf(m, smax[k]);
+  unsigned long long part;
+  if (a.vec) {
+    FxSum acc;
+    int it = 0;
+#pragma unroll 4
+    for (int j = threadIdx.x; j < (V >> 2); j += kStatsThreads) {
+      const float4 v = __ldg(r4 + j);
+      fx_add2(acc, canon_exp2(__fadd2_rn(make_float2(v.x, v.y), f2(-m))));
+      fx_add2(acc, canon_exp2(__fadd2_rn(make_float2(v.z, v.w), f2(-m))));
+      if ((++it & 63) == 0) acc.flush();  // 256 terms: A and B stay below 2^32
+    }
+    part = acc.total();
+  } else {
+    part = 0;
+    for (int j = threadIdx.x; j < V; j += kStatsThreads) part += fx(canon_exp(__fsub_rn(__ldg(row + j), m)));
+  }
+  part = warp_sum_u64(part);
+  if (lane == 0) ssum[w] = part;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long S = 0;
+#pragma unroll
+    for (int k = 0; k < kStatsWarps; ++k) S += ssum[k];
+    RowStats r;
+    r.m = m;
+    r.pad = 0;
+    r.S = S;
+    stats[off + u] = r;
   }
 }
 
@@ -665,6 +750,28 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
     // their order does not matter; only the final sample scans in index order.
     float4* D4 = reinterpret_cast<float4*>(D);
     const int len4 = len >> 2;
+    const bool use_stats = a.stats != nullptr;
+    bool loaded = true;  // D holds the current node's slice (the root's copy is in flight)
+    // statistics mode: every node's entries, read once at the start (the
+    // second draft buffer's room holds them): its logit and draft
+    // probability at its token (rows of its parent), its acceptance word and
+    // its row statistics
+    float* NX = Qb + a.slice;
+    float* NQ = NX + a.n_max;
+    uint32_t* NU = reinterpret_cast<uint32_t*>(NQ + a.n_max);
+    float* NM = reinterpret_cast<float*>(NU + a.n_max);
+    unsigned long long* NS = reinterpret_cast<unsigned long long*>(NM + a.n_max);
+    if (use_stats) {
+      for (int c = threadIdx.x; c < n; c += kWalkThreads) {
+        const int pc = sh.par[c], t = sh.tok[c];
+        NX[c] = c > 0 ? __ldcg(a.p_logits + (size_t)(off + pc) * V + t) : 0.0f;
+        NQ[c] = c > 0 ? __ldcg(a.q_probs + (size_t)(off + pc) * V + t) : 0.0f;
+        NU[c] = a.uniforms[off + c].x;
+        const RowStats r = a.stats[off + c];
+        NM[c] = r.m;
+        NS[c] = r.S;
+      }
+    }
     if (threadIdx.x == 0) sh.aux[0] = 0;
     int u = 0, L = 1;
     auto load_target = [&](int node) {
@@ -692,75 +799,127 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
       // loads in flight through the max and exp passes, stored before the sum
       float rx[2], rq[2];
       uint32_t ru[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int i = threadIdx.x + r * kWalkThreads;
-        if (i < k) {
-          const int c = sh.s.kids[i];
-          const int t = sh.tok[c];
-          rx[r] = __ldcg(prow + t);
-          rq[r] = __ldcg(qrow + t);
-          ru[r] = a.uniforms[off + c].x;
-          if (vec) prefetch_l2(a.p_logits + (size_t)(off + c) * V + x0, (uint32_t)len * 4);
-        }
-      }
-      const uint32_t uterm = threadIdx.x == 0 ? a.uniforms[off + u].y : 0u;
-      // the draft slice into the buffer of this node's parity; its previous copy
-      // (two nodes back) was waited for here or at a rejection
-      const int qb = (L - 1) & 1;
+      uint32_t uterm = 0;
+      // the draft slice: without statistics, into the buffer of this node's
+      // parity at once (its previous copy, two nodes back, was waited for here
+      // or at a rejection); with statistics, into buffer 0 at the node's first
+      // rejection
+      const int qb = use_stats ? 0 : (L - 1) & 1;
       float* Q = Qb + qb * a.slice;
       const float4* Q4 = reinterpret_cast<const float4*>(Q);
-      if (qpend & (1u << qb)) wait_draft(sh, qb, qphase, qpend, status);
-      if (k > 0 && vec && len > 0) {
-        if (threadIdx.x == 0) start_copy(Q, qrow + x0, (uint32_t)len * 4, &sh.qbar[qb]);
-        qpend |= 1u << qb;
+      bool q_ready = !use_stats;
+      if (!use_stats) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int i = threadIdx.x + r * kWalkThreads;
+          if (i < k) {
+            const int c = sh.s.kids[i];
+            const int t = sh.tok[c];
+            rx[r] = __ldcg(prow + t);
+            rq[r] = __ldcg(qrow + t);
+            ru[r] = a.uniforms[off + c].x;
+            if (vec) prefetch_l2(a.p_logits + (size_t)(off + c) * V + x0, (uint32_t)len * 4);
+          }
+        }
+        if (threadIdx.x == 0) uterm = a.uniforms[off + u].y;
+        if (qpend & (1u << qb)) wait_draft(sh, qb, qphase, qpend, status);
+        if (k > 0 && vec && len > 0) {
+          if (threadIdx.x == 0) start_copy(Q, qrow + x0, (uint32_t)len * 4, &sh.qbar[qb]);
+          qpend |= 1u << qb;
+        }
       }
 
-      // C4: m = max, e = E(l - m), S_0 = sum FX(e)
-      float lmax = -INFINITY;
-      if (vec) {
+      // C4: m = max, e = E(l - m), S_0 = sum FX(e); with precomputed row
+      // statistics the slice is left alone until a rejection or the sample
+      // needs the weights
+      float m;
+      unsigned long long mp = 0, lt = 0, S;
+      bool have_e;  // D holds this node's weights (e, or a residual)
+      if (use_stats) {
+        m = NM[u];
+        S = NS[u];
+        have_e = false;
+        for (int i = threadIdx.x; i < k; i += kWalkThreads) {
+          const int c = sh.s.kids[i];
+          sh.s.cx[i] = NX[c];
+          sh.s.cq[i] = NQ[c];
+          sh.s.cu[i] = NU[c];
+        }
+        __syncthreads();
+      } else {
+        float lmax = -INFINITY;
+        if (vec) {
 #pragma unroll 4
-        for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
-          const float4 v = D4[j];
-          lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+          for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
+            const float4 v = D4[j];
+            lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+          }
+        } else {
+          for (int j = threadIdx.x; j < len; j += kWalkThreads) lmax = fmaxf(lmax, D[j]);
         }
-      } else {
-        for (int j = threadIdx.x; j < len; j += kWalkThreads) lmax = fmaxf(lmax, D[j]);
-      }
-      const float m = cluster_max<C>(lmax, sh.red, sh.ex, xk, rank, status);
-      unsigned long long mp;  // this thread's share of S
-      if (vec) {
-        FxSum acc;
-        for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
-          const float4 v = D4[j];
-          const float2 lo = canon_exp2(__fadd2_rn(make_float2(v.x, v.y), f2(-m)));
-          const float2 hi = canon_exp2(__fadd2_rn(make_float2(v.z, v.w), f2(-m)));
-          D4[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
-          fx_add2(acc, lo);
-          fx_add2(acc, hi);
+        m = cluster_max<C>(lmax, sh.red, sh.ex, xk, rank, status);
+        if (vec) {
+          FxSum acc;
+          for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
+            const float4 v = D4[j];
+            const float2 lo = canon_exp2(__fadd2_rn(make_float2(v.x, v.y), f2(-m)));
+            const float2 hi = canon_exp2(__fadd2_rn(make_float2(v.z, v.w), f2(-m)));
+            D4[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            fx_add2(acc, lo);
+            fx_add2(acc, hi);
+          }
+          mp = acc.total();
+        } else {
+          mp = 0;
+          for (int j = threadIdx.x; j < len; j += kWalkThreads) {
+            const float e = canon_exp(__fsub_rn(D[j], m));
+            D[j] = e;
+            mp += fx(e);
+          }
         }
-        mp = acc.total();
-      } else {
-        mp = 0;
-        for (int j = threadIdx.x; j < len; j += kWalkThreads) {
-          const float e = canon_exp(__fsub_rn(D[j], m));
-          D[j] = e;
-          mp += fx(e);
-        }
-      }
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int i = threadIdx.x + r * kWalkThreads;
-        if (i < k) {
-          sh.s.cx[i] = rx[r];
-          sh.s.cq[i] = rq[r];
-          sh.s.cu[i] = ru[r];
+        for (int r = 0; r < 2; ++r) {
+          const int i = threadIdx.x + r * kWalkThreads;
+          if (i < k) {
+            sh.s.cx[i] = rx[r];
+            sh.s.cq[i] = rq[r];
+            sh.s.cu[i] = ru[r];
+          }
         }
+        if (threadIdx.x == 0) sh.uterm = uterm;
+        // lt: this CTA's share of S (the sum publishes the stores above)
+        S = cluster_sum<C>(mp, sh.red, sh.ex, xk, rank, status, lt);
+        have_e = true;
       }
-      if (threadIdx.x == 0) sh.uterm = uterm;
-      unsigned long long lt;  // this CTA's share of S (the sum publishes the stores above)
-      unsigned long long S = cluster_sum<C>(mp, sh.red, sh.ex, xk, rank, status, lt);
       float Z = z_of(S);
+      // with row statistics: the node's weights e = E(l - m) in D, and this
+      // CTA's share lt of S, made when a rejection or the sample needs them
+      auto ensure_e = [&]() {
+        if (have_e) return;
+        if (!loaded) load_target(u);
+        loaded = true;
+        if (vec) {
+          FxSum acc;
+          for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
+            const float4 v = D4[j];
+            const float2 lo = canon_exp2(__fadd2_rn(make_float2(v.x, v.y), f2(-m)));
+            const float2 hi = canon_exp2(__fadd2_rn(make_float2(v.z, v.w), f2(-m)));
+            D4[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            fx_add2(acc, lo);
+            fx_add2(acc, hi);
+          }
+          mp = acc.total();
+        } else {
+          mp = 0;
+          for (int j = threadIdx.x; j < len; j += kWalkThreads) {
+            const float e = canon_exp(__fsub_rn(D[j], m));
+            D[j] = e;
+            mp += fx(e);
+          }
+        }
+        lt = block_sum_u64(mp, sh.red);  // its barriers also publish D
+        have_e = true;
+      };
 
       // C5 / C6: children in increasing index, each against the residual left
       // by the siblings rejected before it
@@ -779,6 +938,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           break;
         }
         if (frozen) continue;  // the next residual would be the same all-zero one
+        if (!q_ready) {  // statistics mode: this node's draft slice, on its first rejection,
+          if (vec && len > 0) {  // in flight while the weights are made
+            if (threadIdx.x == 0) start_copy(Q, qrow + x0, (uint32_t)len * 4, &sh.qbar[0]);
+            qpend |= 1u;
+          }
+          q_ready = true;
+        }
+        ensure_e();
         if (qpend & (1u << qb)) wait_draft(sh, qb, qphase, qpend, status);
         if (threadIdx.x == 0) sh.s.z[nsteps] = Z;  // read only after the exchange below
         unsigned long long np;
@@ -831,19 +998,25 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         u = accepted;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();  // D and Q are no longer read before the copies overwrite them
-        load_target(u);
+        if (use_stats) loaded = false;
+        else load_target(u);
         continue;
       }
 
       // C7: sample from the current weights: the smallest x whose fixed-point
       // prefix sum exceeds floor(U * S / 2^32)
+      ensure_e();
+      if (use_stats) {
+        if (threadIdx.x == 0) sh.uterm = a.uniforms[off + u].y;
+        __syncthreads();
+      }
       const unsigned long long target = sample_target(sh.uterm, S);
       const unsigned long long before = cluster_prefix<C>(lt, sh.ex, xk, rank, status);
       if (target >= before && target - before < lt) {
         // The token lies in this slice.  Warp w owns the contiguous chunk
         // [w * cs, (w + 1) * cs): chunk totals (any order), their exclusive
         // prefix in warp order, then the one warp whose chunk holds the target
-        // scans it in index order, 32 entries per round.
+        // finds it (per-lane sub-range totals, then one lane's in-order scan).
         const unsigned long long tl = target - before;
         const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const int cs = (len + kWarps - 1) / kWarps;
@@ -856,20 +1029,31 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         unsigned long long run = 0;
         for (int q = 0; q < w; ++q) run += sh.wsum[q];
         if (tl >= run && tl - run < wt) {  // warp-uniform: exactly one warp
-          for (int base = c0; base < c1; base += 32) {
-            const int j = base + lane;
-            unsigned long long incl = j < c1 ? fx(D[j]) : 0ull;
+          // lane l owns the contiguous sub-range [s0, s1) of the chunk: its
+          // total, a warp scan of the totals, then the one lane whose
+          // sub-range holds the target scans it in index order
+          const int sub = (c1 - c0 + 31) >> 5;
+          const int s0 = min(c1, c0 + lane * sub), s1 = min(c1, s0 + sub);
+          unsigned long long ls = 0;
+          for (int j = s0; j < s1; ++j) ls += fx(D[j]);
+          unsigned long long incl = ls;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += y;
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const unsigned hit = __ballot_sync(0xffffffffu, run + incl > tl);
+          if (hit && lane == __ffs(hit) - 1) {  // the first such lane has a non-empty sub-range
+            unsigned long long acc = run + incl - ls;
+            int x = s1 - 1;
+            for (int j = s0; j < s1; ++j) {
+              acc += fx(D[j]);
+              if (acc > tl) {
+                x = j;
+                break;
+              }
             }
-            const unsigned hit = __ballot_sync(0xffffffffu, j < c1 && run + incl > tl);
-            if (hit) {
-              if (lane == __ffs(hit) - 1) out_emit[L - 1] = x0 + j;
-              break;
-            }
-            run += __shfl_sync(0xffffffffu, incl, 31);
+            out_emit[L - 1] = x0 + x;
           }
         }
       }
@@ -900,14 +1084,23 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
   // goes on, so no CTA leaves while a peer may still write into it.
 }
 
-// The walk keeps no state in global memory.  The workspace argument stays in
-// the interface (callers size it with spec_verify_workspace_size).
+// Workspace: the row statistics of every node (stochastic verification of
+// large batches); the walk itself keeps its state in shared memory.
 constexpr size_t kVerifyWorkspace = 256;
+inline size_t stats_bytes(int B, int n_max) { return (size_t)B * (size_t)n_max * sizeof(RowStats); }
+// Stochastic walks get the precomputed statistics when the batch leaves a
+// request at most this many CTAs: the passes over a node's row are then the
+// walk's bottleneck, and the statistics kernel spreads them over every SM.
+constexpr int kStatsMaxCluster = 2;
 
 template <int MODE, int C>
 cudaError_t launch_walk(const VerifyArgs& a, int B, cudaStream_t stream) {
   auto kern = verify_walk_kernel<MODE, C>;
-  const size_t dyn = MODE == 1 ? 3 * (size_t)a.slice * sizeof(float) : 0;
+  // stochastic: the target slice and two draft buffers; with row statistics
+  // the second draft buffer's room also holds 6 words per node
+  size_t words = MODE == 1 ? 3 * (size_t)a.slice : 0;
+  if (MODE == 1 && a.stats) words = std::max(words, 2 * (size_t)a.slice + 6 * (size_t)a.n_max);
+  const size_t dyn = words * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
   if (C > 8) {
@@ -988,6 +1181,17 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
   if (MODE == 1 && a.slice > kMaxSlice) return SPEC_ERR_UNSUPPORTED;
   a.vec = (a.V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p_logits) & 15) == 0 &&
           (MODE == 0 || (reinterpret_cast<uintptr_t>(a.q_probs) & 15) == 0);
+  a.stats = nullptr;
+  if (MODE == 1 && C <= kStatsMaxCluster && ws_bytes >= stats_bytes(B, a.n_max) &&
+      (reinterpret_cast<uintptr_t>(workspace) & 15) == 0) {
+    RowStats* st = static_cast<RowStats*>(workspace);
+    const long long ctas = (long long)B * a.n_max;
+    if (ctas > 0 && ctas < (1LL << 31)) {
+      row_stats_kernel<<<(unsigned)ctas, kStatsThreads, 0, stream>>>(a, st);
+      if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+      a.stats = st;
+    }
+  }
   cudaError_t e;
   switch (C) {
     case 1: e = launch_walk<MODE, 1>(a, B, stream); break;
@@ -1006,10 +1210,9 @@ using namespace spectree;
 extern "C" {
 
 size_t spec_verify_workspace_size(int B, int n_max, int V) {
-  (void)B;
-  (void)n_max;
   (void)V;
-  return kVerifyWorkspace;
+  if (B <= 0 || n_max <= 0) return kVerifyWorkspace;
+  return std::max(kVerifyWorkspace, stats_bytes(B, n_max));
 }
 
 static spec_status verify_check(int B, int n_max, int V) {
