@@ -91,6 +91,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 3-D box of Q [T][Hq][D]: columns x.., heads y.., nodes z..
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -193,6 +202,7 @@ struct Layout {
 
 struct TcParams {
   AttnArgs a;
+  int q_tma;         // the Q tile arrives by one TMA per 64 columns (g divides 128), else threads stage it
   int box_rows;      // rows per TMA box: min(block_size, 128)
   long long rows_total;  // num_blocks * Hkv * block_size (rows of the 2-D cache view)
 };
@@ -275,7 +285,7 @@ __device__ __forceinline__ int request_by_length(const AttnArgs& a, int slot) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                   const TcParams prm) {
+                   const __grid_constant__ CUtensorMap tmap_q, const TcParams prm) {
   using L_ = Layout<D>;
   constexpr int HC = BN / 2;        // score columns per softmax thread
   constexpr int OC = D / 2;         // output columns per softmax thread
@@ -328,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_full[i], kSoftmaxThreads);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(&q_full, kThreads - 96);
+    mbar_init(&q_full, prm.q_tma ? 1 : kThreads - 96);
     mbar_init(&drain, 1);
     for (int i = 0; i < 4; ++i) mbar_init(&lbar[i], 64);
     abort_flag = 0;
@@ -349,12 +359,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- K producer
+    // (the Q tile first: node r / g, head kvh*g + r % g of row r is box
+    // element (node, head) of a (64, g, 128/g) box; nodes past the request
+    // are masked rows, past T zero fill)
     if (lane == 0) {
+      if (prm.q_tma) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
+        mbar_expect_tx(&q_full, L_::kQ);
+#pragma unroll
+        for (int h = 0; h < L_::DH; ++h)
+          tma_load_3d(sbase + L_::kOffQ + h * (BM * 128), &tmap_q, h * 64, kvh * g, off + mt * (BM / g), &q_full);
+      }
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
     }
     produce_ring<D, KST>(sbase + L_::kOffK, &tmap_k, prm, b, kvh, k_begin, Lk, ntiles, k_full, k_empty, &bad_block,
                          &abort_flag);
+    if (lane == 0 && prm.q_tma) mbar_wait(&q_full, 0, &abort_flag);  // the Q copy has landed before any exit
   } else if (warp == 2) {
     // ---------------------------------------------------------- V producer
     produce_ring<D, VST>(sbase + L_::kOffV, &tmap_v, prm, b, kvh, k_begin, Lk, ntiles, v_full, v_empty, &bad_block,
@@ -423,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------ Q tile (warps 3..11)
     // row r = (node r / g, head kvh*g + r % g); rows past the group are zero
-    {
+    if (!prm.q_tma) {
       const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
       constexpr int CPR = D / 8;  // 16-byte chunks per row
       constexpr int NT = kThreads - 96;
@@ -726,6 +747,20 @@ static bool make_cache_map(CUtensorMap* m, const void* base, long long rows, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q [T][Hq][D] as a 3-D tensor (columns, heads, nodes); a box of (64, g,
+// 128 / g) is one 64-column half of a 128-row (node, head) tile.
+static bool make_q_map(CUtensorMap* m, const void* base, int T, int Hq, int D, int g) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)(tc::BM / g)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 static cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t stream) {
   tc::TcParams prm;
@@ -733,17 +768,21 @@ static cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t stream) {
   prm.box_rows = a.block_size < tc::BN ? a.block_size : tc::BN;
   prm.rows_total = (long long)a.num_blocks * a.Hkv * a.block_size;
   if (prm.rows_total >= (long long)INT32_MAX) return cudaErrorInvalidValue;
-  alignas(64) CUtensorMap mk, mv;
+  alignas(64) CUtensorMap mk, mv, mq;
   if (!make_cache_map(&mk, a.k_cache, prm.rows_total, D, prm.box_rows) ||
       !make_cache_map(&mv, a.v_cache, prm.rows_total, D, prm.box_rows))
     return cudaErrorInvalidValue;
+  // Q by TMA when g divides the 128-row tile (else the CTA's threads stage it)
+  prm.q_tma = a.g >= 1 && tc::BM % a.g == 0 && (reinterpret_cast<uintptr_t>(a.q) & 15) == 0 &&
+              make_q_map(&mq, a.q, a.T, a.Hq, D, a.g);
+  if (!prm.q_tma) mq = mk;  // unused
   auto kern = tc::attn_tc_kernel<D>;
   const int dyn = (int)tc::Layout<D>::kDyn;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
   const int rows_max = a.n_max * a.g;
   dim3 grid((rows_max + tc::BM - 1) / tc::BM, a.splits, a.B * a.Hkv);
-  kern<<<grid, tc::kThreads, dyn, stream>>>(mk, mv, prm);
+  kern<<<grid, tc::kThreads, dyn, stream>>>(mk, mv, mq, prm);
   return cudaGetLastError();
 }
 
