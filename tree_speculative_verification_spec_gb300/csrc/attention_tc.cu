@@ -21,14 +21,15 @@
 // O = (2^(m0-m) O_0 + 2^(m1-m) O_1) / (2^(m0-m) l_0 + 2^(m1-m) l_1).
 // Tensor memory: S/P slots 0 and 1 (128 columns each), O_0 and O_1 (D each).
 // K and V tiles arrive by TMA (2-D tensor maps over the paged cache, one box
-// per page or per 128 rows), 128-byte swizzled, into a three-stage K ring and
-// a two-stage V ring.  While the softmax works on tile j the tensor core runs
+// per page or per 128 rows), 128-byte swizzled, into three-stage K and V
+// rings.  While the softmax works on tile j the tensor core runs
 // PV_{j-1} and QK_{j+1}.  O_h is rescaled only when the half's maximum grows
 // by more than 2^8 (the stale maximum is exact for the final normalisation).
 //
-// Warp roles (384 threads): warps 0 and 2 issue the K and V loads from the
-// start, warp 1 issues MMAs and owns the TMEM allocation, warps 3-11 stage the
-// Q tile, then warps 4-11 run softmax and the epilogue
+// Warp roles (384 threads): warps 0 and 2 issue the Q, K and V loads from
+// the start, warp 1 issues the QK MMAs and owns the TMEM allocation, warp 3
+// issues the PV MMAs (after staging its part of Q when Q does not come by
+// TMA), and warps 4-11 run softmax and the epilogue
 // (row r == TMEM lane r, the warp's lane quadrant; warps 4-7 take key half 0,
 // warps 8-11 key half 1).  Every mbarrier wait is bounded: on expiry the CTA
 // records SPEC_DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and
@@ -189,7 +190,7 @@ template <int D>
 struct Layout {
   static constexpr int DH = D / 64;           // 128-byte halves of a row
   static constexpr int KST = 3;               // K stages: a K load goes out three tiles before its QK
-  static constexpr int VST = 2;               // V stages: a V load goes out two tiles before its PV
+  static constexpr int VST = 3;               // V stages: a V load goes out three tiles before its PV
   static constexpr uint32_t kQ = BM * D * 2;  // Q tile bytes
   static constexpr uint32_t kKV = BN * D * 2; // one K (or V) stage
   static constexpr uint32_t kOffQ = 0;
@@ -198,6 +199,7 @@ struct Layout {
   static constexpr uint32_t kBytes = kOffV + VST * kKV;
   // one CTA per SM: TMEM is allocated whole (512 columns)
   static constexpr uint32_t kDyn = (kBytes + 1024 < 120 * 1024 ? 120 * 1024 : kBytes + 1024);
+  static_assert(kDyn <= 230400, "static shared memory (< 2 KB) plus kDyn must stay within 227 KB");
 };
 
 struct TcParams {
@@ -265,9 +267,10 @@ __device__ __forceinline__ void produce_ring(uint32_t ring, const CUtensorMap* m
 // ranks the candidates itself from prefix_len and tree_off (O(B^2 / threads)
 // comparisons on a shared copy); batches above kOrderMax keep their order.
 constexpr int kOrderMax = 256;
-__device__ __forceinline__ int request_by_length(const AttnArgs& a, int slot) {
+// `len` is scratch shared memory of kOrderMax ints (the first bytes of the
+// K ring, which no copy has reached yet).
+__device__ __forceinline__ int request_by_length(const AttnArgs& a, int slot, int* len) {
   if (a.B < 2 || a.B > kOrderMax) return slot;
-  __shared__ int len[kOrderMax];
   __shared__ int pick;
   for (int i = threadIdx.x; i < a.B; i += blockDim.x) len[i] = a.prefix_len[i] + (a.tree_off[i + 1] - a.tree_off[i]);
   if (threadIdx.x == 0) pick = slot;
@@ -278,6 +281,8 @@ __device__ __forceinline__ int request_by_length(const AttnArgs& a, int slot) {
     for (int j = 0; j < a.B; ++j) rank += (len[j] > L) || (len[j] == L && j < c);
     if (rank == slot) pick = c;
   }
+  // the ring's TMA writes (async proxy) come after these generic accesses
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
   return pick;
 }
@@ -296,12 +301,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag, bad_block;
-  __shared__ float mfin[2][BM], lfin[2][BM];  // [key half][row]: final maximum and sum of each half
-  __shared__ uint64_t lbar[4];                 // their exchange, per lane quadrant (bounded waits)
+  __shared__ uint64_t lbar[4];  // the epilogue's exchange of the halves' maxima and sums, per lane quadrant
 
   const int mt = blockIdx.x, split = blockIdx.y;
   const int kvh = blockIdx.z % a.Hkv;
-  const int b = request_by_length(a, blockIdx.z / a.Hkv);
+  // 1024-byte aligned dynamic shared memory (128-byte swizzle atoms)
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  const int b = request_by_length(a, blockIdx.z / a.Hkv, reinterpret_cast<int*>(smem + L_::kOffK));
   const int off = a.tree_off[b];
   const int n = a.tree_off[b + 1] - off;
   const int P = a.prefix_len[b];
@@ -319,9 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (k_begin >= k_end) return;
   const int ntiles = (k_end - k_begin + BN - 1) / BN;
 
-  // 1024-byte aligned dynamic shared memory (128-byte swizzle atoms)
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~(uintptr_t)1023);
-  const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -339,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(&q_full, prm.q_tma ? 1 : kThreads - 96);
-    mbar_init(&drain, 1);
+    mbar_init(&drain, 2);  // one commit from each MMA issuer
     for (int i = 0; i < 4; ++i) mbar_init(&lbar[i], 64);
     abort_flag = 0;
     bad_block = 0;
@@ -381,25 +385,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     produce_ring<D, VST>(sbase + L_::kOffV, &tmap_v, prm, b, kvh, k_begin, Lk, ntiles, v_full, v_empty, &bad_block,
                          &abort_flag);
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // S_j = Q K_j^T into slot j % 2; P_j (bf16) overwrites part of that slot;
-    // O_h += P_j,h V_j,h reads A from tensor memory.  Issue order: QK_0 QK_1,
-    // then PV_j followed by QK_{j+2} (which reuses P_j's slot; the tensor pipe
-    // executes them in issue order).
+    // --------------------------------------------------------- QK issuer
+    // S_j = Q K_j^T into slot j % 2, once K_j has landed and PV_{j-2} (the
+    // last reader of that slot's P) has completed.  The PV MMAs come from a
+    // second thread (warp 3), so neither stream's waits stall the other's
+    // issue: tcgen05.mma issue blocks at the pipe's rate.
     if (lane == 0) {
       // Descriptors are computed once: a 128B-swizzled descriptor holds the
       // address >> 4 in its low 14 bits, and every operand offset below keeps
       // that field under 2^14 (shared addresses < 256 KB), so an operand at
       // base + off has descriptor desc(base) + (off >> 4).
       constexpr uint32_t idesc_qk = idesc_bf16(BN, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16(D, 1);
       const uint64_t qdesc = smem_desc_sw128(sbase + L_::kOffQ, 16, 1024);
       const uint64_t kdesc0 = smem_desc_sw128(sbase + L_::kOffK, 16, 1024);
-      const uint64_t vdesc0 = smem_desc_sw128(sbase + L_::kOffV, BN * 128, 1024);
       bool ok = mbar_wait(&q_full, 0, &abort_flag);
-      auto issue_qk = [&](int j) -> bool {
+      for (int j = 0; j < ntiles && ok; ++j) {
         const int st = j % KST;
-        if (!mbar_wait(&k_full[st], (j / KST) & 1, &abort_flag)) return false;
+        if (j >= 2 && !mbar_wait(&pv_done[j & 1], ((j - 2) >> 1) & 1, &abort_flag)) break;
+        if (!mbar_wait(&k_full[st], (j / KST) & 1, &abort_flag)) break;
         tc_fence_after();
         const uint64_t kdesc = kdesc0 + (uint64_t)(st * (L_::kKV >> 4));
         const uint32_t d = tS + (j & 1) * BN;
@@ -411,33 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(&s_full[j & 1]);
         umma_commit(&k_empty[st]);
-        return true;
-      };
-      for (int j = 0; j < min(2, ntiles) && ok; ++j) ok = issue_qk(j);
-      for (int j = 0; j < ntiles && ok; ++j) {
-        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, &abort_flag) ||
-            !mbar_wait(&v_full[j % VST], (j / VST) & 1, &abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t vdesc = vdesc0 + (uint64_t)((j % VST) * (L_::kKV >> 4));
-        const uint32_t pa = tS + (j & 1) * BN;
-        const uint32_t acc0 = j > 0 ? 1u : 0u;
-        // key half h: P at columns h*64 .. h*64+31 of the slot (two keys per
-        // column), V rows h*64 .. h*64+63, accumulator O_h
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int kk = 0; kk < HC / 16; ++kk)
-            umma_bf16_ts(tO + h * D, pa + h * HC + kk * 8, vdesc + (uint64_t)(((h * (HC / 16) + kk) * 2048) >> 4),
-                         idesc_pv, kk > 0 ? 1u : acc0);
-        }
-        umma_commit(&pv_done[j & 1]);
-        umma_commit(&v_empty[j % VST]);
-        if (j + 2 < ntiles) ok = issue_qk(j + 2);
       }
-      // drain: every issued MMA has completed before TMEM is freed
+      // drain: both issuers' MMAs have completed before TMEM is freed
       umma_commit(&drain);
       mbar_wait(&drain, 0, &abort_flag);
     }
@@ -472,7 +450,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       mbar_arrive(&q_full);
     }
-    if (warp >= 4) {
+    if (warp == 3) {
+      // ----------------------------------------------------- PV issuer
+      // O_h += P_j,h V_j,h once the softmax has written P_j (tensor memory)
+      // and V_j has landed
+      if (lane == 0) {
+        constexpr uint32_t idesc_pv = idesc_bf16(D, 1);
+        const uint64_t vdesc0 = smem_desc_sw128(sbase + L_::kOffV, BN * 128, 1024);
+        for (int j = 0; j < ntiles; ++j) {
+          if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, &abort_flag) ||
+              !mbar_wait(&v_full[j % VST], (j / VST) & 1, &abort_flag))
+            break;
+          tc_fence_after();
+          const uint64_t vdesc = vdesc0 + (uint64_t)((j % VST) * (L_::kKV >> 4));
+          const uint32_t pa = tS + (j & 1) * BN;
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
+          // key half h: P at columns h*64 .. h*64+31 of the slot (two keys per
+          // column), V rows h*64 .. h*64+63, accumulator O_h
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int kk = 0; kk < HC / 16; ++kk)
+              umma_bf16_ts(tO + h * D, pa + h * HC + kk * 8, vdesc + (uint64_t)(((h * (HC / 16) + kk) * 2048) >> 4),
+                           idesc_pv, kk > 0 ? 1u : acc0);
+          }
+          umma_commit(&pv_done[j & 1]);
+          umma_commit(&v_empty[j % VST]);
+        }
+        umma_commit(&drain);
+        mbar_wait(&drain, 0, &abort_flag);
+      }
+    } else if (warp >= 4) {
       // -------------------------------------------------- softmax + epilogue
       // key half `half` of every tile: its own running maximum m_used (log2
       // units), sum and accumulator O_half
@@ -621,15 +629,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // epilogue: merge the halves; this thread writes output columns
       // half*D/2 .. half*D/2 + D/2 - 1 of its row
-      mfin[half][r] = m_used;
-      lfin[half][r] = (lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y);
+      // [key half][row] maxima and sums in the Q tile's room: every QK MMA
+      // has completed (this thread saw the last tile's S)
+      float* mfin = reinterpret_cast<float*>(smem + L_::kOffQ);
+      float* lfin = mfin + 2 * BM;
+      mfin[half * BM + r] = m_used;
+      lfin[half * BM + r] = (lacc[0].x + lacc[0].y) + (lacc[1].x + lacc[1].y);
       mbar_arrive(&lbar[quad]);
       ok = ok && wait_warp(&lbar[quad], 0);
-      const float m0 = mfin[0][r], m1 = mfin[1][r];
+      const float m0 = mfin[r], m1 = mfin[BM + r];
       const float mrow_max = fmaxf(m0, m1);
       const float f0 = m0 == -INFINITY ? 0.0f : fast_exp2(m0 - mrow_max);
       const float f1 = m1 == -INFINITY ? 0.0f : fast_exp2(m1 - mrow_max);
-      const float lsum = lfin[0][r] * f0 + lfin[1][r] * f1;
+      const float lsum = lfin[r] * f0 + lfin[BM + r] * f1;
       if (ok && wait_warp(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
         tc_fence_after();
         const size_t orow = (size_t)t * a.Hq + kvh * g + (valid ? row % g : 0);
