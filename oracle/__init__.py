@@ -64,6 +64,7 @@ def lib():
         L.oracle_verify_greedy.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P]
         L.oracle_verify_stochastic.argtypes = [P, P, P, P, P, P, i32, i32, i32, P, P, P, P, P]
         L.oracle_kv_commit.argtypes = [P, P, i64, P, i32, i32, i32, P, P, i32, P, i32, i32, i32, i32, P, P]
+        L.oracle_kv_release.argtypes = [P, i32, i32, P, P, P, P, i32, P, i32, P]
         L.oracle_philox4x32_10.argtypes = [P, P, P]
         L.oracle_philox_uniforms.argtypes = [u64, u32, P, i32, P]
         L.oracle_canon_exp.argtypes = [ctypes.c_float]
@@ -159,6 +160,35 @@ def kv_commit(k_cache, v_cache, block_table, block_size, prefix_len, path, accep
                            _p(prefix_len), _p(path), path.shape[1], _p(accept_len), B, Hkv, D, dtype,
                            _p(new_len), _p(st))
     return k_new, v_new, new_len, st
+
+
+def kv_release(block_table, block_size, prefix_len, tree_off, new_len, status, free_cap, free_count=0):
+    """Page release after a commit.  Returns (block_table_out, free_pool[:count],
+    count, status_out); the inputs are not modified."""
+    bt = np.array(block_table, dtype=np.int32, copy=True, order="C")
+    st = np.array(status, dtype=np.int32, copy=True)
+    prefix_len, tree_off, new_len = _c(prefix_len, np.int32), _c(tree_off, np.int32), _c(new_len, np.int32)
+    pool = np.full(max(int(free_cap), 1), -1, np.int32)
+    cnt = np.array([free_count], np.int32)
+    lib().oracle_kv_release(_p(bt), bt.shape[1], block_size, _p(prefix_len), _p(tree_off), _p(new_len), _p(st),
+                            len(prefix_len), _p(pool), int(free_cap), _p(cnt))
+    return bt, pool[:int(cnt[0])], int(cnt[0]), st
+
+
+def kv_commit_layers(k_caches, v_caches, block_table, block_size, prefix_len, tree_off, path, accept_len, Hkv, D,
+                     dtype, status, free_cap, free_count=0):
+    """Every layer's commit (the single-layer commit per layer, each starting
+    from the same status), then the page release.  Returns (k_list, v_list,
+    new_len, status_out, block_table_out, free_pool, count)."""
+    ks, vs = [], []
+    new_len, st = None, None
+    for k, v in zip(k_caches, v_caches):
+        k2, v2, nl, s2 = kv_commit(k, v, block_table, block_size, prefix_len, path, accept_len, Hkv, D, dtype, status)
+        ks.append(k2)
+        vs.append(v2)
+        new_len, st = nl, s2
+    bt, pool, cnt, st = kv_release(block_table, block_size, prefix_len, tree_off, new_len, st, free_cap, free_count)
+    return ks, vs, new_len, st, bt, pool, cnt
 
 
 def philox4x32_10(ctr, key):

@@ -623,6 +623,47 @@ int oracle_kv_commit(void *k_cache, void *v_cache, int64_t cache_elems,
 }
 
 /* ------------------------------------------------------------------ */
+/* Multi-layer commit and page release                                 */
+/* "SpecInfer Guide", "PagedKV Allocation with Zero-Copy Pruning": the  */
+/* tree's K/V rows sit in pages of the request's block table; after     */
+/* verification the accepted path is compacted in every layer (the same */
+/* single-layer commit per layer), then the pages lying wholly past the */
+/* new length go back to the free pool in one metadata update.          */
+/* Reading: the tree of request b occupies slots [P, P + n_b); pages    */
+/* ceil(new_len / bs) .. ceil((P + n_b) / bs) - 1 are released, their   */
+/* block-table entries set to -1 and their ids appended to the pool in  */
+/* request order, then page order.  Failed requests (status != 0) keep  */
+/* every page.  A request whose pages do not all fit in the pool keeps  */
+/* them all and gets ORC_CAPACITY.                                      */
+/* ------------------------------------------------------------------ */
+int oracle_kv_release(int32_t *block_table, int max_blocks, int block_size, const int32_t *prefix_len,
+                      const int32_t *tree_off, const int32_t *new_len, int32_t *status, int B,
+                      int32_t *free_pool, int free_cap, int32_t *free_count)
+{
+    int cnt = *free_count;
+    for (int b = 0; b < B; b++) {
+        if (status[b] != 0) continue;
+        int n = tree_off[b + 1] - tree_off[b];
+        int P = prefix_len[b];
+        int keep = (new_len[b] + block_size - 1) / block_size;
+        int span = (P + n + block_size - 1) / block_size;
+        if (span > max_blocks) span = max_blocks;
+        if (span <= keep) continue;
+        if (cnt + (span - keep) > free_cap) {
+            status[b] |= ORC_CAPACITY;
+            continue;
+        }
+        int32_t *row = block_table + (size_t)b * max_blocks;
+        for (int i = keep; i < span; i++) {
+            free_pool[cnt++] = row[i];
+            row[i] = -1;
+        }
+    }
+    *free_count = cnt;
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* Philox4x32-10 uniforms                                              */
 /* ------------------------------------------------------------------ */
 

@@ -581,6 +581,88 @@ def test_commit_rejects_bad_paths(oracle):
     assert np.array_equal(k2, kc) and np.array_equal(v2, vc)
 
 
+def _random_paths(w, rng):
+    path = np.full((w.B, w.n_max), -1, np.int32)
+    alen = np.zeros(w.B, np.int32)
+    for b in range(w.B):
+        par = w.parent[int(w.tree_off[b]):int(w.tree_off[b + 1])].numpy()
+        u = int(rng.integers(0, len(par)))
+        p = []
+        while u != -1:
+            p.append(u)
+            u = par[u]
+        path[b, :len(p)] = p[::-1]
+        alen[b] = len(p)
+    return path, alen
+
+
+def test_release_of_a_printed_page_layout(oracle):
+    """Pages of 4 slots; prefix 5 and a 10-node tree fill slots 5..14 (pages
+    1..3).  Three accepted nodes give new length 8: pages 0 and 1 stay, pages
+    2 and 3 lie wholly past it and go back to the pool; page 4 was never the
+    tree's."""
+    bt = np.array([[10, 11, 12, 13, 14]], np.int32)
+    out, pool, cnt, st = oracle.kv_release(bt, 4, [5], [0, 10], [8], [0], 16)
+    assert out.tolist() == [[10, 11, -1, -1, 14]] and pool.tolist() == [12, 13] and cnt == 2 and st.tolist() == [0]
+    # everything accepted into the last page: nothing is past the new length
+    out, pool, cnt, _ = oracle.kv_release(bt, 4, [5], [0, 10], [15], [0], 16)
+    assert cnt == 0 and out.tolist() == bt.tolist()
+    # a failed request keeps every page; a full pool keeps them and flags capacity
+    out, pool, cnt, st = oracle.kv_release(bt, 4, [5], [0, 10], [8], [oracle.ST_BAD_TOKEN], 16)
+    assert cnt == 0 and st.tolist() == [oracle.ST_BAD_TOKEN]
+    out, pool, cnt, st = oracle.kv_release(bt, 4, [5], [0, 10], [8], [0], 1)
+    assert cnt == 0 and out.tolist() == bt.tolist() and st.tolist() == [oracle.ST_CAPACITY]
+
+
+def test_release_invariants_on_random_batches(oracle):
+    """Every released id is a page wholly past the new length inside the
+    tree's span, listed in request then page order; every other entry of the
+    block table is unchanged."""
+    rng = np.random.default_rng(9)
+    for seed in range(6):
+        w = W.small_random(40 + seed, B=7, n_range=(1, 40), prefix_range=(0, 60), Hq=2, Hkv=1, D=8, dtype=W.F32,
+                           block_size=int(rng.choice([4, 8, 16])))
+        path, alen = _random_paths(w, rng)
+        P, bs = w.prefix_len.numpy(), w.block_size
+        new_len = (P + alen).astype(np.int32)
+        bt = w.block_table.numpy()
+        out, pool, cnt, st = oracle.kv_release(bt, bs, P, w.tree_off.numpy(), new_len, np.zeros(w.B, np.int32), 10000)
+        expect = []
+        for b in range(w.B):
+            n = int(w.tree_off[b + 1] - w.tree_off[b])
+            keep, span = -(-int(new_len[b]) // bs), min(bt.shape[1], -(-(int(P[b]) + n) // bs))
+            for i in range(bt.shape[1]):
+                if keep <= i < span:
+                    expect.append(int(bt[b, i]))
+                    assert out[b, i] == -1
+                else:
+                    assert out[b, i] == bt[b, i]
+        assert pool.tolist() == expect and cnt == len(expect) and (st == 0).all()
+        assert len(set(expect)) == len(expect)
+
+
+def test_layered_commit_moves_each_layers_rows(oracle):
+    """Three layers with different contents: each layer's rows move per the
+    path (numpy gather of that layer's snapshot), the release follows."""
+    rng = np.random.default_rng(4)
+    w = W.small_random(33, B=4, n_range=(3, 20), prefix_range=(0, 50), Hq=4, Hkv=2, D=8, dtype=W.BF16, block_size=4)
+    path, alen = _random_paths(w, rng)
+    layers_k = [(w.k_cache.view(torch.int16).numpy().view(np.uint16) + 3 * l).astype(np.uint16) for l in range(3)]
+    layers_v = [(w.v_cache.view(torch.int16).numpy().view(np.uint16) + 5 * l).astype(np.uint16) for l in range(3)]
+    ks, vs, new_len, st, bt_out, pool, cnt = oracle.kv_commit_layers(
+        layers_k, layers_v, w.block_table.numpy(), w.block_size, w.prefix_len.numpy(), w.tree_off.numpy(), path, alen,
+        w.Hkv, w.D, W.BF16, np.zeros(w.B, np.int32), 1000)
+    P, bt, bs = w.prefix_len.numpy(), w.block_table.numpy(), w.block_size
+    assert new_len.tolist() == (P + alen).tolist() and (st == 0).all()
+    for l in range(3):
+        for b in range(w.B):
+            for i in range(alen[b]):
+                d, src = P[b] + i, P[b] + path[b, i]
+                assert np.array_equal(ks[l][bt[b, d // bs], :, d % bs], layers_k[l][bt[b, src // bs], :, src % bs])
+                assert np.array_equal(vs[l][bt[b, d // bs], :, d % bs], layers_v[l][bt[b, src // bs], :, src % bs])
+    assert cnt == len(pool) and all(int(x) >= 0 for x in pool)
+
+
 # --------------------------------------------------------------- Philox ----
 
 _PHILOX_CPP = r"""
