@@ -633,23 +633,33 @@ int oracle_kv_commit(void *k_cache, void *v_cache, int64_t cache_elems,
 /* ceil(new_len / bs) .. ceil((P + n_b) / bs) - 1 are released, their   */
 /* block-table entries set to -1 and their ids appended to the pool in  */
 /* request order, then page order.  Failed requests (status != 0) keep  */
-/* every page.  A request whose pages do not all fit in the pool keeps  */
-/* them all and gets ORC_CAPACITY.                                      */
+/* every page.  When the pool cannot take every page of the call, none  */
+/* is released and each request that had pages to release gets          */
+/* ORC_CAPACITY.                                                        */
 /* ------------------------------------------------------------------ */
 int oracle_kv_release(int32_t *block_table, int max_blocks, int block_size, const int32_t *prefix_len,
                       const int32_t *tree_off, const int32_t *new_len, int32_t *status, int B,
                       int32_t *free_pool, int free_cap, int32_t *free_count)
 {
     int cnt = *free_count;
+    long long total = 0;
     for (int b = 0; b < B; b++) {
         if (status[b] != 0) continue;
         int n = tree_off[b + 1] - tree_off[b];
-        int P = prefix_len[b];
         int keep = (new_len[b] + block_size - 1) / block_size;
-        int span = (P + n + block_size - 1) / block_size;
+        int span = (prefix_len[b] + n + block_size - 1) / block_size;
+        if (span > max_blocks) span = max_blocks;
+        if (span > keep) total += span - keep;
+    }
+    int fits = cnt + total <= free_cap;
+    for (int b = 0; b < B; b++) {
+        if (status[b] != 0) continue;
+        int n = tree_off[b + 1] - tree_off[b];
+        int keep = (new_len[b] + block_size - 1) / block_size;
+        int span = (prefix_len[b] + n + block_size - 1) / block_size;
         if (span > max_blocks) span = max_blocks;
         if (span <= keep) continue;
-        if (cnt + (span - keep) > free_cap) {
+        if (!fits) {
             status[b] |= ORC_CAPACITY;
             continue;
         }

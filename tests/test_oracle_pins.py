@@ -607,11 +607,21 @@ def test_release_of_a_printed_page_layout(oracle):
     # everything accepted into the last page: nothing is past the new length
     out, pool, cnt, _ = oracle.kv_release(bt, 4, [5], [0, 10], [15], [0], 16)
     assert cnt == 0 and out.tolist() == bt.tolist()
-    # a failed request keeps every page; a full pool keeps them and flags capacity
+    # a failed request keeps every page
     out, pool, cnt, st = oracle.kv_release(bt, 4, [5], [0, 10], [8], [oracle.ST_BAD_TOKEN], 16)
     assert cnt == 0 and st.tolist() == [oracle.ST_BAD_TOKEN]
-    out, pool, cnt, st = oracle.kv_release(bt, 4, [5], [0, 10], [8], [0], 1)
-    assert cnt == 0 and out.tolist() == bt.tolist() and st.tolist() == [oracle.ST_CAPACITY]
+    # a pool that cannot take every page of the call takes none, and the
+    # requests that had pages to release are flagged
+    bt2 = np.array([[10, 11, 12, 13, 14], [20, 21, 22, 23, 24]], np.int32)
+    out, pool, cnt, st = oracle.kv_release(bt2, 4, [5, 5], [0, 10, 20], [8, 8], [0, 0], 3)
+    assert cnt == 0 and out.tolist() == bt2.tolist() and st.tolist() == [oracle.ST_CAPACITY] * 2
+    # a failed request's pages do not count
+    out, pool, cnt, st = oracle.kv_release(bt2, 4, [5, 5], [0, 10, 20], [8, 8], [0, oracle.ST_BAD_TOKEN], 3)
+    assert cnt == 2 and pool.tolist() == [12, 13] and st.tolist() == [0, oracle.ST_BAD_TOKEN]
+    # appends after the pool's current count, in request then page order
+    out, pool, cnt, st = oracle.kv_release(bt2, 4, [5, 5], [0, 10, 20], [8, 8], [0, 0], 5, free_count=1)
+    assert cnt == 5 and pool.tolist()[1:] == [12, 13, 22, 23] and (st == 0).all()
+    assert out.tolist() == [[10, 11, -1, -1, 14], [20, 21, -1, -1, 24]]
 
 
 def test_release_invariants_on_random_batches(oracle):
