@@ -434,6 +434,8 @@ def bench_gpu(args):
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind},
             "kernels": kernels}
+    if args.commit_layers > 0:
+        line["commit_layers"] = measure_commit_layers(args.commit_layers, passes[0], dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, _ = run_cpu_baseline(works[0], args.mode)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
@@ -526,6 +528,77 @@ def run_e2e(args, works, sets, passes, stream, dev, n_sets):
             "ms_per_step": ms / steps}
 
 
+def measure_commit_layers(L, vp, dev, reps=20, replays=5):
+    """The commit of L layers' caches for input set 0 in one launch, against L
+    single-layer launches, and the layered commit followed by the page release
+    (the block table and the pool count put back before each, and that reset
+    timed alone and subtracted).  Each figure: one graph of `reps` back-to-back
+    calls, replayed `replays` times between CUDA events; microseconds per call."""
+    import torch
+    import tree_speculative_verification_spec_gb300 as S
+    d = vp.batch
+    ks = [d.k_cache] + [torch.empty_like(d.k_cache) for _ in range(L - 1)]
+    vs = [d.v_cache] + [torch.empty_like(d.v_cache) for _ in range(L - 1)]
+    kp = torch.tensor([t.data_ptr() for t in ks], dtype=torch.int64, device=dev)
+    vp_ = torch.tensor([t.data_ptr() for t in vs], dtype=torch.int64, device=dev)
+    dtype = S.SPEC_BF16 if d.k_cache.element_size() == 2 else S.SPEC_F32
+    new_len = torch.zeros(d.B, dtype=torch.int32, device=dev)
+    st = torch.zeros(d.B, dtype=torch.int32, device=dev)
+    bt0 = d.block_table.clone()
+    pool = torch.empty(d.B * d.max_blocks, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def layered(release):
+        S.spec_kv_commit_layers(kp, vp_, L, d.block_table, d.max_blocks, d.block_size, d.num_blocks, d.prefix_len,
+                                d.tree_off, vp.path, d.n_max, vp.accept_len, d.B, d.Hkv, d.D, dtype, new_len,
+                                pool if release else None, cnt if release else None, st)
+
+    def per_layer():
+        for l in range(L):
+            S.spec_kv_commit(ks[l], vs[l], d.block_table, d.max_blocks, d.block_size, d.num_blocks, d.prefix_len,
+                             vp.path, d.n_max, vp.accept_len, d.B, d.Hkv, d.D, new_len, st)
+
+    def reset():
+        d.block_table.copy_(bt0)
+        cnt.zero_()
+
+    def with_release():
+        reset()
+        layered(True)
+
+    def time_us(fn):
+        cap = torch.cuda.Stream(dev)
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(reps):
+                fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream = torch.cuda.current_stream(dev)
+        a.record(stream)
+        for _ in range(replays):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * replays)
+
+    one = time_us(lambda: layered(False))
+    many = time_us(per_layer)
+    rel = time_us(with_release) - time_us(reset)
+    with_release()
+    torch.cuda.synchronize()
+    released = int(cnt.item())
+    reset()
+    torch.cuda.synchronize()
+    ok = int(st.abs().sum()) == 0
+    return {"layers": L, "us_one_launch": one, "us_per_layer_launches": many, "us_commit_and_release": rel,
+            "pages_released": released, "status_ok": ok}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -536,6 +609,8 @@ def main():
     ap.add_argument("--workload", type=int, default=1, choices=sorted(WORKLOADS))
     ap.add_argument("--attn-flags", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--commit-layers", type=int, default=0,
+                    help="also time the commit of this many layers' caches in one launch (0: off)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -248,6 +248,36 @@ spec_status spec_kv_commit(void* k_cache, void* v_cache, const int32_t* block_ta
                            int32_t* new_len, int32_t* status, void* stream);
 
 /*
+ * Multi-layer KV commit and page release.  "SpecInfer Guide", "PagedKV
+ * Allocation with Zero-Copy Pruning": after verification the accepted path is
+ * compacted in every layer's cache (each layer exactly as spec_kv_commit
+ * does, in one launch), then the tree's pages lying wholly past the new length
+ * go back to the free pool in one metadata update.  The tree of request b
+ * fills slots [prefix_len[b], prefix_len[b] + n_b); its pages
+ * ceil(new_len / block_size) .. ceil((prefix_len + n_b) / block_size) - 1 are
+ * released: their block-table entries become -1 and their ids are appended to
+ * free_pool after *free_count, in request order then page order, and
+ * *free_count grows by their number.  Requests with a non-zero status after
+ * the commit keep every page.  When the pool cannot take every page of the
+ * call (*free_count + released > free_cap), none is released and each request
+ * that had pages to release gets SPEC_DEV_CAPACITY.
+ *   k_caches, v_caches  device arrays of `layers` device pointers, each a paged
+ *                       cache [num_blocks][Hkv][block_size][D] of dtype
+ *   block_table int32 [B][max_blocks]  in/out (released entries become -1)
+ *   tree_off    int32 [B+1]  tree sizes (as for the mask build)
+ *   free_pool   int32 [free_cap], free_count int32 [1]: device memory, in/out;
+ *               both NULL: commit only, no release
+ *   other arguments as in spec_kv_commit.  Two kernels: the commit (grid
+ *   B x Hkv x 2*layers), then the release (one CTA).
+ */
+spec_status spec_kv_commit_layers(void* const* k_caches, void* const* v_caches, int layers,
+                                  int32_t* block_table, int max_blocks, int block_size, int num_blocks,
+                                  const int32_t* prefix_len, const int32_t* tree_off, const int32_t* path,
+                                  int path_stride, const int32_t* accept_len, int B, int Hkv, int D,
+                                  spec_dtype dtype, int32_t* new_len, int32_t* free_pool, int free_cap,
+                                  int32_t* free_count, int32_t* status, void* stream);
+
+/*
  * Philox4x32-10 random words for one verification round (Salmon et al.,
  * "Parallel random numbers: as easy as 1, 2, 3", SC'11): node u (local index)
  * of request b uses counter (u, b, round, 0) and key (seed low 32 bits, seed

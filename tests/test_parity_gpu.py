@@ -449,6 +449,79 @@ def test_commit_bad_paths_and_failed_requests():
     assert np.array_equal(np_elems(d.v_cache, W.BF16), v_ref)
 
 
+def _root_paths(w, rng):
+    path = np.full((w.B, w.n_max), -1, np.int32)
+    alen = np.zeros(w.B, np.int32)
+    for b in range(w.B):
+        par = w.parent[int(w.tree_off[b]):int(w.tree_off[b + 1])].numpy()
+        u = int(rng.integers(0, len(par)))
+        p = []
+        while u != -1:
+            p.append(u)
+            u = par[u]
+        path[b, :len(p)] = p[::-1]
+        alen[b] = len(p)
+    return path, alen
+
+
+@pytest.mark.parametrize("dtype,D,bs,cap,B", [(W.BF16, 128, 16, 4096, 6), (W.F32, 64, 8, 4096, 6),
+                                              (W.BF16, 64, 8, 3, 6), (W.BF16, 128, 16, 8192, 70)])
+def test_commit_layers_and_page_release(dtype, D, bs, cap, B):
+    """Three layers committed in one launch, then the page release: every
+    layer's cache, new lengths, statuses, the block table and the free list
+    (order included) exactly as the oracle; a short pool releases nothing.
+    With 70 requests x 2 kv-heads one CTA moves several of the six caches."""
+    rng = np.random.default_rng(61)
+    w = W.small_random(62, B=B, n_range=(2, 60), prefix_range=(0, 90), Hq=4, Hkv=2, D=D, dtype=dtype, V=3,
+                       block_size=bs)
+    path, alen = _root_paths(w, rng)
+    path[4, :3] = [0, 2, 1]  # not increasing: BAD_PATH, untouched
+    alen[4] = 3
+    status = np.zeros(w.B, np.int32)
+    status[5] = S.SPEC_DEV_BAD_TOKEN  # failed upstream: untouched, keeps its pages
+    L = 3
+    k_layers = [np_elems(w.k_cache, dtype) for _ in range(L)]
+    v_layers = [np_elems(w.v_cache, dtype) for _ in range(L)]
+    for l in range(L):  # different contents per layer
+        if dtype == W.F32:
+            k_layers[l] = k_layers[l] + l
+            v_layers[l] = v_layers[l] - l
+        else:
+            k_layers[l] = (k_layers[l] ^ np.uint16(l)).astype(np.uint16)
+            v_layers[l] = (v_layers[l] ^ np.uint16(3 * l)).astype(np.uint16)
+    ks, vs, nl_ref, st_ref, bt_ref, pool_ref, cnt_ref = O.kv_commit_layers(
+        k_layers, v_layers, w.block_table.numpy(), bs, w.prefix_len.numpy(), w.tree_off.numpy(), path, alen, w.Hkv,
+        D, dtype, status, cap, free_count=1)
+    dev = "cuda"
+    tdt = torch.float32 if dtype == W.F32 else torch.int16
+    kd = [torch.from_numpy(k.view(np.int16) if dtype == W.BF16 else k).to(dev) for k in k_layers]
+    vd = [torch.from_numpy(v.view(np.int16) if dtype == W.BF16 else v).to(dev) for v in v_layers]
+    kp = torch.tensor([t.data_ptr() for t in kd], dtype=torch.int64, device=dev)
+    vp = torch.tensor([t.data_ptr() for t in vd], dtype=torch.int64, device=dev)
+    bt = w.block_table.to(dev).contiguous()
+    pool = torch.full((cap,), -7, dtype=torch.int32, device=dev)
+    cnt = torch.tensor([1], dtype=torch.int32, device=dev)
+    new_len = torch.zeros(w.B, dtype=torch.int32, device=dev)
+    st = torch.from_numpy(status).to(dev)
+    S.spec_kv_commit_layers(kp, vp, L, bt, bt.shape[1], bs, w.num_blocks, w.prefix_len.to(dev), w.tree_off.to(dev),
+                            torch.from_numpy(path).to(dev), path.shape[1], torch.from_numpy(alen).to(dev), w.B,
+                            w.Hkv, D, dtype, new_len, pool, cnt, st)
+    torch.cuda.synchronize()
+    for l in range(L):
+        got_k = kd[l].cpu().numpy().view(np.uint16) if dtype == W.BF16 else kd[l].cpu().numpy()
+        got_v = vd[l].cpu().numpy().view(np.uint16) if dtype == W.BF16 else vd[l].cpu().numpy()
+        assert np.array_equal(got_k, ks[l]) and np.array_equal(got_v, vs[l]), l
+    assert new_len.cpu().tolist() == nl_ref.tolist()
+    assert st.cpu().tolist() == st_ref.tolist()
+    assert bt.cpu().numpy().tolist() == bt_ref.tolist()
+    assert int(cnt.item()) == cnt_ref
+    assert pool.cpu().numpy()[1:cnt_ref].tolist() == pool_ref[1:].tolist()
+    if cap == 3:
+        assert cnt_ref == 1 and any(x & S.SPEC_DEV_CAPACITY for x in st_ref)
+    else:
+        assert cnt_ref > 1
+
+
 # ------------------------------------------------------------- full pass ----
 
 @pytest.mark.parametrize("mode", ["stochastic", "greedy"])

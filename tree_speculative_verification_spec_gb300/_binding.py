@@ -34,6 +34,8 @@ SIGNATURES = {
     "spec_tree_verify_greedy": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "spec_tree_verify_stochastic": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "spec_kv_commit": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "spec_kv_commit_layers": ([_P, _P, _I, _P, _I, _I, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P],
+                              _I),
     "spec_philox_uniforms": ([_U64, _U32, _P, _I, _I, _P, _P], _I),
     "spec_selftest_bounded_wait": ([_P, _U32, _P], _I),
 }
@@ -155,6 +157,19 @@ def spec_kv_commit(k_cache, v_cache, block_table, max_blocks, block_size, num_bl
         _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_blocks, block_size, num_blocks, _ptr(prefix_len),
         _ptr(path), path_stride, _ptr(accept_len), B, Hkv, D, _dtype_code(k_cache), _ptr(new_len), _ptr(status),
         _stream(stream)))
+
+
+def spec_kv_commit_layers(k_ptrs, v_ptrs, layers, block_table, max_blocks, block_size, num_blocks, prefix_len, tree_off,
+                          path, path_stride, accept_len, B, Hkv, D, dtype, new_len, free_pool, free_count, status,
+                          stream=None):
+    """k_ptrs / v_ptrs: int64 device tensors of the layers' cache addresses;
+    dtype: SPEC_F32 or SPEC_BF16; free_pool / free_count: int32 device
+    tensors, or None for a commit without release."""
+    cap = 0 if free_pool is None else free_pool.numel()
+    _check("spec_kv_commit_layers", lib().spec_kv_commit_layers(
+        _ptr(k_ptrs), _ptr(v_ptrs), layers, _ptr(block_table), max_blocks, block_size, num_blocks, _ptr(prefix_len),
+        _ptr(tree_off), _ptr(path), path_stride, _ptr(accept_len), B, Hkv, D, dtype, _ptr(new_len), _ptr(free_pool),
+        cap, _ptr(free_count), _ptr(status), _stream(stream)))
 
 
 def spec_philox_uniforms(seed, round_, tree_off, B, n_max, out, stream=None):

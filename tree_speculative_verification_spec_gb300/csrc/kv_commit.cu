@@ -7,6 +7,8 @@
 // increasing i is safe provided every row of a chunk is read before any row
 // of that chunk is written (a later chunk's sources are all above every
 // earlier destination).  One CTA per (request, kv-head, K or V).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace spectree {
@@ -14,26 +16,19 @@ namespace spectree {
 constexpr int kCommitThreads = 256;
 constexpr int kCommitChunkBytes = 32 * 1024;
 
-__global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(
-    char* __restrict__ k_cache, char* __restrict__ v_cache, const int32_t* __restrict__ block_table, int max_blocks,
-    int bs, int num_blocks, const int32_t* __restrict__ prefix_len, const int32_t* __restrict__ path, int path_stride,
-    const int32_t* __restrict__ accept_len, int Hkv, int row_bytes, int32_t* __restrict__ new_len,
-    int32_t* __restrict__ status) {
-  __shared__ uint4 buf[kCommitChunkBytes / 16];
-  __shared__ int s_bad;
-  const int b = blockIdx.x, h = blockIdx.y;
-  char* cache = blockIdx.z == 0 ? k_cache : v_cache;
-  const bool writer = h == 0 && blockIdx.z == 0;
-  const int P = prefix_len[b];
-  const int a = accept_len[b];
-  const int32_t* bt = block_table + (size_t)b * max_blocks;
-  const int32_t* pth = path + (size_t)b * path_stride;
-  const int st = *(volatile int32_t*)&status[b];
-  if (st != 0 || a <= 0) {
-    if (writer && threadIdx.x == 0) new_len[b] = P;
-    return;
-  }
-  // validation (identical in every CTA of the request)
+// Checks shared by both commit kernels (identical in every CTA of request
+// b): 0 when the accepted rows are to be moved, -1 when there is nothing to
+// move (the request failed upstream or accepted nothing), else the
+// SPEC_DEV_* bit that describes a bad path or block table.
+__device__ __forceinline__ int commit_check(int b, const int32_t* __restrict__ bt, int max_blocks, int bs,
+                                            int num_blocks, int P, int a, const int32_t* __restrict__ pth,
+                                            int path_stride, const int32_t* __restrict__ status) {
+  __shared__ int s_bad, s_st;
+  // one read, broadcast: the request's writer CTA may set a bit meanwhile,
+  // and every thread of this CTA must take the same branch
+  if (threadIdx.x == 0) s_st = *(volatile const int32_t*)&status[b];
+  __syncthreads();
+  if (s_st != 0 || a <= 0) return -1;
   int bad = 0;
   if (a > path_stride || P < 0) bad = SPEC_DEV_BAD_PATH;
   if (!bad) {
@@ -57,9 +52,27 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(
   if (threadIdx.x == 0) s_bad = bad;
   __syncthreads();
   bad = s_bad;
-  if (bad) {
+  __syncthreads();  // s_bad is read by every thread before a later call may write it
+  return bad;
+}
+
+// One CTA's share of a commit: kv-head h of request b in one cache (K or V
+// of one layer); `writer` CTAs set new_len and the status bits.
+__device__ __forceinline__ void commit_rows(char* __restrict__ cache, bool writer, int b, int h,
+                                            const int32_t* __restrict__ block_table, int max_blocks, int bs,
+                                            int num_blocks, const int32_t* __restrict__ prefix_len,
+                                            const int32_t* __restrict__ path, int path_stride,
+                                            const int32_t* __restrict__ accept_len, int Hkv, int row_bytes,
+                                            int32_t* __restrict__ new_len, int32_t* __restrict__ status) {
+  __shared__ uint4 buf[kCommitChunkBytes / 16];
+  const int P = prefix_len[b];
+  const int a = accept_len[b];
+  const int32_t* bt = block_table + (size_t)b * max_blocks;
+  const int32_t* pth = path + (size_t)b * path_stride;
+  const int bad = commit_check(b, bt, max_blocks, bs, num_blocks, P, a, pth, path_stride, status);
+  if (bad != 0) {
     if (writer && threadIdx.x == 0) {
-      atomicOr(&status[b], bad);
+      if (bad > 0) atomicOr(&status[b], bad);
       new_len[b] = P;
     }
     return;
@@ -88,6 +101,185 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(
   if (writer && threadIdx.x == 0) new_len[b] = P + a;
 }
 
+__global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(
+    char* __restrict__ k_cache, char* __restrict__ v_cache, const int32_t* __restrict__ block_table, int max_blocks,
+    int bs, int num_blocks, const int32_t* __restrict__ prefix_len, const int32_t* __restrict__ path, int path_stride,
+    const int32_t* __restrict__ accept_len, int Hkv, int row_bytes, int32_t* __restrict__ new_len,
+    int32_t* __restrict__ status) {
+  commit_rows(blockIdx.z == 0 ? k_cache : v_cache, blockIdx.y == 0 && blockIdx.z == 0, blockIdx.x, blockIdx.y,
+              block_table, max_blocks, bs, num_blocks, prefix_len, path, path_stride, accept_len, Hkv, row_bytes,
+              new_len, status);
+}
+
+// Every layer in one launch.  The caches are numbered c = 2 * layer (K) and
+// 2 * layer + 1 (V); CTA (b, h, z) moves kv-head h of request b in caches z,
+// z + Z, z + 2Z, ... (Z = gridDim.z, chosen so that the grid fills the GPU
+// about once).  The accepted rows that actually move (path[i] != i) are listed
+// once per CTA with their source and destination offsets, which every cache
+// shares; then (cache, row, 16-byte vector) is flattened and staged through
+// shared memory chunk by chunk, every read of a chunk before any write of it
+// (in each cache a chunk's sources lie above every earlier destination, the
+// same argument as for one cache).
+constexpr int kLayerRowBatch = 1024;
+constexpr int kLayerBufVec = 1536;  // 24 KB staging
+__global__ void __launch_bounds__(kCommitThreads) kv_commit_layers_kernel(
+    char* const* __restrict__ k_caches, char* const* __restrict__ v_caches, int n_caches,
+    const int32_t* __restrict__ block_table, int max_blocks, int bs, int num_blocks,
+    const int32_t* __restrict__ prefix_len, const int32_t* __restrict__ path, int path_stride,
+    const int32_t* __restrict__ accept_len, int Hkv, int row_bytes, int32_t* __restrict__ new_len,
+    int32_t* __restrict__ status) {
+  __shared__ uint4 buf[kLayerBufVec];
+  __shared__ long long s_src[kLayerRowBatch], s_dst[kLayerRowBatch];
+  __shared__ int s_warp[kCommitThreads / 32];
+  const int b = blockIdx.x, h = blockIdx.y, z = blockIdx.z, Z = gridDim.z;
+  const bool writer = h == 0 && z == 0;
+  const int P = prefix_len[b];
+  const int a = accept_len[b];
+  const int32_t* bt = block_table + (size_t)b * max_blocks;
+  const int32_t* pth = path + (size_t)b * path_stride;
+  const int bad = commit_check(b, bt, max_blocks, bs, num_blocks, P, a, pth, path_stride, status);
+  if (bad != 0) {
+    if (writer && threadIdx.x == 0) {
+      if (bad > 0) atomicOr(&status[b], bad);
+      new_len[b] = P;
+    }
+    return;
+  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int nq = (n_caches - z + Z - 1) / Z;  // caches of this CTA
+  const int vpr = row_bytes / 16;
+  auto slot = [&](int s) -> long long { return (((long long)bt[s / bs] * Hkv + h) * bs + s % bs) * row_bytes; };
+  auto cache_of = [&](int q) -> char* {
+    const int c = z + q * Z;
+    return (c & 1) ? v_caches[c >> 1] : k_caches[c >> 1];
+  };
+  constexpr int kPer = kLayerRowBatch / kCommitThreads;
+  for (int r0 = 0; r0 < a; r0 += kLayerRowBatch) {
+    const int r1 = min(a, r0 + kLayerRowBatch);
+    // list the moving rows of [r0, r1) in increasing i
+    const int i0 = r0 + threadIdx.x * kPer;
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) cnt += (i0 + e < r1 && pth[i0 + e] != i0 + e);
+    int incl = cnt;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[w] = incl;
+    __syncthreads();
+    int pos = 0, m = 0;
+    for (int k = 0; k < kCommitThreads / 32; ++k) {
+      pos += k < w ? s_warp[k] : 0;
+      m += s_warp[k];
+    }
+    pos += incl - cnt;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int i = i0 + e;
+      if (i < r1 && pth[i] != i) {
+        s_src[pos] = slot(P + pth[i]);
+        s_dst[pos] = slot(P + i);
+        ++pos;
+      }
+    }
+    __syncthreads();
+    const long long per_cache = (long long)m * vpr;
+    const long long total = per_cache * nq;
+    for (long long j0 = 0; j0 < total; j0 += kLayerBufVec) {
+      const int n = (int)min((long long)kLayerBufVec, total - j0);
+      for (int t = threadIdx.x; t < n; t += kCommitThreads) {
+        const long long j = j0 + t;
+        const int q = (int)(j / per_cache);
+        const int r = (int)(j - q * per_cache);
+        buf[t] = reinterpret_cast<const uint4*>(cache_of(q) + s_src[r / vpr])[r % vpr];
+      }
+      __syncthreads();
+      for (int t = threadIdx.x; t < n; t += kCommitThreads) {
+        const long long j = j0 + t;
+        const int q = (int)(j / per_cache);
+        const int r = (int)(j - q * per_cache);
+        reinterpret_cast<uint4*>(cache_of(q) + s_dst[r / vpr])[r % vpr] = buf[t];
+      }
+      __syncthreads();
+    }
+  }
+  if (writer && threadIdx.x == 0) new_len[b] = P + a;
+}
+
+// "SpecInfer Guide", "PagedKV Allocation with Zero-Copy Pruning": the pages
+// of request b's tree lying wholly past its new length, ceil(new_len / bs) ..
+// ceil((prefix + n) / bs) - 1, go back to the pool in one metadata update:
+// block-table entries -1, ids appended after *free_count in request, then
+// page order.  All or nothing: when the pool cannot take every page of the
+// call, none is released and each request that had pages to release is
+// flagged SPEC_DEV_CAPACITY.  Failed requests keep their pages.  One CTA.
+constexpr int kReleaseThreads = 1024;
+__global__ void __launch_bounds__(kReleaseThreads) kv_release_kernel(
+    int32_t* __restrict__ block_table, int max_blocks, int bs, const int32_t* __restrict__ prefix_len,
+    const int32_t* __restrict__ tree_off, const int32_t* __restrict__ new_len, int B, int32_t* __restrict__ free_pool,
+    int free_cap, int32_t* __restrict__ free_count, int32_t* __restrict__ status) {
+  __shared__ long long warp_tot[kReleaseThreads / 32];
+  __shared__ long long base;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  auto pages = [&](int b, int& keep) -> int {  // pages request b releases
+    if (status[b] != 0) return 0;
+    const int n = tree_off[b + 1] - tree_off[b];
+    keep = (new_len[b] + bs - 1) / bs;
+    const int span = min(max_blocks, (prefix_len[b] + n + bs - 1) / bs);
+    return span > keep ? span - keep : 0;
+  };
+  // the call's total
+  long long t = 0;
+  for (int b = threadIdx.x; b < B; b += kReleaseThreads) {
+    int keep;
+    t += pages(b, keep);
+  }
+  for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  if (lane == 0) warp_tot[w] = t;
+  __syncthreads();
+  long long total = 0;
+  for (int k = 0; k < kReleaseThreads / 32; ++k) total += warp_tot[k];
+  const long long start = *free_count;
+  if (start + total > free_cap) {
+    for (int b = threadIdx.x; b < B; b += kReleaseThreads) {
+      int keep;
+      if (pages(b, keep) > 0) atomicOr(&status[b], SPEC_DEV_CAPACITY);
+    }
+    return;
+  }
+  // in request order: an exclusive scan per round of kReleaseThreads requests
+  if (threadIdx.x == 0) base = start;
+  __syncthreads();
+  for (int b0 = 0; b0 < B; b0 += kReleaseThreads) {
+    const int b = b0 + threadIdx.x;
+    int keep = 0;
+    const int c = b < B ? pages(b, keep) : 0;
+    long long incl = c;
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    __syncthreads();  // warp_tot and base of the previous round are read
+    if (lane == 31) warp_tot[w] = incl;
+    __syncthreads();
+    long long wbase = base;
+    for (int k = 0; k < w; ++k) wbase += warp_tot[k];
+    const long long pos = wbase + incl - c;
+    if (c > 0) {
+      int32_t* row = block_table + (size_t)b * max_blocks;
+      for (int i = 0; i < c; ++i) {
+        free_pool[pos + i] = row[keep + i];
+        row[keep + i] = -1;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == kReleaseThreads - 1) base = wbase + incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *free_count = (int32_t)base;
+}
+
 }  // namespace spectree
 
 using namespace spectree;
@@ -110,5 +302,45 @@ extern "C" spec_status spec_kv_commit(void* k_cache, void* v_cache, const int32_
       (char*)k_cache, (char*)v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len, path, path_stride,
       accept_len, Hkv, row_bytes, new_len, status);
   SPEC_LAUNCH_CHECK();
+  return SPEC_OK;
+}
+
+extern "C" spec_status spec_kv_commit_layers(void* const* k_caches, void* const* v_caches, int layers,
+                                             int32_t* block_table, int max_blocks, int block_size, int num_blocks,
+                                             const int32_t* prefix_len, const int32_t* tree_off, const int32_t* path,
+                                             int path_stride, const int32_t* accept_len, int B, int Hkv, int D,
+                                             spec_dtype dtype, int32_t* new_len, int32_t* free_pool, int free_cap,
+                                             int32_t* free_count, int32_t* status, void* stream) {
+  if (B < 0 || layers <= 0 || Hkv <= 0 || max_blocks <= 0 || num_blocks <= 0 || path_stride <= 0 || free_cap < 0)
+    return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
+  if (block_size < 8 || block_size > 65536 || (block_size & (block_size - 1))) return SPEC_ERR_UNSUPPORTED;
+  if (B > 65535 || Hkv > 65535 || layers > 32767) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPEC_OK;
+  if (!k_caches || !v_caches || !block_table || !prefix_len || !path || !accept_len || !new_len || !status)
+    return SPEC_ERR_INVALID_ARG;
+  const bool release = free_pool != nullptr || free_count != nullptr;
+  if (release && (!free_pool || !free_count || !tree_off)) return SPEC_ERR_INVALID_ARG;
+  const int row_bytes = D * (dtype == SPEC_F32 ? 4 : 2);
+  // about one wave: Z cache groups per (request, kv-head), at least one
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return SPEC_ERR_CUDA;
+  const long long pairs = (long long)B * Hkv;
+  const int n_caches = 2 * layers;
+  const int Z = (int)std::min<long long>(n_caches, std::max<long long>(1, (4LL * sms + pairs - 1) / pairs));
+  dim3 grid(B, Hkv, Z);
+  spectree::kv_commit_layers_kernel<<<grid, spectree::kCommitThreads, 0, (cudaStream_t)stream>>>(
+      (char* const*)k_caches, (char* const*)v_caches, n_caches, block_table, max_blocks, block_size, num_blocks,
+      prefix_len, path, path_stride, accept_len, Hkv, row_bytes, new_len, status);
+  SPEC_LAUNCH_CHECK();
+  if (release) {
+    spectree::kv_release_kernel<<<1, spectree::kReleaseThreads, 0, (cudaStream_t)stream>>>(
+        block_table, max_blocks, block_size, prefix_len, tree_off, new_len, B, free_pool, free_cap, free_count,
+        status);
+    SPEC_LAUNCH_CHECK();
+  }
   return SPEC_OK;
 }
