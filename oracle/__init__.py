@@ -32,7 +32,12 @@ Pins (in tests/test_oracle_pins.py, all ``-m "not gpu"``):
   * stochastic: the two per-token examples of the "Inference Optimization
     Techniques" page (tests/golden), a Monte-Carlo chi-square test that the
     emitted tokens follow p, and the closed form E[T] = (1-a^(g+1))/(1-a) of
-    the same page on chains;
+    the same page on chains; with an inverse temperature tau the target is
+    softmax(l tau) and its residual (fp64 closed forms), and the emitted
+    tokens follow p^tau normalised (Monte Carlo); with per-child draft rows
+    the residuals after two rejections match the fp64 closed form in either
+    order, the emitted tokens follow p (Monte Carlo), and children whose
+    rows copy their parent's reproduce the per-parent mode exactly;
   * canonical exp: <= 2 ulp from libm's fp64 exp;
   * FX sums: equal to exact integer sums;
   * commit: invariants against a snapshot gather;
@@ -46,7 +51,7 @@ import numpy as np
 from . import build as _build
 
 F32, BF16 = 0, 1
-ST_BAD_TREE, ST_BAD_TOKEN, ST_CAPACITY, ST_BAD_BLOCK, ST_BAD_PATH = 1, 2, 4, 16, 32
+ST_BAD_TREE, ST_BAD_TOKEN, ST_CAPACITY, ST_BAD_BLOCK, ST_BAD_PATH, ST_BAD_TEMP = 1, 2, 4, 16, 32, 64
 
 _lib = None
 
@@ -62,7 +67,7 @@ def lib():
         L.oracle_tree_attention.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, i32, i32, i32, i32, i32, i32,
                                             f64, P, i64, P, P, P]
         L.oracle_verify_greedy.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P]
-        L.oracle_verify_stochastic.argtypes = [P, P, P, P, P, P, i32, i32, i32, P, P, P, P, P]
+        L.oracle_verify_stochastic.argtypes = [P, P, P, P, P, P, i32, i32, i32, P, i32, P, P, P, P, P]
         L.oracle_kv_commit.argtypes = [P, P, i64, P, i32, i32, i32, P, P, i32, P, i32, i32, i32, i32, P, P]
         L.oracle_kv_release.argtypes = [P, i32, i32, P, P, P, P, i32, P, i32, P]
         L.oracle_philox4x32_10.argtypes = [P, P, P]
@@ -74,7 +79,7 @@ def lib():
         L.oracle_fx.restype = u64
         L.oracle_f64_to_bf16.argtypes = [f64]
         L.oracle_f64_to_bf16.restype = ctypes.c_uint16
-        L.oracle_residual.argtypes = [P, P, i32, i32, P, P, P]
+        L.oracle_residual.argtypes = [P, P, i32, i32, ctypes.c_float, P, P, P]
         _lib = L
     return _lib
 
@@ -134,14 +139,20 @@ def verify_greedy(p_logits, tokens, parent, tree_off, n_max):
     return dict(path=path, accept_len=alen, emitted=emitted, n_emitted=nem, status=status)
 
 
-def verify_stochastic(p_logits, q_probs, tokens, parent, tree_off, uniforms, n_max):
+def verify_stochastic(p_logits, q_probs, tokens, parent, tree_off, uniforms, n_max, inv_temp=None,
+                      q_per_child=False):
+    """inv_temp: per-request inverse temperatures (None: 1); q_per_child:
+    q_probs row c is child c's own draft distribution (else row u serves
+    every child of u)."""
     p_logits, q_probs = _c(p_logits, np.float32), _c(q_probs, np.float32)
     tokens, parent, tree_off = _c(tokens, np.int32), _c(parent, np.int32), _c(tree_off, np.int32)
     uniforms = _c(uniforms, np.uint32)
     B, V = len(tree_off) - 1, p_logits.shape[-1]
+    tau = None if inv_temp is None else _c(inv_temp, np.float32)
     path, alen, emitted, nem, status = _verify_outputs(B, n_max)
     lib().oracle_verify_stochastic(_p(p_logits), _p(q_probs), _p(tokens), _p(parent), _p(tree_off), _p(uniforms),
-                                   B, n_max, V, _p(path), _p(alen), _p(emitted), _p(nem), _p(status))
+                                   B, n_max, V, None if tau is None else _p(tau), int(bool(q_per_child)),
+                                   _p(path), _p(alen), _p(emitted), _p(nem), _p(status))
     return dict(path=path, accept_len=alen, emitted=emitted, n_emitted=nem, status=status)
 
 
@@ -221,10 +232,14 @@ def f64_to_bf16_bits(x):
     return int(lib().oracle_f64_to_bf16(float(x)))
 
 
-def residual(l, q, j):
-    """Target distribution r_j and weights d_j of one row after j rejections."""
+def residual(l, q, j, inv_temp=1.0):
+    """Target distribution r_j and weights d_j of one row after j rejections:
+    q is one draft row (used j times) or j rows [j][V], one per rejection."""
     l, q = _c(l, np.float32), _c(q, np.float32)
     V = l.size
+    if q.ndim == 1:
+        q = np.ascontiguousarray(np.tile(q, (max(j, 1), 1)))
+    assert q.shape[0] >= j
     r, d, S = np.zeros(V, np.float32), np.zeros(V, np.float32), np.zeros(1, np.uint64)
-    lib().oracle_residual(_p(l), _p(q), V, j, _p(r), _p(d), _p(S))
+    lib().oracle_residual(_p(l), _p(q), V, j, ctypes.c_float(inv_temp), _p(r), _p(d), _p(S))
     return r, d, int(S[0])

@@ -33,7 +33,8 @@ enum {
     ORC_BAD_TOKEN = 2,  /* a token outside [0, V) */
     ORC_CAPACITY = 4,   /* prefix_len < 0 or prefix_len + n beyond the block table */
     ORC_BAD_BLOCK = 16, /* a block-table entry outside [0, num_blocks) */
-    ORC_BAD_PATH = 32   /* a commit path that is not a strictly increasing root path */
+    ORC_BAD_PATH = 32,  /* a commit path that is not a strictly increasing root path */
+    ORC_BAD_TEMP = 64   /* an inverse temperature that is not finite and positive */
 };
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
 
@@ -443,16 +444,21 @@ typedef struct {
     uint64_t S;
 } row_state;
 
-/* C4: row state of logits l (V entries); d holds the current weights
- * (e for j == 0), r the current target distribution r_j. */
-static void row_init(row_state *st, const float *l, int V)
+/* C4: row state of logits l (V entries) at inverse temperature tau
+ * ([SpecInfer guide] "Stochastic Verification Algorithm" samples at
+ * temperature T > 0: the target is softmax(l / T), here with tau = 1/T given
+ * in fp32 and applied as one rounded multiply of l - m); d holds the current
+ * weights (e for j == 0), r the current target distribution r_j. */
+static void row_init(row_state *st, const float *l, int V, float tau)
 {
     float m = l[0];
     for (int x = 1; x < V; x++)
         if (l[x] > m) m = l[x];
     uint64_t S = 0;
     for (int x = 0; x < V; x++) {
-        st->e[x] = oracle_canon_exp(l[x] - m);
+        float y = l[x] - m;
+        y = y * tau;
+        st->e[x] = oracle_canon_exp(y);
         S += oracle_fx(st->e[x]);
     }
     st->S = S;
@@ -493,16 +499,18 @@ static int row_sample(const row_state *st, int V, uint32_t U)
 }
 
 /* Exposed for the per-token pins: the target distribution r_j of a row
- * (logits l, draft q) after j rejections, and its weights d_j. */
-void oracle_residual(const float *l, const float *q, int V, int j, float *r_out, float *d_out, uint64_t *S_out)
+ * (logits l at inverse temperature tau) after j rejections against the
+ * draft rows q[0..j-1] (each V entries), and its weights d_j. */
+void oracle_residual(const float *l, const float *q, int V, int j, float tau, float *r_out, float *d_out,
+                     uint64_t *S_out)
 {
     row_state st;
     st.e = (float *)malloc(sizeof(float) * (size_t)V * 4);
     st.d = st.e + V;
     st.r = st.d + V;
     st.dn = st.r + V;
-    row_init(&st, l, V);
-    for (int k = 0; k < j; k++) row_reject(&st, q, V);
+    row_init(&st, l, V, tau);
+    for (int k = 0; k < j; k++) row_reject(&st, q + (size_t)k * V, V);
     memcpy(r_out, st.r, sizeof(float) * (size_t)V);
     memcpy(d_out, st.d, sizeof(float) * (size_t)V);
     *S_out = st.S;
@@ -514,10 +522,20 @@ void oracle_residual(const float *l, const float *q, int V, int j, float *r_out,
  * target to the next residual (C5); the first accepted child becomes the
  * new node; if every child is rejected, or u is a leaf, a token is sampled
  * from the current weights (C7) and the walk ends.  Outputs as in
- * oracle_verify_greedy.  status[b] is written. */
+ * oracle_verify_greedy.  status[b] is written.
+ *
+ * inv_temp[b] (NULL: 1) is request b's inverse temperature (C4); it must be
+ * finite and positive, else the request gets ORC_BAD_TEMP and is skipped.
+ * Draft rows: with q_per_child == 0, q_probs row u is the distribution all
+ * children of u were drawn from (one draft model expanding u).  With
+ * q_per_child != 0, row c is the distribution child c itself was drawn from
+ * ([SpecInfer guide] "Merge-Based Tree Construction": siblings proposed by
+ * different draft models); child c is then tested against, and on rejection
+ * subtracted as, its own row: accept iff u * q_c(t_c) <= r_j(t_c), and
+ * r_{j+1} = norm(max(r_j - q_c, 0)). */
 int oracle_verify_stochastic(const float *p_logits, const float *q_probs, const int32_t *tokens,
                              const int32_t *parent, const int32_t *tree_off, const uint32_t *uniforms,
-                             int B, int n_max, int V,
+                             int B, int n_max, int V, const float *inv_temp, int q_per_child,
                              int32_t *path, int32_t *accept_len, int32_t *emitted, int32_t *n_emitted,
                              int32_t *status)
 {
@@ -530,6 +548,8 @@ int oracle_verify_stochastic(const float *p_logits, const float *q_probs, const 
         int off = tree_off[b], n = tree_off[b + 1] - off;
         clear_outputs(b, n_max, path, accept_len, emitted, n_emitted);
         status[b] = verify_checks(parent, tokens, off, n, n_max, V);
+        const float tau = inv_temp ? inv_temp[b] : 1.0f;
+        if (!(tau > 0.0f) || isinf(tau)) status[b] |= ORC_BAD_TEMP;
         if (status[b] != 0 || n == 0) continue;
         const int32_t *par = parent + off;
         int32_t *pth = path + (size_t)b * n_max, *emt = emitted + (size_t)b * n_max;
@@ -538,17 +558,18 @@ int oracle_verify_stochastic(const float *p_logits, const float *q_probs, const 
         for (;;) {
             const float *l = p_logits + (size_t)(off + u) * V;
             const float *q = q_probs + (size_t)(off + u) * V;
-            row_init(&st, l, V);
+            row_init(&st, l, V, tau);
             int accepted = -1;
             for (int c = u + 1; c < n; c++) {
                 if (par[c] != u) continue;
                 int t = tokens[off + c];
+                const float *qc = q_per_child ? q_probs + (size_t)(off + c) * V : q;
                 float ua = (float)(uniforms[(size_t)(off + c) * 2] >> 8) * 0x1p-24f;
-                if (ua * q[t] <= st.r[t]) {
+                if (ua * qc[t] <= st.r[t]) {
                     accepted = c;
                     break;
                 }
-                row_reject(&st, q, V);
+                row_reject(&st, qc, V);
             }
             if (accepted >= 0) {
                 emt[len - 1] = tokens[off + accepted];

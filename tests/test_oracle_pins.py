@@ -358,10 +358,15 @@ def _p_row(key, V):
     return rng.dirichlet(np.full(V, 0.7))
 
 
-def mc_tree_inputs(n_trials, V, root_kids, kid_kids, seed):
+def mc_tree_inputs(n_trials, V, root_kids, kid_kids, seed, per_child=False):
     """Inputs of n_trials depth-2 trees whose draft tokens are i.i.d. draws
     from the parent's draft row; p and q rows are fixed functions of the token
-    path.  Returns (dict of verifier inputs, table of p rows by path)."""
+    path.  Returns (dict of verifier inputs, table of p rows by path).
+    per_child: each sibling is drawn from a row of its own (the i-th child
+    of a node from draft model i, as in a merged tree), and q_probs row c is
+    the row child c was drawn from."""
+    if per_child:
+        return _mc_tree_inputs_per_child(n_trials, V, root_kids, kid_kids, seed)
     rng = np.random.default_rng(seed)
     key0 = seed * 1000
 
@@ -409,6 +414,51 @@ def mc_tree_inputs(n_trials, V, root_kids, kid_kids, seed):
     return inputs, P1
 
 
+def _mc_tree_inputs_per_child(n_trials, V, root_kids, kid_kids, seed):
+    rng = np.random.default_rng(seed)
+    key0 = seed * 1000 + 500
+
+    def p_of(path):
+        return _p_row((key0, 1) + tuple(path), V)
+
+    def qk(i, path):  # draft model i's row after the token path
+        return _p_row((key0, 3, i) + tuple(path), V)
+
+    n = 1 + root_kids + root_kids * kid_kids
+    parent = np.array([-1] + [0] * root_kids + [1 + i for i in range(root_kids) for _ in range(kid_kids)], np.int32)
+    P1 = {(): p_of(())}
+    for a in range(V):
+        P1[(a,)] = p_of((a,))
+        for b in range(V):
+            P1[(a, b)] = p_of((a, b))
+    t1 = np.stack([rng.choice(V, n_trials, p=qk(i, ())) for i in range(root_kids)], 1)
+    t2 = np.zeros((n_trials, root_kids, kid_kids), np.int64)
+    for a in range(V):
+        sel = t1 == a
+        cnt = int(sel.sum())
+        t2[sel] = np.stack([rng.choice(V, cnt, p=qk(j, (a,))) for j in range(kid_kids)], 1)
+    tokens = np.concatenate([np.zeros((n_trials, 1), np.int64), t1, t2.reshape(n_trials, -1)], 1).astype(np.int32)
+    logp = np.zeros((n_trials, n, V), np.float32)
+    qpr = np.zeros((n_trials, n, V), np.float32)
+    logp[:, 0] = np.log(P1[()])
+    qpr[:, 0] = 1.0 / V  # the root's own row is never read
+    for i in range(root_kids):
+        qpr[:, 1 + i] = qk(i, ())
+    for a in range(V):
+        logp[:, 1:1 + root_kids][t1 == a] = np.log(P1[(a,)])
+        for i in range(root_kids):
+            for j in range(kid_kids):
+                qpr[t1[:, i] == a, 1 + root_kids + i * kid_kids + j] = qk(j, (a,))
+        for b in range(V):
+            flat = ((t1[:, :, None] == a) & (t2 == b)).reshape(n_trials, -1)
+            logp[:, 1 + root_kids:][flat] = np.log(P1[(a, b)])
+    uni = rng.integers(0, 2 ** 32, (n_trials * n, 2), dtype=np.uint64).astype(np.uint32)
+    inputs = dict(p_logits=logp.reshape(-1, V), q_probs=qpr.reshape(-1, V), tokens=tokens.reshape(-1),
+                  parent=np.tile(parent, n_trials), tree_off=np.arange(0, n * n_trials + 1, n, dtype=np.int32),
+                  uniforms=uni, n_max=n)
+    return inputs, P1
+
+
 def _run_mc_tree(oracle, n_trials, V, root_kids, kid_kids, seed):
     inputs, P1 = mc_tree_inputs(n_trials, V, root_kids, kid_kids, seed)
     return oracle.verify_stochastic(**inputs), P1
@@ -442,6 +492,124 @@ def test_stochastic_emits_target_distribution(oracle, seed, root_kids, kid_kids)
             continue
         second = r["emitted"][sel, 1]
         assert _chisq_pvalue(np.bincount(second, minlength=V), P[(x,)]) > 1e-4, x
+
+
+def _tempered(p, tau):
+    w = np.asarray(p, np.float64) ** tau
+    return w / w.sum()
+
+
+def _softmax64(l, tau=1.0):
+    z = np.asarray(l, np.float64) * tau
+    e = np.exp(z - z.max())
+    return e / e.sum()
+
+
+@pytest.mark.parametrize("tau", [0.25, 0.5, 1.0, 2.0, 3.7])
+def test_temperature_target_is_tempered_softmax(oracle, tau):
+    """Sampling at temperature T ("Stochastic Verification Algorithm"): the
+    row's target is softmax(l / T), here with tau = 1/T; after a rejection the
+    residual is norm(max(softmax(l tau) - q, 0)) (fp64 closed forms)."""
+    rng = np.random.default_rng(int(tau * 100))
+    V = 1000
+    l = (3.0 * rng.standard_normal(V)).astype(np.float32)
+    q = rng.dirichlet(np.full(V, 0.3)).astype(np.float32)
+    r0, _, _ = oracle.residual(l, q, 0, tau)
+    ref0 = _softmax64(l, tau)
+    np.testing.assert_allclose(r0, ref0, rtol=2e-5, atol=1e-12)
+    r1, _, _ = oracle.residual(l, q, 1, tau)
+    d = np.maximum(ref0 - q.astype(np.float64), 0)
+    np.testing.assert_allclose(r1, d / d.sum(), rtol=0, atol=2e-6)
+
+
+def test_per_child_residuals_follow_each_siblings_row(oracle):
+    """Merged trees ("Merge-Based Tree Construction"): siblings drawn from
+    different draft rows; each rejection subtracts the rejected child's own
+    row: r_2 = norm(max(norm(max(p - q1, 0)) - q2, 0)) (fp64 closed form)."""
+    rng = np.random.default_rng(12)
+    V = 500
+    l = (2.0 * rng.standard_normal(V)).astype(np.float32)
+    q1 = rng.dirichlet(np.full(V, 0.5)).astype(np.float32)
+    q2 = rng.dirichlet(np.full(V, 0.5)).astype(np.float32)
+    r2, _, _ = oracle.residual(l, np.stack([q1, q2]), 2)
+    p = _softmax64(l)
+    d1 = np.maximum(p - q1, 0)
+    r1 = d1 / d1.sum()
+    d2 = np.maximum(r1 - q2, 0)
+    np.testing.assert_allclose(r2, d2 / d2.sum(), rtol=0, atol=2e-6)
+    # and the other order gives the other closed form
+    r2b, _, _ = oracle.residual(l, np.stack([q2, q1]), 2)
+    d1b = np.maximum(p - q2, 0)
+    d2b = np.maximum(d1b / d1b.sum() - q1, 0)
+    np.testing.assert_allclose(r2b, d2b / d2b.sum(), rtol=0, atol=2e-6)
+
+
+@pytest.mark.parametrize("tau", [0.5, 2.0])
+def test_stochastic_with_temperature_emits_tempered_target(oracle, tau):
+    """Losslessness at temperature T: the first emitted token follows
+    p(.|root)^(1/T) normalised, the second p(.|x)^(1/T) normalised."""
+    V, N = 8, 200_000
+    inputs, P = mc_tree_inputs(N, V, 3, 2, 11)
+    r = oracle.verify_stochastic(**inputs, inv_temp=np.full(N, tau, np.float32))
+    assert (r["status"] == 0).all()
+    first = r["emitted"][:, 0]
+    assert _chisq_pvalue(np.bincount(first, minlength=V), _tempered(P[()], tau)) > 1e-4
+    # the untempered target is rejected at this sample size
+    assert _chisq_pvalue(np.bincount(first, minlength=V), P[()]) < 1e-6
+    cont = r["accept_len"] >= 2
+    for x in range(V):
+        sel = cont & (first == x)
+        if sel.sum() < 2000:
+            continue
+        assert _chisq_pvalue(np.bincount(r["emitted"][sel, 1], minlength=V), _tempered(P[(x,)], tau)) > 1e-4, x
+
+
+@pytest.mark.parametrize("seed,root_kids,kid_kids", [(21, 3, 2), (22, 2, 3), (23, 4, 1)])
+def test_stochastic_per_child_rows_emit_target_distribution(oracle, seed, root_kids, kid_kids):
+    """Losslessness with siblings from different draft models (each child
+    tested against, and on rejection subtracted as, its own row)."""
+    V, N = 8, 200_000
+    inputs, P = mc_tree_inputs(N, V, root_kids, kid_kids, seed, per_child=True)
+    r = oracle.verify_stochastic(**inputs, q_per_child=True)
+    assert (r["status"] == 0).all()
+    first = r["emitted"][:, 0]
+    assert _chisq_pvalue(np.bincount(first, minlength=V), P[()]) > 1e-4
+    cont = r["accept_len"] >= 2
+    for x in range(V):
+        sel = cont & (first == x)
+        if sel.sum() < 2000:
+            continue
+        assert _chisq_pvalue(np.bincount(r["emitted"][sel, 1], minlength=V), P[(x,)]) > 1e-4, x
+
+
+def test_per_child_rows_copied_from_parents_equal_per_parent_mode(oracle):
+    """Special case: when every child's row is its parent's row, the per-child
+    layout is the per-parent one, outcome for outcome; and tau = 1 given
+    explicitly is the default."""
+    inputs, _ = mc_tree_inputs(3000, 8, 3, 2, 5)
+    r0 = oracle.verify_stochastic(**inputs)
+    par = inputs["parent"]
+    n = inputs["n_max"]
+    qc = inputs["q_probs"].copy()
+    for g in range(len(par)):
+        if par[g] >= 0:
+            qc[g] = inputs["q_probs"][(g // n) * n + par[g]]
+    r1 = oracle.verify_stochastic(**dict(inputs, q_probs=qc), q_per_child=True)
+    r2 = oracle.verify_stochastic(**inputs, inv_temp=np.ones(3000, np.float32))
+    for k in r0:
+        assert np.array_equal(r0[k], r1[k]) and np.array_equal(r0[k], r2[k]), k
+
+
+def test_bad_inverse_temperature_is_flagged(oracle):
+    logits = np.zeros((10, 4), np.float32)
+    qp = np.full((10, 4), 0.25, np.float32)
+    tokens = np.array([0, 1] * 4 + [0, 7], np.int32)
+    parent = np.array([-1, 0] * 5, np.int32)
+    uni = np.zeros((10, 2), np.uint32)
+    tau = np.array([0.0, -1.0, np.inf, np.nan, np.inf], np.float32)
+    r = oracle.verify_stochastic(logits, qp, tokens, parent, [0, 2, 4, 6, 8, 10], uni, 2, inv_temp=tau)
+    assert r["status"].tolist() == [oracle.ST_BAD_TEMP] * 4 + [oracle.ST_BAD_TEMP | oracle.ST_BAD_TOKEN]
+    assert (r["accept_len"] == 0).all() and (r["path"] == -1).all()
 
 
 def test_stochastic_chain_matches_closed_form_expected_tokens(oracle):
