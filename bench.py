@@ -321,7 +321,11 @@ def bench_gpu(args):
         works.append(w)
         d = DeviceBatch.from_workload(w, device=dev)
         sets.append(d)
-        passes.append(VerifyPass(d))
+        vp = VerifyPass(d)
+        if args.temperature is not None:
+            vp.inv_temp = torch.full((w.B,), 1.0 / args.temperature, dtype=torch.float32, device=dev)
+        vp.q_layout = S.SPEC_Q_PER_CHILD if args.q_per_child else S.SPEC_Q_PER_PARENT
+        passes.append(vp)
     torch.cuda.synchronize()
 
     stages = ("mask", "attention", "verify", "commit")
@@ -421,6 +425,7 @@ def bench_gpu(args):
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl["desc"], "verify": args.mode, "input_sets": n_sets,
+                       "temperature": args.temperature, "draft_rows": "per child" if args.q_per_child else "per parent",
                        "l2": (f"{n_sets} rotating input sets of {_set_mb(works[0]):.0f} MB each (inputs larger than L2)"
                               if n_sets > 1 else f"one input set of {_set_mb(works[0]):.0f} MB (larger than L2)"),
                        "launch": "one CUDA graph per step (the C-ABI calls of the pass captured, no event nodes)",
@@ -609,6 +614,10 @@ def main():
     ap.add_argument("--workload", type=int, default=1, choices=sorted(WORKLOADS))
     ap.add_argument("--attn-flags", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--temperature", type=float, default=None,
+                    help="stochastic verification at this temperature for every request (default: none, T = 1)")
+    ap.add_argument("--q-per-child", action="store_true",
+                    help="read the draft rows per child (merged trees) instead of per parent")
     ap.add_argument("--commit-layers", type=int, default=0,
                     help="also time the commit of this many layers' caches in one launch (0: off)")
     args = ap.parse_args()

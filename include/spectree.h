@@ -66,6 +66,7 @@ typedef int32_t spec_status;
 #define SPEC_DEV_TIMEOUT 8    /* a bounded device wait expired (the kernel returned early) */
 #define SPEC_DEV_BAD_BLOCK 16 /* a block-table entry outside [0, num_blocks) */
 #define SPEC_DEV_BAD_PATH 32  /* a commit path that is not strictly increasing from node 0 */
+#define SPEC_DEV_BAD_TEMP 64  /* stochastic verify: an inverse temperature that is not finite and positive */
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 
@@ -207,23 +208,39 @@ spec_status spec_tree_verify_greedy(const float* p_logits, const int32_t* tokens
  * node.  When every child is rejected, a token is sampled from the last
  * residual; at a leaf, the bonus token is sampled from p.  The emitted tokens
  * follow the target distribution when each node's children were drawn
- * i.i.d. from q_probs of that node.
+ * i.i.d. from q_probs of that node (SPEC_Q_PER_PARENT), or each child
+ * independently from its own row (SPEC_Q_PER_CHILD: "Merge-Based Tree
+ * Construction", siblings proposed by different draft models; child c is
+ * tested against, and on rejection subtracted as, row c).  Sampling at
+ * temperature T > 0 ("Stochastic Verification Algorithm"): the target is
+ * softmax(p_logits / T), given as the inverse temperature tau = 1/T per
+ * request; q_probs are the draft's probabilities as drawn (its own
+ * temperature already applied).
  * Arithmetic (fixed so that every decision is reproducible bit for bit):
- * p = softmax(p_logits) with its own fp32 exp (x <= 0: Cody-Waite reduction,
- * degree-7 Taylor polynomial), normalisers as exact fixed-point sums of
- * trunc(v * 2^46); accept iff u * q(t) <= r(t) with u = (word0 >> 8) * 2^-24;
- * terminal sample = smallest x whose fixed-point prefix sum exceeds
+ * p = softmax(tau * p_logits) with e = E(fp32(fp32(l - max l) * tau)), E
+ * the library's own fp32 exp (x <= 0: Cody-Waite reduction, degree-7 Taylor
+ * polynomial), normalisers as exact fixed-point sums of trunc(v * 2^46);
+ * accept iff u * q(t) <= r(t) with u = (word0 >> 8) * 2^-24; terminal
+ * sample = smallest x whose fixed-point prefix sum exceeds
  * floor(word1 * S / 2^32).
- *   q_probs    float [T][V]    row u: the draft distribution the children of u were drawn from
- *   uniforms   uint32 [T][2]   raw random words: [t][0] acceptance word of node t,
- *                              [t][1] sampling word used if the walk stops at node t
+ *   q_probs          float [T][V]  SPEC_Q_PER_PARENT: row u is the draft distribution the
+ *                                  children of u were drawn from; SPEC_Q_PER_CHILD: row c is
+ *                                  the distribution node c was drawn from (row 0 unused)
+ *   uniforms         uint32 [T][2] raw random words: [t][0] acceptance word of node t,
+ *                                  [t][1] sampling word used if the walk stops at node t
+ *   inv_temperature  float [B]     tau of each request, or NULL for tau = 1 (device memory).
+ *                                  A tau that is not finite and positive sets
+ *                                  SPEC_DEV_BAD_TEMP; the request is skipped.
+ *   q_layout         SPEC_Q_PER_PARENT or SPEC_Q_PER_CHILD (else SPEC_ERR_INVALID_ARG)
  *   other arguments as in spec_tree_verify_greedy.  One cluster per request
  *   follows the walk: a node's target row is read when the walk reaches it,
- *   its draft row when one of its children is rejected.
+ *   a draft row when a child is rejected against it.
  */
+#define SPEC_Q_PER_PARENT 0
+#define SPEC_Q_PER_CHILD 1
 spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_probs, const int32_t* tokens,
                                         const int32_t* parent, const int32_t* tree_off, const uint32_t* uniforms,
-                                        int B, int n_max, int V,
+                                        const float* inv_temperature, int q_layout, int B, int n_max, int V,
                                         int32_t* path, int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
                                         void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 

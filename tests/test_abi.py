@@ -89,8 +89,10 @@ def test_host_argument_checks_return_codes_without_launching(libpath):
         S.SPEC_ERR_UNSUPPORTED
     assert L.spec_tree_verify_greedy(*v[:4], 1, 4, 1000, None, None, None, None, None, 0, None, None) == \
         S.SPEC_ERR_INVALID_ARG
-    assert L.spec_tree_verify_stochastic(*v, 1, 4, 0, None, None, None, None, None, 0, None, None) == \
+    assert L.spec_tree_verify_stochastic(*v, None, 0, 1, 4, 0, None, None, None, None, None, 0, None, None) == \
         S.SPEC_ERR_INVALID_ARG
+    assert L.spec_tree_verify_stochastic(*v, None, 2, 1, 4, 1000, None, None, None, None, None, 0, None, None) == \
+        S.SPEC_ERR_INVALID_ARG  # unknown draft-row layout
     # commit: head dim, page size
     assert L.spec_kv_commit(None, None, None, 4, 16, 4, None, None, 4, None, 1, 2, 80, 1, None, None, None) == \
         S.SPEC_ERR_UNSUPPORTED

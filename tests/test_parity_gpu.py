@@ -252,6 +252,102 @@ def test_stochastic_gpu_matches_oracle_on_monte_carlo_trees():
     assert np.array_equal(alen.cpu().numpy(), r["accept_len"])
 
 
+# ------------------------------------ temperature and per-child draft rows ----
+
+def _gpu_verify_opts(w, inv_temp=None, q_layout=S.SPEC_Q_PER_PARENT, ws_bytes=None):
+    vp = _pass(w)
+    if ws_bytes is not None:  # 256 bytes: no room for row statistics, the walk makes them
+        vp.verify_ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    vp.mask_build()
+    tau = None if inv_temp is None else torch.from_numpy(np.asarray(inv_temp, np.float32)).cuda()
+    vp.verify("stochastic", inv_temp=tau, q_layout=q_layout)
+    torch.cuda.synchronize()
+    return dict(path=vp.path.cpu().numpy(), accept_len=vp.accept_len.cpu().numpy(),
+                emitted=vp.emitted.cpu().numpy(), n_emitted=vp.n_emitted.cpu().numpy(),
+                status=vp.status.cpu().numpy())
+
+
+def _oracle_opts(w, inv_temp=None, q_per_child=False):
+    return O.verify_stochastic(w.p_logits.numpy(), w.q_probs.numpy(), w.tokens.numpy(), w.parent.numpy(),
+                               w.tree_off.numpy(), w.uniforms.numpy().view(np.uint32), w.n_max,
+                               inv_temp=inv_temp, q_per_child=q_per_child)
+
+
+OPTS_VERIFY = [c for c in SMALL_VERIFY if c["V"] in (7, 64, 1000, 4099, 32000, 128256)]
+
+
+@pytest.mark.parametrize("cfg", OPTS_VERIFY, ids=lambda c: f"V{c['V']}_s{c['seed']}")
+@pytest.mark.parametrize("ws", ["full", "256"])
+@pytest.mark.parametrize("layout", [S.SPEC_Q_PER_PARENT, S.SPEC_Q_PER_CHILD])
+def test_stochastic_temperature_and_layout_parity(cfg, ws, layout):
+    """Per-request inverse temperatures (0.3 ... 4) and both draft-row
+    layouts, with and without row statistics: every output bit-exact."""
+    w = W.small_random(cfg["seed"] + 100, B=cfg["B"], n_range=cfg["n_range"], prefix_range=(0, 4), Hq=2, Hkv=1,
+                       D=64, V=cfg["V"], block_size=16)
+    g = np.random.default_rng(cfg["seed"])
+    # draft rows away from the target: rejections, and several residual steps per node, are common
+    w.q_probs = torch.softmax(torch.from_numpy(g.standard_normal((w.T, w.V)).astype(np.float32)) * 3, -1)
+    tau = g.choice(np.array([0.3, 0.7, 1.0, 1.6, 4.0], np.float32), w.B)
+    ref = _oracle_opts(w, tau, layout == S.SPEC_Q_PER_CHILD)
+    got = _gpu_verify_opts(w, tau, layout, None if ws == "full" else 256)
+    _assert_verify_equal(got, ref, w.B)
+    assert (got["status"][:w.B] == 0).all()
+
+
+@pytest.mark.parametrize("ws", ["full", "256"])
+def test_per_child_star_with_frozen_residuals(ws):
+    """A 120-child star per request with per-child rows; a third of the
+    children have an all-ones row, so rejecting them leaves a zero-sum
+    residual (the state freezes after a varying number of steps), and every
+    acceptance word is at its maximum."""
+    n, V, B = 121, 4099, 3
+    g = np.random.default_rng(9)
+    w = W.small_random(45, B=B, n_range=(n, n), prefix_range=(0, 1), Hq=2, Hkv=1, D=64, V=V, block_size=16)
+    w.parent = torch.cat([torch.tensor([-1] + [0] * (n - 1), dtype=torch.int32)] * B)
+    q = torch.softmax(torch.from_numpy(g.standard_normal((w.T, V)).astype(np.float32)) * 3, -1)
+    ones = torch.from_numpy(g.random(w.T) < 0.33)
+    q[ones] = 1.0
+    w.q_probs = q
+    w.uniforms[:, 0] = -1
+    ref = _oracle_opts(w, None, True)
+    got = _gpu_verify_opts(w, None, S.SPEC_Q_PER_CHILD, None if ws == "full" else 256)
+    _assert_verify_equal(got, ref, B)
+
+
+def test_bad_inverse_temperature_status():
+    w = W.small_random(46, B=6, n_range=(2, 9), prefix_range=(0, 1), Hq=2, Hkv=1, D=64, V=1000, block_size=16)
+    tau = np.array([0.0, -1.0, np.inf, np.nan, 1.0, 0.5], np.float32)
+    ref = _oracle_opts(w, tau)
+    got = _gpu_verify_opts(w, tau)
+    _assert_verify_equal(got, ref, w.B)
+    assert got["status"].tolist()[:4] == [S.SPEC_DEV_BAD_TEMP] * 4 and got["status"][4] == got["status"][5] == 0
+
+
+def test_per_child_gpu_matches_oracle_on_monte_carlo_trees():
+    """The oracle's per-child Monte-Carlo workload (siblings from different
+    draft rows) through the GPU verifier, trial by trial, at tau = 1 and 2."""
+    from test_oracle_pins import mc_tree_inputs
+    V, N = 8, 20000
+    c, _ = mc_tree_inputs(N, V, 3, 2, 21, per_child=True)
+    B, n_max, dev = len(c["tree_off"]) - 1, c["n_max"], "cuda"
+
+    def d(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    for tau_v in (1.0, 2.0):
+        tau = np.full(B, tau_v, np.float32)
+        r = O.verify_stochastic(**c, inv_temp=tau, q_per_child=True)
+        outs = [torch.zeros((B, n_max), dtype=torch.int32, device=dev), torch.zeros(B, dtype=torch.int32, device=dev),
+                torch.zeros((B, n_max), dtype=torch.int32, device=dev), torch.zeros(B, dtype=torch.int32, device=dev)]
+        st = torch.zeros(B, dtype=torch.int32, device=dev)
+        ws = torch.empty(S.spec_verify_workspace_size(B, n_max, V), dtype=torch.uint8, device=dev)
+        S.spec_tree_verify_stochastic(d(c["p_logits"]), d(c["q_probs"]), d(c["tokens"]), d(c["parent"]),
+                                      d(c["tree_off"]), d(c["uniforms"].view(np.int32)), B, n_max, V, *outs, ws, st,
+                                      inv_temp=d(tau), q_layout=S.SPEC_Q_PER_CHILD)
+        torch.cuda.synchronize()
+        assert np.array_equal(outs[2].cpu().numpy(), r["emitted"])
+        assert np.array_equal(outs[1].cpu().numpy(), r["accept_len"])
+
+
 # ------------------------------------------------------------- attention ----
 
 def _gpu_attention(w, flags=S.SPEC_ATTN_AUTO, max_prefix=None):

@@ -13,7 +13,8 @@ LIB_PATH = os.path.join(_PKG, "libspectree.so")
 
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA, SPEC_ERR_WORKSPACE = 0, 1, 2, 3, 4
 SPEC_DEV_BAD_TREE, SPEC_DEV_BAD_TOKEN, SPEC_DEV_CAPACITY, SPEC_DEV_TIMEOUT = 1, 2, 4, 8
-SPEC_DEV_BAD_BLOCK, SPEC_DEV_BAD_PATH = 16, 32
+SPEC_DEV_BAD_BLOCK, SPEC_DEV_BAD_PATH, SPEC_DEV_BAD_TEMP = 16, 32, 64
+SPEC_Q_PER_PARENT, SPEC_Q_PER_CHILD = 0, 1  # layouts of the draft rows
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_ATTN_AUTO, SPEC_ATTN_CUDA_CORE, SPEC_ATTN_TCGEN05 = 0, 1, 2
 SPEC_ATTN_NOALLOC_BYTES = 16 << 20  # scratch of spec_tree_attention_noalloc
@@ -32,7 +33,7 @@ SIGNATURES = {
                                      _P, _U32, _P], _I),
     "spec_verify_workspace_size": ([_I, _I, _I], _SZ),
     "spec_tree_verify_greedy": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
-    "spec_tree_verify_stochastic": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
+    "spec_tree_verify_stochastic": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "spec_kv_commit": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "spec_kv_commit_layers": ([_P, _P, _I, _P, _I, _I, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P],
                               _I),
@@ -143,10 +144,14 @@ def spec_tree_verify_greedy(p_logits, tokens, parent, tree_off, B, n_max, V, pat
 
 
 def spec_tree_verify_stochastic(p_logits, q_probs, tokens, parent, tree_off, uniforms, B, n_max, V, path,
-                                accept_len, emitted, n_emitted, workspace, status, stream=None):
+                                accept_len, emitted, n_emitted, workspace, status, stream=None, inv_temp=None,
+                                q_layout=SPEC_Q_PER_PARENT):
+    """inv_temp: float32 device tensor [B] of inverse temperatures, or None
+    (1); q_layout: SPEC_Q_PER_PARENT or SPEC_Q_PER_CHILD."""
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("spec_tree_verify_stochastic", lib().spec_tree_verify_stochastic(
-        _ptr(p_logits), _ptr(q_probs), _ptr(tokens), _ptr(parent), _ptr(tree_off), _ptr(uniforms), B, n_max, V,
+        _ptr(p_logits), _ptr(q_probs), _ptr(tokens), _ptr(parent), _ptr(tree_off), _ptr(uniforms), _ptr(inv_temp),
+        q_layout, B, n_max, V,
         _ptr(path), _ptr(accept_len), _ptr(emitted), _ptr(n_emitted), _ptr(workspace), ws_bytes, _ptr(status),
         _stream(stream)))
 

@@ -397,7 +397,14 @@ struct VerifyArgs {
   int32_t* n_emitted;
   int32_t* status;
   const RowStats* stats;  // stochastic: every node's row statistics, or null (the walk computes them)
+  const float* inv_temp;  // stochastic: per-request inverse temperature, or null (1)
+  int q_per_child;        // stochastic: q_probs row c is child c's own draft row (else row u serves u's children)
 };
+
+// A request's inverse temperature tau (1 without an array); usable iff
+// finite and positive.
+__device__ __forceinline__ float request_tau(const VerifyArgs& a, int b) { return a.inv_temp ? a.inv_temp[b] : 1.0f; }
+__device__ __forceinline__ bool tau_ok(float t) { return t > 0.0f && t <= 3.402823466e38f; }
 
 struct WalkShared {
   Red red;
@@ -511,6 +518,9 @@ __global__ void __launch_bounds__(kStatsThreads) row_stats_kernel(VerifyArgs a, 
   const int off = a.tree_off[b];
   const int n = a.tree_off[b + 1] - off;
   if (n < 1 || n > a.n_max || u >= n) return;  // uniform across the CTA
+  const float tau = request_tau(a, b);
+  if (!tau_ok(tau)) return;  // the walk flags the request
+  const float2 tau2 = f2(tau);
   const int V = a.V, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* row = a.p_logits + (size_t)(off + u) * V;
   const float4* r4 = reinterpret_cast<const float4*>(row);
@@ -537,14 +547,15 @@ __global__ void __launch_bounds__(kStatsThreads) row_stats_kernel(VerifyArgs a, 
 #pragma unroll 4
     for (int j = threadIdx.x; j < (V >> 2); j += kStatsThreads) {
       const float4 v = __ldg(r4 + j);
-      fx_add2(acc, canon_exp2(__fadd2_rn(make_float2(v.x, v.y), f2(-m))));
-      fx_add2(acc, canon_exp2(__fadd2_rn(make_float2(v.z, v.w), f2(-m))));
+      fx_add2(acc, canon_exp2(__fmul2_rn(__fadd2_rn(make_float2(v.x, v.y), f2(-m)), tau2)));
+      fx_add2(acc, canon_exp2(__fmul2_rn(__fadd2_rn(make_float2(v.z, v.w), f2(-m)), tau2)));
       if ((++it & 63) == 0) acc.flush();  // 256 terms: A and B stay below 2^32
     }
     part = acc.total();
   } else {
     part = 0;
-    for (int j = threadIdx.x; j < V; j += kStatsThreads) part += fx(canon_exp(__fsub_rn(__ldg(row + j), m)));
+    for (int j = threadIdx.x; j < V; j += kStatsThreads)
+      part += fx(canon_exp(__fmul_rn(__fsub_rn(__ldg(row + j), m), tau)));
   }
   part = warp_sum_u64(part);
   if (lane == 0) ssum[w] = part;
@@ -581,7 +592,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
   int32_t* status = &a.status[b];
   int xk = 0;  // exchange counter
   const int st_in = *(volatile int32_t*)status;
-  const bool may_run = n >= 1 && n <= a.n_max && (st_in & ~(SPEC_DEV_BAD_TOKEN | SPEC_DEV_BAD_TREE)) == 0;
+  constexpr int kOwnBits = SPEC_DEV_BAD_TOKEN | SPEC_DEV_BAD_TREE | SPEC_DEV_BAD_TEMP;
+  const float tau = MODE == 1 ? request_tau(a, b) : 1.0f;
+  const bool may_run = n >= 1 && n <= a.n_max && (st_in & ~kOwnBits) == 0 && tau_ok(tau);
 
   // stochastic: the root's target slice is copied while the inputs are checked
   float* D = reinterpret_cast<float*>(dyn_smem);  // current weights of this CTA's slice
@@ -604,12 +617,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
   // are checked.
   if constexpr (C > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
-  // The tree and token checks are made by every CTA from the inputs; the only
-  // status bits this kernel sets are those checks' (by rank 0, when every CTA
-  // of the cluster skips the walk), so ignoring them in the incoming status
-  // keeps the decision uniform.
+  // The tree, token and temperature checks are made by every CTA from the
+  // inputs; the only status bits this kernel sets are those checks' (by rank
+  // 0, when every CTA of the cluster skips the walk), so ignoring them in the
+  // incoming status keeps the decision uniform.
   int bad = 0;
-  bool skip = (st_in & ~(SPEC_DEV_BAD_TOKEN | SPEC_DEV_BAD_TREE)) != 0;
+  bool skip = (st_in & ~kOwnBits) != 0;
   if (!skip) {
     const int nc = min(max(n, 0), a.n_max);  // nodes whose entries are checked
     bool bt = false, bp = n < 0 || n > a.n_max;
@@ -620,7 +633,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
       bt |= (unsigned)t >= (unsigned)V;
       bp |= i == 0 ? p != -1 : (p < 0 || p >= i);
     }
-    bad = (__syncthreads_or(bt) ? SPEC_DEV_BAD_TOKEN : 0) | (__syncthreads_or(bp) ? SPEC_DEV_BAD_TREE : 0);
+    bad = (__syncthreads_or(bt) ? SPEC_DEV_BAD_TOKEN : 0) | (__syncthreads_or(bp) ? SPEC_DEV_BAD_TREE : 0) |
+          (tau_ok(tau) ? 0 : SPEC_DEV_BAD_TEMP);
     skip = bad != 0 || n == 0;
   }
   if constexpr (C > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -751,6 +765,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
     float4* D4 = reinterpret_cast<float4*>(D);
     const int len4 = len >> 2;
     const bool use_stats = a.stats != nullptr;
+    const bool per_child = a.q_per_child != 0;
+    // the draft slice is copied on demand (at a rejection, into buffer 0)
+    // with row statistics or per-child rows; otherwise at node entry
+    const bool q_lazy = use_stats || per_child;
+    const float2 tau2 = f2(tau);
     bool loaded = true;  // D holds the current node's slice (the root's copy is in flight)
     // statistics mode: every node's entries, read once at the start (the
     // second draft buffer's room holds them): its logit and draft
@@ -765,7 +784,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
       for (int c = threadIdx.x; c < n; c += kWalkThreads) {
         const int pc = sh.par[c], t = sh.tok[c];
         NX[c] = c > 0 ? __ldcg(a.p_logits + (size_t)(off + pc) * V + t) : 0.0f;
-        NQ[c] = c > 0 ? __ldcg(a.q_probs + (size_t)(off + pc) * V + t) : 0.0f;
+        NQ[c] = c > 0 ? __ldcg(a.q_probs + (size_t)(off + (per_child ? c : pc)) * V + t) : 0.0f;
         NU[c] = a.uniforms[off + c].x;
         const RowStats r = a.stats[off + c];
         NM[c] = r.m;
@@ -800,14 +819,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
       float rx[2], rq[2];
       uint32_t ru[2];
       uint32_t uterm = 0;
-      // the draft slice: without statistics, into the buffer of this node's
-      // parity at once (its previous copy, two nodes back, was waited for here
-      // or at a rejection); with statistics, into buffer 0 at the node's first
-      // rejection
-      const int qb = use_stats ? 0 : (L - 1) & 1;
+      // the draft slice: per parent without statistics, into the buffer of
+      // this node's parity at once (its previous copy, two nodes back, was
+      // waited for here or at a rejection); otherwise into buffer 0 at each
+      // rejection that needs a row the buffer does not hold
+      const int qb = q_lazy ? 0 : (L - 1) & 1;
       float* Q = Qb + qb * a.slice;
       const float4* Q4 = reinterpret_cast<const float4*>(Q);
-      bool q_ready = !use_stats;
+      int q_row = q_lazy ? -1 : u;  // the row the draft buffer holds (or is receiving)
       if (!use_stats) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -816,16 +835,18 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
             const int c = sh.s.kids[i];
             const int t = sh.tok[c];
             rx[r] = __ldcg(prow + t);
-            rq[r] = __ldcg(qrow + t);
+            rq[r] = __ldcg((per_child ? a.q_probs + (size_t)(off + c) * V : qrow) + t);
             ru[r] = a.uniforms[off + c].x;
             if (vec) prefetch_l2(a.p_logits + (size_t)(off + c) * V + x0, (uint32_t)len * 4);
           }
         }
         if (threadIdx.x == 0) uterm = a.uniforms[off + u].y;
-        if (qpend & (1u << qb)) wait_draft(sh, qb, qphase, qpend, status);
-        if (k > 0 && vec && len > 0) {
-          if (threadIdx.x == 0) start_copy(Q, qrow + x0, (uint32_t)len * 4, &sh.qbar[qb]);
-          qpend |= 1u << qb;
+        if (!q_lazy) {
+          if (qpend & (1u << qb)) wait_draft(sh, qb, qphase, qpend, status);
+          if (k > 0 && vec && len > 0) {
+            if (threadIdx.x == 0) start_copy(Q, qrow + x0, (uint32_t)len * 4, &sh.qbar[qb]);
+            qpend |= 1u << qb;
+          }
         }
       }
 
@@ -862,8 +883,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           FxSum acc;
           for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
             const float4 v = D4[j];
-            const float2 lo = canon_exp2(__fadd2_rn(make_float2(v.x, v.y), f2(-m)));
-            const float2 hi = canon_exp2(__fadd2_rn(make_float2(v.z, v.w), f2(-m)));
+            const float2 lo = canon_exp2(__fmul2_rn(__fadd2_rn(make_float2(v.x, v.y), f2(-m)), tau2));
+            const float2 hi = canon_exp2(__fmul2_rn(__fadd2_rn(make_float2(v.z, v.w), f2(-m)), tau2));
             D4[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
             fx_add2(acc, lo);
             fx_add2(acc, hi);
@@ -872,7 +893,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         } else {
           mp = 0;
           for (int j = threadIdx.x; j < len; j += kWalkThreads) {
-            const float e = canon_exp(__fsub_rn(D[j], m));
+            const float e = canon_exp(__fmul_rn(__fsub_rn(D[j], m), tau));
             D[j] = e;
             mp += fx(e);
           }
@@ -902,8 +923,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           FxSum acc;
           for (int j = threadIdx.x; j < len4; j += kWalkThreads) {
             const float4 v = D4[j];
-            const float2 lo = canon_exp2(__fadd2_rn(make_float2(v.x, v.y), f2(-m)));
-            const float2 hi = canon_exp2(__fadd2_rn(make_float2(v.z, v.w), f2(-m)));
+            const float2 lo = canon_exp2(__fmul2_rn(__fadd2_rn(make_float2(v.x, v.y), f2(-m)), tau2));
+            const float2 hi = canon_exp2(__fmul2_rn(__fadd2_rn(make_float2(v.z, v.w), f2(-m)), tau2));
             D4[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
             fx_add2(acc, lo);
             fx_add2(acc, hi);
@@ -912,7 +933,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         } else {
           mp = 0;
           for (int j = threadIdx.x; j < len; j += kWalkThreads) {
-            const float e = canon_exp(__fsub_rn(D[j], m));
+            const float e = canon_exp(__fmul_rn(__fsub_rn(D[j], m), tau));
             D[j] = e;
             mp += fx(e);
           }
@@ -929,8 +950,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         const int c = sh.s.kids[i];
         // r_j(t) from this node's logit and draft probability at t: the same
         // operations the slice passes apply to entry t
-        float d = canon_exp(__fsub_rn(sh.s.cx[i], m));
-        for (int s = 0; s < nsteps; ++s) d = resid(d, sh.s.z[s], sh.s.cq[i]);
+        float d = canon_exp(__fmul_rn(__fsub_rn(sh.s.cx[i], m), tau));
+        if (per_child) {  // step s subtracted rejected sibling s's own row
+          const int t = sh.tok[c];
+          for (int s = 0; s < nsteps; ++s)
+            d = resid(d, sh.s.z[s], __ldg(a.q_probs + (size_t)(off + sh.s.kids[s]) * V + t));
+        } else {
+          for (int s = 0; s < nsteps; ++s) d = resid(d, sh.s.z[s], sh.s.cq[i]);
+        }
         const float rt = __fdiv_rn(d, Z);
         const float ua = __fmul_rn((float)(sh.s.cu[i] >> 8), 0x1p-24f);
         if (__fmul_rn(ua, sh.s.cq[i]) <= rt) {
@@ -938,13 +965,20 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           break;
         }
         if (frozen) continue;  // the next residual would be the same all-zero one
-        if (!q_ready) {  // statistics mode: this node's draft slice, on its first rejection,
-          if (vec && len > 0) {  // in flight while the weights are made
-            if (threadIdx.x == 0) start_copy(Q, qrow + x0, (uint32_t)len * 4, &sh.qbar[0]);
+        const int need = per_child ? c : u;  // the draft row this rejection subtracts
+        if (q_row != need) {  // copied on demand, in flight while the weights are made
+          if (vec && len > 0) {
+            if (q_row >= 0) {  // the previous row's readers are done before the copy overwrites it
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              __syncthreads();
+            }
+            if (threadIdx.x == 0)
+              start_copy(Q, a.q_probs + (size_t)(off + need) * V + x0, (uint32_t)len * 4, &sh.qbar[0]);
             qpend |= 1u;
           }
-          q_ready = true;
+          q_row = need;
         }
+        const float* qsrc = a.q_probs + (size_t)(off + need) * V;
         ensure_e();
         if (qpend & (1u << qb)) wait_draft(sh, qb, qphase, qpend, status);
         if (threadIdx.x == 0) sh.s.z[nsteps] = Z;  // read only after the exchange below
@@ -965,7 +999,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         } else {
           np = 0;
           for (int j = threadIdx.x; j < len; j += kWalkThreads) {
-            const float dn = resid(D[j], Z, __ldg(qrow + x0 + j));
+            const float dn = resid(D[j], Z, __ldg(qsrc + x0 + j));
             D[j] = dn;
             np += fx(dn);
           }
@@ -984,9 +1018,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           // Rebuild step j-1 from the logits: e, then the nsteps earlier steps.
           frozen = true;
           for (int j = threadIdx.x; j < len; j += kWalkThreads) {
-            float e = canon_exp(__fsub_rn(__ldg(prow + x0 + j), m));
-            const float q = vec ? Q[j] : __ldg(qrow + x0 + j);
-            for (int s = 0; s < nsteps; ++s) e = resid(e, sh.s.z[s], q);
+            float e = canon_exp(__fmul_rn(__fsub_rn(__ldg(prow + x0 + j), m), tau));
+            for (int s = 0; s < nsteps; ++s) {
+              const float q = per_child ? __ldg(a.q_probs + (size_t)(off + sh.s.kids[s]) * V + x0 + j)
+                                        : (vec ? Q[j] : __ldg(qrow + x0 + j));
+              e = resid(e, sh.s.z[s], q);
+            }
             D[j] = e;
           }
           __syncthreads();
@@ -1247,11 +1284,12 @@ spec_status spec_tree_verify_greedy(const float* p_logits, const int32_t* tokens
 
 spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_probs, const int32_t* tokens,
                                         const int32_t* parent, const int32_t* tree_off, const uint32_t* uniforms,
-                                        int B, int n_max, int V, int32_t* path, int32_t* accept_len,
-                                        int32_t* emitted, int32_t* n_emitted, void* workspace,
-                                        size_t workspace_bytes, int32_t* status, void* stream) {
+                                        const float* inv_temperature, int q_layout, int B, int n_max, int V,
+                                        int32_t* path, int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
+                                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
   spec_status s = verify_check(B, n_max, V);
   if (s != SPEC_OK) return s;
+  if (q_layout != SPEC_Q_PER_PARENT && q_layout != SPEC_Q_PER_CHILD) return SPEC_ERR_INVALID_ARG;
   if (B == 0 || n_max == 0) return SPEC_OK;
   if (!p_logits || !q_probs || !tokens || !parent || !tree_off || !uniforms || !path || !accept_len || !emitted ||
       !n_emitted || !status)
@@ -1263,6 +1301,8 @@ spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_pr
   a.parent = parent;
   a.tree_off = tree_off;
   a.uniforms = reinterpret_cast<const uint2*>(uniforms);
+  a.inv_temp = inv_temperature;
+  a.q_per_child = q_layout == SPEC_Q_PER_CHILD;
   a.n_max = n_max;
   a.V = V;
   a.path = path;

@@ -56,6 +56,12 @@ class DeviceBatch:
 
 
 class VerifyPass:
+    # stochastic verification options used when verify() is not given them:
+    # per-request inverse temperatures (float32 device tensor [B], or None for
+    # 1) and the draft-row layout
+    inv_temp = None
+    q_layout = S.SPEC_Q_PER_PARENT
+
     def __init__(self, batch: DeviceBatch):
         b = batch
         dev = b.q.device
@@ -86,15 +92,17 @@ class VerifyPass:
                               b.prefix_len, b.tree_off, self.mask, b.B, b.T, b.n_max, b.max_prefix, b.Hq, b.Hkv, b.D,
                               b.scale, self.out, self.attn_ws, self.status, flags, stream)
 
-    def verify(self, mode="stochastic", stream=None):
+    def verify(self, mode="stochastic", stream=None, inv_temp=None, q_layout=None):
         b = self.batch
+        inv_temp = self.inv_temp if inv_temp is None else inv_temp
+        q_layout = self.q_layout if q_layout is None else q_layout
         if mode == "greedy":
             S.spec_tree_verify_greedy(b.p_logits, b.tokens, b.parent, b.tree_off, b.B, b.n_max, b.V, self.path, self.accept_len, self.emitted, self.n_emitted,
                                       self.verify_ws, self.status, stream)
         else:
             S.spec_tree_verify_stochastic(b.p_logits, b.q_probs, b.tokens, b.parent, b.tree_off, b.uniforms, b.B,
                                           b.n_max, b.V, self.path, self.accept_len, self.emitted, self.n_emitted,
-                                          self.verify_ws, self.status, stream)
+                                          self.verify_ws, self.status, stream, inv_temp=inv_temp, q_layout=q_layout)
 
     def commit(self, stream=None):
         b = self.batch
