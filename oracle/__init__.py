@@ -17,6 +17,9 @@ What each function follows (page title, section):
                          "Misconception" section and its traced example)
   * kv_commit         -- SpecInfer guide, "Depth-First Flattening and KV Cache
                          Reuse" and "PagedKV Allocation with Zero-Copy Pruning"
+  * tree_expand_level / tree_expand -- SpecInfer guide, "Method A:
+                         Expansion-Based Tree Construction"
+  * tree_merge        -- same page, "Method B: Merge-Based Tree Construction"
   * philox_uniforms   -- Philox4x32-10 (Salmon et al., SC'11)
 
 Pins (in tests/test_oracle_pins.py, all ``-m "not gpu"``):
@@ -41,6 +44,12 @@ Pins (in tests/test_oracle_pins.py, all ``-m "not gpu"``):
   * canonical exp: <= 2 ulp from libm's fp64 exp;
   * FX sums: equal to exact integer sums;
   * commit: invariants against a snapshot gather;
+  * expansion: the page's schedule <3, 2, 1, 1> gives levels of 3, 6, 6, 6
+    nodes; children are the top-k of their row in numpy's lexicographic
+    order (value, then token id; NaN last), level by level;
+  * merge: brute force over the page's condition: every prefix of every
+    sequence is one node with that token path, no two nodes share a path,
+    first-appearance numbering; chains and identical drafts;
   * Philox: equal to the Philox4x32-10 engine shipped in PyTorch's headers.
 """
 import ctypes
@@ -70,6 +79,8 @@ def lib():
         L.oracle_verify_stochastic.argtypes = [P, P, P, P, P, P, i32, i32, i32, P, i32, P, P, P, P, P]
         L.oracle_kv_commit.argtypes = [P, P, i64, P, i32, i32, i32, P, P, i32, P, i32, i32, i32, i32, P, P]
         L.oracle_kv_release.argtypes = [P, i32, i32, P, P, P, P, i32, P, i32, P]
+        L.oracle_tree_expand_level.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P]
+        L.oracle_tree_merge.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P]
         L.oracle_philox4x32_10.argtypes = [P, P, P]
         L.oracle_philox_uniforms.argtypes = [u64, u32, P, i32, P]
         L.oracle_canon_exp.argtypes = [ctypes.c_float]
@@ -200,6 +211,55 @@ def kv_commit_layers(k_caches, v_caches, block_table, block_size, prefix_len, tr
         new_len, st = nl, s2
     bt, pool, cnt, st = kv_release(block_table, block_size, prefix_len, tree_off, new_len, st, free_cap, free_count)
     return ks, vs, new_len, st, bt, pool, cnt
+
+
+def tree_expand_level(scores, F, k, level_start, parent, tokens, n_total):
+    """Appends level level_start + F .. of every request (see oracle.c);
+    parent/tokens are [B * n_total] int32 arrays, updated in place."""
+    scores = _c(scores, np.float32)
+    V = scores.shape[-1]
+    B = scores.size // (F * V) if F > 0 else 0
+    assert parent.dtype == np.int32 and tokens.dtype == np.int32
+    rc = lib().oracle_tree_expand_level(_p(scores), B, F, V, k, level_start, n_total, _p(parent), _p(tokens))
+    assert rc == 0
+    return parent, tokens
+
+
+def tree_expand(root_tokens, level_scores, schedule, V):
+    """A whole expansion tree: level_scores(level, frontier_node_ids) gives the
+    [B * F, V] score rows of that level's frontier.  Returns (parent, tokens,
+    tree_off) packed, each request's tree 1 + k1 + k1 k2 + ... nodes."""
+    B = len(root_tokens)
+    sizes = [1]
+    for k in schedule:
+        sizes.append(sizes[-1] * k)
+    n_total = sum(sizes)
+    parent = np.full(B * n_total, -1, np.int32)
+    tokens = np.zeros(B * n_total, np.int32)
+    tokens[::n_total] = root_tokens
+    start = 0
+    for lev, k in enumerate(schedule):
+        F = sizes[lev]
+        tree_expand_level(level_scores(lev, np.arange(start, start + F)), F, k, start, parent, tokens, n_total)
+        start += F
+    return parent, tokens, np.arange(0, B * n_total + 1, n_total, dtype=np.int32)
+
+
+def tree_merge(seqs, lens, root_tok, V):
+    """seqs [B, M, m] int32, lens [B, M], root_tok [B].  Returns dict of
+    tree_off, parent, tokens, src (packed, trimmed to tree_off[-1]), node_of
+    [B, M, m] and status [B]."""
+    seqs, lens, root_tok = _c(seqs, np.int32), _c(lens, np.int32), _c(root_tok, np.int32)
+    B, M, m = seqs.shape
+    cap = B * (1 + M * m)
+    tree_off = np.zeros(B + 1, np.int32)
+    parent, tokens, src = np.zeros(cap, np.int32), np.zeros(cap, np.int32), np.zeros(cap, np.int32)
+    node_of, status = np.zeros((B, M, m), np.int32), np.zeros(B, np.int32)
+    lib().oracle_tree_merge(_p(seqs), _p(lens), _p(root_tok), B, M, m, V, _p(tree_off), _p(parent), _p(tokens),
+                            _p(src), _p(node_of), _p(status))
+    T = int(tree_off[-1])
+    return dict(tree_off=tree_off, parent=parent[:T], tokens=tokens[:T], src=src[:T], node_of=node_of,
+                status=status)
 
 
 def philox4x32_10(ctr, key):

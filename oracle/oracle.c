@@ -695,6 +695,116 @@ int oracle_kv_release(int32_t *block_table, int max_blocks, int block_size, cons
 }
 
 /* ------------------------------------------------------------------ */
+/* Tree construction                                                   */
+/* ------------------------------------------------------------------ */
+
+/* Rank order of draft scores: a before b iff a's value is larger, or equal
+ * with the lower token id.  NaN ranks below every number; -0 equals +0. */
+static int score_before(float va, int ia, float vb, int ib)
+{
+    int na = isnan(va), nb = isnan(vb);
+    if (na != nb) return nb;
+    if (!na && va != vb) return va > vb;
+    return ia < ib;
+}
+
+/* One level of expansion ([SpecInfer guide] "Method A: Expansion-Based Tree
+ * Construction": level i expands the top-k_i tokens of every node of level
+ * i-1).  Each of the B requests has the same shape: its tree occupies
+ * n_total slots from b * n_total; the F frontier nodes are level_start ..
+ * level_start + F - 1; frontier node i's draft scores (logits or
+ * probabilities: the top-k is the same) are row b * F + i of `scores`.
+ * Children are appended after the frontier, frontier node by frontier
+ * node, each node's k children in rank order: child r of frontier node i
+ * is node level_start + F + i * k + r.  Selection is k passes, each taking
+ * the best-ranked token not yet taken. */
+int oracle_tree_expand_level(const float *scores, int B, int F, int V, int k, int level_start, int n_total,
+                             int32_t *parent, int32_t *tokens)
+{
+    if (k < 0 || k > V || level_start + F + F * k > n_total) return -1;
+    char *taken = (char *)malloc((size_t)V);
+    for (int b = 0; b < B; b++)
+        for (int i = 0; i < F; i++) {
+            const float *row = scores + ((size_t)b * F + i) * V;
+            memset(taken, 0, (size_t)V);
+            for (int r = 0; r < k; r++) {
+                int best = -1;
+                for (int x = 0; x < V; x++)
+                    if (!taken[x] && (best < 0 || score_before(row[x], x, row[best], best))) best = x;
+                taken[best] = 1;
+                size_t c = (size_t)b * n_total + level_start + F + (size_t)i * k + r;
+                parent[c] = level_start + i;
+                tokens[c] = best;
+            }
+        }
+    free(taken);
+    return 0;
+}
+
+/* Merge ([SpecInfer guide] "Method B: Merge-Based Tree Construction"):
+ * request b's M candidate sequences (sequence s: seqs[b][s][0 .. lens[b][s]-1],
+ * row stride m) are united into one token tree in which every prefix of
+ * every sequence is a node and no two nodes share a token path (for all u
+ * in N_s there is v in the merged tree with S_v = S_u; identical prefixes
+ * are one node).  Node 0 is the root (root_tok[b], parent -1).  Nodes are
+ * numbered in insertion order: sequences in order, each from its first
+ * token on, a prefix getting the next index when no earlier sequence has
+ * it.  Output is packed: request b's nodes at tree_off[b] .. tree_off[b+1]-1
+ * (tree_off written, tree_off[0] = 0); node_of[b][s][j] = the node of prefix
+ * (s, j) (-1 past the sequence's length); src[node] = s * m + j of the
+ * prefix that created it (-1 for roots).  A length outside [0, m] sets
+ * ORC_BAD_TREE, a token outside [0, V) ORC_BAD_TOKEN; such a request gets
+ * only its root.  Arrays parent/tokens/src hold B * (1 + M * m) entries. */
+int oracle_tree_merge(const int32_t *seqs, const int32_t *lens, const int32_t *root_tok, int B, int M, int m, int V,
+                      int32_t *tree_off, int32_t *parent, int32_t *tokens, int32_t *src, int32_t *node_of,
+                      int32_t *status)
+{
+    tree_off[0] = 0;
+    for (int b = 0; b < B; b++) {
+        const int32_t *S = seqs + (size_t)b * M * m;
+        const int32_t *len = lens + (size_t)b * M;
+        int32_t *no = node_of + (size_t)b * M * m;
+        int st = 0;
+        for (int s = 0; s < M; s++) {
+            if (len[s] < 0 || len[s] > m) st |= ORC_BAD_TREE;
+            else
+                for (int j = 0; j < len[s]; j++)
+                    if (S[(size_t)s * m + j] < 0 || S[(size_t)s * m + j] >= V) st |= ORC_BAD_TOKEN;
+        }
+        if (root_tok[b] < 0 || root_tok[b] >= V) st |= ORC_BAD_TOKEN;
+        status[b] = st;
+        int base = tree_off[b], n = 1;
+        parent[base] = -1;
+        tokens[base] = root_tok[b];
+        src[base] = -1;
+        for (int i = 0; i < M * m; i++) no[i] = -1;
+        if (st == 0) {
+            for (int s = 0; s < M; s++)
+                for (int j = 0; j < len[s]; j++) {
+                    int par = j == 0 ? 0 : no[(size_t)s * m + j - 1];
+                    int tok = S[(size_t)s * m + j];
+                    /* an existing child of par with this token is the same prefix */
+                    int found = -1;
+                    for (int v = 1; v < n; v++)
+                        if (parent[base + v] == par && tokens[base + v] == tok) {
+                            found = v;
+                            break;
+                        }
+                    if (found < 0) {
+                        found = n++;
+                        parent[base + found] = par;
+                        tokens[base + found] = tok;
+                        src[base + found] = s * m + j;
+                    }
+                    no[(size_t)s * m + j] = found;
+                }
+        }
+        tree_off[b + 1] = base + n;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* Philox4x32-10 uniforms                                              */
 /* ------------------------------------------------------------------ */
 

@@ -862,6 +862,130 @@ int main() {
 """
 
 
+# ----------------------------------------------------- tree construction ----
+
+def _rank_order(row):
+    """Tokens of a score row best first: larger value, then lower id; NaN last; -0 == +0."""
+    r = np.asarray(row, np.float64) + 0.0  # -0 -> +0
+    nan = np.isnan(r)
+    return np.lexsort((np.arange(len(r)), -np.where(nan, 0, r), nan))
+
+
+def _depths(parent, lo, hi):
+    d = []
+    for u in range(hi - lo):
+        c, k = u, 0
+        while parent[lo + c] != -1:
+            c = parent[lo + c]
+            k += 1
+        d.append(k)
+    return np.array(d)
+
+
+def test_expansion_of_the_printed_schedule(oracle):
+    """"Method A": schedule <3, 2, 1, 1> gives 3 nodes at depth 1, 6 at depth 2
+    and 6 at depths 3 and 4; every node's children are the top-k of its row
+    in rank order, appended level by level (parents before children)."""
+    rng = np.random.default_rng(31)
+    B, V, sched = 3, 50, [3, 2, 1, 1]
+    rows = {}
+
+    def level_scores(lev, ids):
+        out = rng.standard_normal((B * len(ids), V)).astype(np.float32)
+        out[:, 7] = out[:, 8]  # ties between tokens 7 and 8
+        for b in range(B):
+            for i, u in enumerate(ids):
+                rows[(b, int(u))] = out[b * len(ids) + i]
+        return out
+
+    parent, tokens, tree_off = oracle.tree_expand(np.array([4, 5, 6]), level_scores, sched, V)
+    n = 1 + 3 + 6 + 6 + 6
+    assert tree_off.tolist() == [0, n, 2 * n, 3 * n]
+    for b in range(B):
+        lo = b * n
+        par = parent[lo:lo + n]
+        assert par[0] == -1 and all(0 <= par[u] < u for u in range(1, n))
+        assert np.bincount(_depths(parent, lo, lo + n)).tolist() == [1, 3, 6, 6, 6]
+        assert tokens[lo] == [4, 5, 6][b]
+        for u in range(n):
+            kids = [c for c in range(1, n) if par[c] == u]
+            if not kids:
+                continue
+            want = _rank_order(rows[(b, u)])[:len(kids)]
+            assert [tokens[lo + c] for c in kids] == want.tolist()
+            assert kids == list(range(kids[0], kids[0] + len(kids)))
+
+
+def test_expansion_rank_order_ties_nan_and_signed_zero(oracle):
+    V = 9
+    row = np.array([0.5, np.nan, 0.5, -0.0, 0.0, np.inf, -np.inf, 0.5, np.nan], np.float32)
+    parent = np.full(1 + V, -1, np.int32)
+    tokens = np.zeros(1 + V, np.int32)
+    oracle.tree_expand_level(row[None], 1, V, 0, parent, tokens, 1 + V)
+    assert tokens[1:].tolist() == [5, 0, 2, 7, 3, 4, 6, 1, 8]
+    assert tokens[1:].tolist() == _rank_order(row).tolist()
+    # random rows with many ties against the numpy order
+    rng = np.random.default_rng(3)
+    rows = rng.integers(0, 5, (40, 300)).astype(np.float32)
+    rows[rng.random(rows.shape) < 0.05] = np.nan
+    parent = np.full(40 * 8, -1, np.int32)
+    tokens = np.zeros(40 * 8, np.int32)
+    oracle.tree_expand_level(rows, 1, 7, 0, parent, tokens, 8)
+    for b in range(40):
+        assert tokens[b * 8 + 1:b * 8 + 8].tolist() == _rank_order(rows[b])[:7].tolist()
+        assert parent[b * 8 + 1:b * 8 + 8].tolist() == [0] * 7
+
+
+def _root_path_tokens(parent, tokens, lo, u):
+    out = []
+    while parent[lo + u] != -1:
+        out.append(int(tokens[lo + u]))
+        u = parent[lo + u]
+    return tuple(out[::-1])
+
+
+def test_merge_is_the_union_of_prefixes(oracle):
+    """"Method B": every prefix of every candidate sequence is exactly one
+    node whose token path is that prefix (S_v = S_u), no two nodes share a
+    path, and nodes are numbered in first-appearance order."""
+    rng = np.random.default_rng(17)
+    B, M, m, V = 6, 5, 7, 3  # a small vocabulary: many shared prefixes
+    seqs = rng.integers(0, V, (B, M, m)).astype(np.int32)
+    seqs[:, 3] = seqs[:, 1]  # an identical sequence
+    lens = rng.integers(0, m + 1, (B, M)).astype(np.int32)
+    r = oracle.tree_merge(seqs, lens, np.arange(B) % V, V)
+    assert (r["status"] == 0).all()
+    for b in range(B):
+        lo, hi = r["tree_off"][b], r["tree_off"][b + 1]
+        par = r["parent"][lo:hi]
+        assert par[0] == -1 and all(0 <= par[u] < u for u in range(1, hi - lo))
+        paths = [_root_path_tokens(r["parent"], r["tokens"], lo, u) for u in range(hi - lo)]
+        assert len(set(paths)) == len(paths)  # no duplicate token paths
+        order = []
+        for s in range(M):
+            for j in range(lens[b, s]):
+                pre = tuple(seqs[b, s, :j + 1].tolist())
+                assert paths[r["node_of"][b, s, j]] == pre
+                if pre not in order:
+                    order.append(pre)
+            assert (r["node_of"][b, s, lens[b, s]:] == -1).all()
+        assert paths[1:] == order  # insertion order, and nothing else
+        for u in range(1, hi - lo):
+            s, j = divmod(int(r["src"][lo + u]), m)
+            assert tuple(seqs[b, s, :j + 1].tolist()) == paths[u]
+
+
+def test_merge_special_cases_and_bad_inputs(oracle):
+    seq = np.array([[[1, 2, 3, 4]]], np.int32)
+    r = oracle.tree_merge(seq, [[4]], [0], 10)  # one sequence: a chain
+    assert r["parent"].tolist() == [-1, 0, 1, 2, 3] and r["tokens"].tolist() == [0, 1, 2, 3, 4]
+    r = oracle.tree_merge(np.repeat(seq, 3, 1), [[4, 4, 4]], [0], 10)  # identical drafts: still one chain
+    assert r["parent"].tolist() == [-1, 0, 1, 2, 3]
+    r = oracle.tree_merge(np.repeat(seq, 3, 0), [[5], [4], [4]], [0, 0, 12], 10)
+    assert r["status"].tolist() == [oracle.ST_BAD_TREE, 0, oracle.ST_BAD_TOKEN]
+    assert r["tree_off"].tolist() == [0, 1, 6, 7] and (r["node_of"][0] == -1).all()
+
+
 def test_philox_matches_pytorch_engine(oracle):
     """Philox4x32-10 against the independent engine in PyTorch's public
     headers (ATen/core/PhiloxRNGEngine.h): key = seed, counter = (offset lo,
