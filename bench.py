@@ -441,6 +441,8 @@ def bench_gpu(args):
             "kernels": kernels}
     if args.commit_layers > 0:
         line["commit_layers"] = measure_commit_layers(args.commit_layers, passes[0], dev)
+    if args.tree_build:
+        line["tree_build"] = measure_tree_build(dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, _ = run_cpu_baseline(works[0], args.mode)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
@@ -604,6 +606,82 @@ def measure_commit_layers(L, vp, dev, reps=20, replays=5):
             "pages_released": released, "status_ok": ok}
 
 
+def measure_tree_build(dev, reps=20, replays=5):
+    """Device tree construction on the decode layer's shapes: the expansion
+    schedule <4,2,2,1,1,1,1,1> (8 requests, V = 32000, every level's draft rows
+    resident; three rotating row sets, 285 MB together, above L2), and the
+    merge of 32 candidate sequences of 8 tokens per request for 64 requests.
+    Each: one graph of `reps` builds, replayed `replays` times between CUDA
+    events; microseconds per build."""
+    import torch
+    import tree_speculative_verification_spec_gb300 as S
+    B, V, sched = 8, 32000, [4, 2, 2, 1, 1, 1, 1, 1]
+    sizes = [1]
+    for k in sched:
+        sizes.append(sizes[-1] * k)
+    n_total = sum(sizes)
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    sets = [[torch.randn((B * sizes[lev], V), generator=g, device=dev) for lev in range(len(sched))]
+            for _ in range(3)]
+    roots = torch.randint(0, V, (B,), generator=g, device=dev, dtype=torch.int32)
+    tree_off = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    par = torch.empty(B * n_total, dtype=torch.int32, device=dev)
+    tok = torch.empty(B * n_total, dtype=torch.int32, device=dev)
+
+    def expand(rows):
+        S.spec_tree_init(roots, B, n_total, tree_off, par, tok)
+        start = 0
+        for lev, k in enumerate(sched):
+            S.spec_tree_expand_level(rows[lev], B, sizes[lev], V, k, start, n_total, par, tok)
+            start += sizes[lev]
+
+    Bm, M, m = 64, 32, 8
+    seqs = torch.randint(0, 6, (Bm, M, m), generator=g, device=dev, dtype=torch.int32)  # shared prefixes
+    lens = torch.full((Bm, M), m, dtype=torch.int32, device=dev)
+    mroots = torch.zeros(Bm, dtype=torch.int32, device=dev)
+    cap = Bm * (1 + M * m)
+    moff = torch.empty(Bm + 1, dtype=torch.int32, device=dev)
+    mpar, mtok, msrc = (torch.empty(cap, dtype=torch.int32, device=dev) for _ in range(3))
+    mnode = torch.empty(Bm * M * m, dtype=torch.int32, device=dev)
+    mst = torch.empty(Bm, dtype=torch.int32, device=dev)
+
+    def merge():
+        S.spec_tree_merge(seqs, lens, mroots, Bm, M, m, 32000, moff, mpar, mtok, msrc, mnode, mst)
+
+    def time_us(fns):
+        cap_s = torch.cuda.Stream(dev)
+        for f in fns:
+            f()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap_s):
+            for r in range(reps):
+                fns[r % len(fns)]()
+        for _ in range(3):
+            gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream = torch.cuda.current_stream(dev)
+        a.record(stream)
+        for _ in range(replays):
+            gr.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * replays)
+
+    t_exp = time_us([lambda r=r: expand(r) for r in sets])
+    t_merge = time_us([merge])
+    rows_bytes = sum(B * sizes[lev] * V * 4 for lev in range(len(sched)))
+    peak, _ = _peaks()
+    gbs = rows_bytes / (t_exp * 1e-6) / 1e9
+    return {"expansion": {"schedule": sched, "requests": B, "V": V, "nodes_per_tree": n_total,
+                          "us_per_build": t_exp, "launches": 1 + len(sched), "row_bytes": rows_bytes,
+                          "gbs": gbs, "frac_hbm": gbs / peak},
+            "merge": {"requests": Bm, "sequences": M, "tokens_per_sequence": m, "us_per_build": t_merge,
+                      "launches": 3, "nodes": int(moff[-1].item())}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -618,6 +696,7 @@ def main():
                     help="stochastic verification at this temperature for every request (default: none, T = 1)")
     ap.add_argument("--q-per-child", action="store_true",
                     help="read the draft rows per child (merged trees) instead of per parent")
+    ap.add_argument("--tree-build", action="store_true", help="also time device tree construction")
     ap.add_argument("--commit-layers", type=int, default=0,
                     help="also time the commit of this many layers' caches in one launch (0: off)")
     args = ap.parse_args()

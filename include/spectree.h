@@ -305,6 +305,62 @@ spec_status spec_philox_uniforms(uint64_t seed, uint32_t round, const int32_t* t
                                  uint32_t* out, void* stream);
 
 /*
+ * Token-tree construction ("SpecInfer Guide", "Token Tree Construction:
+ * Expansion vs. Merge").  The trees come out in the layout the calls above
+ * take (parent before child, packed by tree_off).
+ *
+ * spec_tree_init: request b's tree occupies n_total slots from b * n_total;
+ * node 0 gets parent -1 and token root_tok[b] (the last verified token), and
+ * tree_off[b] = b * n_total for b = 0..B (tree_off may be NULL).
+ *   root_tok int32 [B]; tree_off int32 [B+1] out; parent, tokens int32 [B * n_total] out.
+ *   n_total in [1, 1024].
+ *
+ * spec_tree_expand_level: one level of "Method A: Expansion-Based Tree
+ * Construction": every frontier node gets its top-k tokens as children.
+ * Every request has the same shape; its F frontier nodes are level_start ..
+ * level_start + F - 1 and their children are appended after them, frontier
+ * node by frontier node, each node's k children in rank order: child r of
+ * frontier node i is node level_start + F + i * k + r, with parent
+ * level_start + i.  Rank order: larger score first, equal scores by lower
+ * token id, NaN after every number, -0 equal to +0.  A whole schedule
+ * <k_1, ..., k_m> is spec_tree_init, then one call per level (level_start
+ * 0, 1, 1 + k_1, ...), with the draft model's rows for the new frontier in
+ * between.
+ *   scores   float [B * F][V]  row b * F + i: draft scores (logits or probabilities)
+ *                              of frontier node i of request b
+ *   parent, tokens  int32 [B * n_total]  in/out: the level's children are written
+ *   k in [0, 32], k <= V; level_start + F + F * k <= n_total <= 1024, else an error
+ *   code and nothing is launched.
+ *
+ * spec_tree_merge: "Method B: Merge-Based Tree Construction": request b's
+ * M candidate sequences (one per draft model: sequence s is
+ * seqs[b][s][0 .. lens[b][s]-1]) are united into one tree in which every
+ * prefix of every sequence is one node and no two nodes share a token path.
+ * Node 0 is the root (root_tok[b]); the others are numbered in
+ * first-appearance order (sequences in order, each from its first token).
+ * The output is packed: tree_off is written (tree_off[0] = 0), request b's
+ * nodes are tree_off[b] .. tree_off[b+1]-1.
+ *   seqs     int32 [B][M][m]   candidate tokens (entries past a length are ignored)
+ *   lens     int32 [B][M]      sequence lengths in [0, m]
+ *   tree_off int32 [B+1] out
+ *   parent, tokens int32 [B * (1 + M * m)] out (capacity; tree_off[B] entries written)
+ *   src      int32 [same]  out: s * m + j of the prefix that created each node, -1 for roots
+ *   node_of  int32 [B][M][m] out: the node (request-local index) of prefix (s, j), -1 past
+ *                              the length; with it per-child draft rows can be gathered
+ *   status   int32 [B]     out: WRITTEN (a merge starts a pass): 0, SPEC_DEV_BAD_TREE (a
+ *                              length outside [0, m]) and/or SPEC_DEV_BAD_TOKEN (a token or
+ *                              root token outside [0, V)); such a request gets only its root.
+ *   M * m <= 1023 and M <= 1023.  Three launches (counts, offsets, nodes).
+ */
+spec_status spec_tree_init(const int32_t* root_tok, int B, int n_total, int32_t* tree_off, int32_t* parent,
+                           int32_t* tokens, void* stream);
+spec_status spec_tree_expand_level(const float* scores, int B, int F, int V, int k, int level_start, int n_total,
+                                   int32_t* parent, int32_t* tokens, void* stream);
+spec_status spec_tree_merge(const int32_t* seqs, const int32_t* lens, const int32_t* root_tok, int B, int M, int m,
+                            int V, int32_t* tree_off, int32_t* parent, int32_t* tokens, int32_t* src,
+                            int32_t* node_of, int32_t* status, void* stream);
+
+/*
  * Diagnostic of the bounded device waits (no counterpart on the pages): one
  * small kernel waits on a barrier that nothing ever completes, with a limit of
  * `polls` polls (1 .. 2^20), the same wait the tensor-core attention roles use

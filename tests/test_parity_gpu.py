@@ -348,6 +348,128 @@ def test_per_child_gpu_matches_oracle_on_monte_carlo_trees():
         assert np.array_equal(outs[1].cpu().numpy(), r["accept_len"])
 
 
+# ----------------------------------------------------- tree construction ----
+
+def _t(x, dtype=None):
+    return torch.from_numpy(np.ascontiguousarray(x if dtype is None else x.astype(dtype))).cuda()
+
+
+@pytest.mark.parametrize("B,F,V,k,kind", [(3, 1, 64, 4, "ints"), (5, 3, 1001, 3, "nan"), (2, 7, 32000, 8, "normal"),
+                                          (4, 2, 517, 17, "ints"), (1, 5, 4096, 32, "zeros"), (2, 4, 7, 7, "normal"),
+                                          (6, 2, 128256, 16, "normal"), (3, 3, 33, 1, "ints")])
+def test_expand_level_parity(B, F, V, k, kind):
+    """One expansion level: every child's parent and token equal the
+    oracle's (ties by token id, NaN last, -0 == +0), aligned and unaligned rows."""
+    g = np.random.default_rng(B * 100 + k)
+    if kind == "ints":
+        sc = g.integers(-3, 3, (B * F, V)).astype(np.float32)
+    elif kind == "zeros":
+        sc = np.where(g.random((B * F, V)) < 0.5, np.float32(-0.0), np.float32(0.0)).astype(np.float32)
+        sc[:, 100] = 1.0
+    else:
+        sc = g.standard_normal((B * F, V)).astype(np.float32)
+    if kind == "nan":
+        sc[g.random(sc.shape) < 0.3] = np.nan
+        sc[0, :] = np.nan
+    level_start = 1
+    n_total = level_start + F + F * k + 2
+    par = np.full(B * n_total, -5, np.int32)
+    tok = np.full(B * n_total, -5, np.int32)
+    O.tree_expand_level(sc, F, k, level_start, par, tok, n_total)
+    gp, gt = _t(np.full(B * n_total, -5, np.int32)), _t(np.full(B * n_total, -5, np.int32))
+    S.spec_tree_expand_level(_t(sc), B, F, V, k, level_start, n_total, gp, gt)
+    torch.cuda.synchronize()
+    assert gp.cpu().numpy().tolist() == par.tolist()
+    assert gt.cpu().numpy().tolist() == tok.tolist()
+
+
+def test_expansion_schedule_then_verify():
+    """The decode layer's schedule <4,2,2,1,1,1,1,1> (V = 32000, 8 requests)
+    built level by level on the device from per-level draft rows, equal to
+    the oracle's tree; the built trees then go through mask build and greedy
+    verification."""
+    B, V, sched = 8, 32000, [4, 2, 2, 1, 1, 1, 1, 1]
+    g = np.random.default_rng(77)
+    sizes = [1]
+    for k in sched:
+        sizes.append(sizes[-1] * k)
+    n_total = sum(sizes)
+    rows = [g.standard_normal((B * sizes[lev], V)).astype(np.float32) for lev in range(len(sched))]
+    roots = g.integers(0, V, B).astype(np.int32)
+    par_ref, tok_ref, off_ref = O.tree_expand(roots, lambda lev, ids: rows[lev], sched, V)
+    tree_off = torch.zeros(B + 1, dtype=torch.int32, device="cuda")
+    par = torch.full((B * n_total,), -9, dtype=torch.int32, device="cuda")
+    tok = torch.full((B * n_total,), -9, dtype=torch.int32, device="cuda")
+    S.spec_tree_init(_t(roots), B, n_total, tree_off, par, tok)
+    start = 0
+    for lev, k in enumerate(sched):
+        S.spec_tree_expand_level(_t(rows[lev]), B, sizes[lev], V, k, start, n_total, par, tok)
+        start += sizes[lev]
+    torch.cuda.synchronize()
+    assert tree_off.cpu().tolist() == off_ref.tolist()
+    assert par.cpu().numpy().tolist() == par_ref.tolist()
+    assert tok.cpu().numpy().tolist() == tok_ref.tolist()
+    # the built trees are valid input for the rest of the pass
+    w = W.small_random(78, B=B, n_range=(n_total, n_total), prefix_range=(0, 1), Hq=2, Hkv=1, D=64, V=V,
+                       block_size=16)
+    w.parent, w.tokens = torch.from_numpy(par_ref), torch.from_numpy(tok_ref)
+    got = _gpu_verify(w, "greedy")
+    ref = oracle_greedy(w)
+    _assert_verify_equal(got, ref, B)
+    assert (got["status"][:B] == 0).all()
+
+
+def _merge_gpu(seqs, lens, roots, V):
+    B, M, m = seqs.shape
+    cap = max(1, B * (1 + M * m))
+    out = dict(tree_off=torch.full((B + 1,), -3, dtype=torch.int32, device="cuda"),
+               parent=torch.full((cap,), -3, dtype=torch.int32, device="cuda"),
+               tokens=torch.full((cap,), -3, dtype=torch.int32, device="cuda"),
+               src=torch.full((cap,), -3, dtype=torch.int32, device="cuda"),
+               node_of=torch.full((max(1, B * M * m),), -3, dtype=torch.int32, device="cuda"),
+               status=torch.full((max(B, 1),), -3, dtype=torch.int32, device="cuda"))
+    S.spec_tree_merge(_t(seqs, np.int32) if seqs.size else None, _t(lens, np.int32) if lens.size else None,
+                      _t(roots, np.int32) if B else None, B, M, m, V, out["tree_off"], out["parent"],
+                      out["tokens"], out["src"], out["node_of"], out["status"])
+    torch.cuda.synchronize()
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    T = int(got["tree_off"][-1])
+    for k in ("parent", "tokens", "src"):
+        got[k] = got[k][:T]
+    got["node_of"] = got["node_of"][:B * M * m].reshape(B, M, m)
+    got["status"] = got["status"][:B]
+    return got
+
+
+@pytest.mark.parametrize("B,M,m,V", [(5, 4, 8, 3), (1500, 3, 5, 4), (7, 31, 33, 2), (2, 31, 33, 100000),
+                                     (3, 1, 9, 50), (4, 16, 1, 5), (2, 0, 4, 5), (0, 4, 4, 5)])
+def test_merge_parity(B, M, m, V):
+    """Merged trees equal the oracle's: offsets, parents, tokens, sources,
+    the prefix-to-node map and statuses (bad lengths and tokens included;
+    1500 requests take the offset scan over two rounds; 31 full sequences of
+    33 distinct tokens come close to the 1024-node limit)."""
+    g = np.random.default_rng(B + M + m)
+    seqs = g.integers(0, V, (B, M, m)).astype(np.int32)
+    lens = g.integers(0, m + 1, (B, M)).astype(np.int32)
+    if V >= 100000:
+        lens[:] = m
+    if B > 3 and M > 0:
+        lens[1, 0] = m + 1          # bad length
+        seqs[2, 0, 0] = V           # bad token (inside the length)
+        lens[2, 0] = max(lens[2, 0], 1)
+        seqs[3, M - 1, m - 1] = -1  # outside the length: ignored
+        lens[3, M - 1] = m - 1
+    if B > 0 and M > 1:
+        seqs[0, 1] = seqs[0, 0]     # an identical draft
+    roots = g.integers(0, V, B).astype(np.int32)
+    ref = O.tree_merge(seqs, lens, roots, V)
+    got = _merge_gpu(seqs, lens, roots, V)
+    for k in ("tree_off", "parent", "tokens", "src", "node_of", "status"):
+        assert np.array_equal(got[k], ref[k]), k
+    if B > 3 and M > 0:
+        assert ref["status"][1] == S.SPEC_DEV_BAD_TREE and ref["status"][2] == S.SPEC_DEV_BAD_TOKEN
+
+
 # ------------------------------------------------------------- attention ----
 
 def _gpu_attention(w, flags=S.SPEC_ATTN_AUTO, max_prefix=None):

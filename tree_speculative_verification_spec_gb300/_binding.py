@@ -33,6 +33,9 @@ SIGNATURES = {
                                      _P, _U32, _P], _I),
     "spec_verify_workspace_size": ([_I, _I, _I], _SZ),
     "spec_tree_verify_greedy": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
+    "spec_tree_init": ([_P, _I, _I, _P, _P, _P, _P], _I),
+    "spec_tree_expand_level": ([_P, _I, _I, _I, _I, _I, _I, _P, _P, _P], _I),
+    "spec_tree_merge": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "spec_tree_verify_stochastic": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "spec_kv_commit": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "spec_kv_commit_layers": ([_P, _P, _I, _P, _I, _I, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P],
@@ -154,6 +157,22 @@ def spec_tree_verify_stochastic(p_logits, q_probs, tokens, parent, tree_off, uni
         q_layout, B, n_max, V,
         _ptr(path), _ptr(accept_len), _ptr(emitted), _ptr(n_emitted), _ptr(workspace), ws_bytes, _ptr(status),
         _stream(stream)))
+
+
+def spec_tree_init(root_tok, B, n_total, tree_off, parent, tokens, stream=None):
+    _check("spec_tree_init", lib().spec_tree_init(_ptr(root_tok), B, n_total, _ptr(tree_off), _ptr(parent),
+                                                  _ptr(tokens), _stream(stream)))
+
+
+def spec_tree_expand_level(scores, B, F, V, k, level_start, n_total, parent, tokens, stream=None):
+    _check("spec_tree_expand_level", lib().spec_tree_expand_level(
+        _ptr(scores), B, F, V, k, level_start, n_total, _ptr(parent), _ptr(tokens), _stream(stream)))
+
+
+def spec_tree_merge(seqs, lens, root_tok, B, M, m, V, tree_off, parent, tokens, src, node_of, status, stream=None):
+    _check("spec_tree_merge", lib().spec_tree_merge(
+        _ptr(seqs), _ptr(lens), _ptr(root_tok), B, M, m, V, _ptr(tree_off), _ptr(parent), _ptr(tokens), _ptr(src),
+        _ptr(node_of), _ptr(status), _stream(stream)))
 
 
 def spec_kv_commit(k_cache, v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len, path, path_stride,
