@@ -21,6 +21,10 @@ What each function follows (page title, section):
                          Expansion-Based Tree Construction"
   * tree_merge        -- same page, "Method B: Merge-Based Tree Construction"
   * philox_uniforms   -- Philox4x32-10 (Salmon et al., SC'11)
+  * dsd_*             -- "Hardware-aware dynamic speculative decoding":
+                         goodput = AL / ITL, the offline K table, its
+                         runtime lookup, live statistics, and the graph keys
+                         <tokens, K> of "Compatibility with full CUDA Graph"
 
 Pins (in tests/test_oracle_pins.py, all ``-m "not gpu"``):
   * mask: the 6-node matrix printed on the SpecInfer guide (tests/golden),
@@ -81,6 +85,11 @@ def lib():
         L.oracle_kv_release.argtypes = [P, i32, i32, P, P, P, P, i32, P, i32, P]
         L.oracle_tree_expand_level.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P]
         L.oracle_tree_merge.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P]
+        L.oracle_dsd_optimal_k.argtypes = [P, P, i32, i32, P, P]
+        L.oracle_dsd_select_k.argtypes = [P, P, i32, i32]
+        L.oracle_dsd_graph_keys.argtypes = [i32, i32, P, P, i32]
+        L.oracle_dsd_blend.argtypes = [f64, f64, f64]
+        L.oracle_dsd_blend.restype = f64
         L.oracle_philox4x32_10.argtypes = [P, P, P]
         L.oracle_philox_uniforms.argtypes = [u64, u32, P, i32, P]
         L.oracle_canon_exp.argtypes = [ctypes.c_float]
@@ -260,6 +269,32 @@ def tree_merge(seqs, lens, root_tok, V):
     T = int(tree_off[-1])
     return dict(tree_off=tree_off, parent=parent[:T], tokens=tokens[:T], src=src[:T], node_of=node_of,
                 status=status)
+
+
+def dsd_optimal_k(al, itl, k_values):
+    """al, itl: [n_bs, n_k]; returns the K of highest AL / ITL per row (-1: none)."""
+    al, itl = _c(al, np.float64), _c(itl, np.float64)
+    k_values = _c(k_values, np.int32)
+    n_bs, n_k = al.shape
+    out = np.zeros(n_bs, np.int32)
+    lib().oracle_dsd_optimal_k(_p(al), _p(itl), n_bs, n_k, _p(k_values), _p(out))
+    return out
+
+
+def dsd_select_k(bs_table, k_table, bs):
+    bs_table, k_table = _c(bs_table, np.int32), _c(k_table, np.int32)
+    return int(lib().oracle_dsd_select_k(_p(bs_table), _p(k_table), len(bs_table), int(bs)))
+
+
+def dsd_graph_keys(max_tokens, max_k):
+    n = lib().oracle_dsd_graph_keys(max_tokens, max_k, None, None, 0)
+    t, k = np.zeros(max(n, 1), np.int32), np.zeros(max(n, 1), np.int32)
+    lib().oracle_dsd_graph_keys(max_tokens, max_k, _p(t), _p(k), n)
+    return list(zip(t[:n].tolist(), k[:n].tolist()))
+
+
+def dsd_blend(cell, sample, w):
+    return float(lib().oracle_dsd_blend(float(cell), float(sample), float(w)))
 
 
 def philox4x32_10(ctr, key):

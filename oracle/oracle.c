@@ -855,3 +855,73 @@ void oracle_canon_exp_array(const float *x, float *y, int64_t n)
 {
     for (int64_t i = 0; i < n; i++) y[i] = oracle_canon_exp(x[i]);
 }
+
+
+/* ------------------------------------------------------------------ */
+/* Dynamic draft length (goodput tables)                               */
+/* ------------------------------------------------------------------ */
+
+/* "Hardware-aware dynamic speculative decoding": goodput = AL / ITL; the
+ * offline table holds, per batch size, the K of highest goodput.  al and
+ * itl are [n_bs][n_k] measurements for the draft lengths k_values[0..n_k-1];
+ * a cell counts only when both are finite and itl > 0.  k_opt[b] = the K of
+ * the largest goodput in row b, the earliest column on ties; -1 when no cell
+ * of the row counts. */
+int oracle_dsd_optimal_k(const double *al, const double *itl, int n_bs, int n_k, const int32_t *k_values,
+                         int32_t *k_opt)
+{
+    for (int b = 0; b < n_bs; b++) {
+        int best = -1;
+        double best_g = 0.0;
+        for (int j = 0; j < n_k; j++) {
+            double a = al[(size_t)b * n_k + j], t = itl[(size_t)b * n_k + j];
+            if (!isfinite(a) || !isfinite(t) || !(t > 0.0)) continue;
+            double g = a / t;
+            if (best < 0 || g > best_g) {
+                best = j;
+                best_g = g;
+            }
+        }
+        k_opt[b] = best < 0 ? -1 : k_values[best];
+    }
+    return 0;
+}
+
+/* Runtime lookup: the table's entry for the largest profiled batch size not
+ * above bs (bs_table ascending); below the first entry, the first. */
+int oracle_dsd_select_k(const int32_t *bs_table, const int32_t *k_table, int n, int bs)
+{
+    if (n <= 0) return -1;
+    int k = k_table[0];
+    for (int i = 0; i < n; i++)
+        if (bs_table[i] <= bs) k = k_table[i];
+    return k;
+}
+
+/* Graph keys (same page, "Compatibility with full CUDA Graph"): every
+ * <tokens, K> with 1 <= tokens <= max_tokens and 1 <= K <= max_k such that
+ * tokens is divisible by K + 1 (then every request of the batch is a decode
+ * request with K drafts), in increasing tokens, then K.  Returns the count;
+ * at most cap pairs are stored. */
+int oracle_dsd_graph_keys(int max_tokens, int max_k, int32_t *tokens_out, int32_t *k_out, int cap)
+{
+    int n = 0;
+    for (int t = 1; t <= max_tokens; t++)
+        for (int k = 1; k <= max_k; k++)
+            if (t % (k + 1) == 0) {
+                if (n < cap) {
+                    tokens_out[n] = t;
+                    k_out[n] = k;
+                }
+                n++;
+            }
+    return n;
+}
+
+/* Live statistics folded into a cell: x <- (1 - w) x + w * sample, for w in
+ * (0, 1]; a cell without a finite value takes the sample. */
+double oracle_dsd_blend(double cell, double sample, double w)
+{
+    if (!isfinite(cell)) return sample;
+    return (1.0 - w) * cell + w * sample;
+}

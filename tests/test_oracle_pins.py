@@ -986,6 +986,66 @@ def test_merge_special_cases_and_bad_inputs(oracle):
     assert r["tree_off"].tolist() == [0, 1, 6, 7] and (r["node_of"][0] == -1).all()
 
 
+# -------------------------------------------------- dynamic draft length ----
+
+def test_graph_keys_of_the_printed_example(oracle):
+    d = dict(read_golden("dsd_graph_keys.txt"))
+    max_k, tokens = int(d["max_k"][0]), int(d["tokens"][0])
+    keys = oracle.dsd_graph_keys(tokens, max_k)
+    assert [k for t, k in keys if t == tokens] == [int(v) for v in d["dynamic_k"]]
+    assert int(d["fixed_k"][0]) in [k for t, k in keys if t == tokens]
+    # brute force over a wider range: exactly the divisible pairs, in order
+    keys = oracle.dsd_graph_keys(200, 9)
+    assert keys == [(t, k) for t in range(1, 201) for k in range(1, 10) if t % (k + 1) == 0]
+
+
+def _al_closed(alpha, K):
+    return (1 - alpha ** (K + 1)) / (1 - alpha)
+
+
+def test_optimal_k_maximises_goodput_and_falls_with_batch_size(oracle):
+    """goodput = AL / ITL with AL the closed form of "Inference Optimization
+    Techniques" (E[T] = (1 - a^(K+1)) / (1 - a)) and a dense-model cost ITL =
+    c0 + c1 * BS * (K + 1): the table equals a brute-force argmax, and the
+    optimal K does not grow with the batch size (the page's dense-model
+    statement)."""
+    ks = np.arange(1, 9, dtype=np.int32)
+    bss = np.array([1, 2, 4, 8, 16, 32, 64, 128, 256, 512])
+    for alpha, c0, c1 in [(0.8, 10.0, 0.05), (0.6, 5.0, 0.2), (0.9, 20.0, 0.01)]:
+        al = np.array([[_al_closed(alpha, k) for k in ks] for _ in bss])
+        itl = np.array([[c0 + c1 * bs * (k + 1) for k in ks] for bs in bss])
+        kopt = oracle.dsd_optimal_k(al, itl, ks)
+        brute = [int(ks[int(np.argmax(al[i] / itl[i]))]) for i in range(len(bss))]
+        assert kopt.tolist() == brute
+        assert all(a >= b for a, b in zip(kopt[:-1], kopt[1:])), kopt
+        assert kopt[0] > kopt[-1]
+
+
+def test_optimal_k_ties_invalid_cells_and_lookup(oracle):
+    ks = np.array([1, 2, 3], np.int32)
+    al = np.array([[2.0, 4.0, 6.0], [1.0, np.nan, 5.0], [1.0, 2.0, 3.0], [np.inf, 1.0, 1.0]])
+    itl = np.array([[1.0, 2.0, 3.0], [1.0, 1.0, 0.0], [-1.0, 0.0, np.nan], [1.0, 1.0, 2.0]])
+    assert oracle.dsd_optimal_k(al, itl, ks).tolist() == [1, 1, -1, 2]
+    bs_tab, k_tab = [1, 4, 32, 128], [6, 5, 3, 1]
+    for bs, want in [(0, 6), (1, 6), (3, 6), (4, 5), (31, 5), (32, 3), (127, 3), (128, 1), (10 ** 6, 1)]:
+        assert oracle.dsd_select_k(bs_tab, k_tab, bs) == want
+    assert oracle.dsd_select_k([], [], 5) == -1
+
+
+def test_blend_is_an_exponential_moving_average(oracle):
+    x = np.nan
+    samples = [3.0, 5.0, 4.0, 10.0]
+    w = 0.25
+    ref = samples[0]
+    x = oracle.dsd_blend(x, samples[0], w)
+    assert x == ref
+    for smp in samples[1:]:
+        ref = (1 - w) * ref + w * smp
+        x = oracle.dsd_blend(x, smp, w)
+        assert abs(x - ref) < 1e-15
+    assert oracle.dsd_blend(7.0, 1.0, 1.0) == 1.0
+
+
 def test_philox_matches_pytorch_engine(oracle):
     """Philox4x32-10 against the independent engine in PyTorch's public
     headers (ATen/core/PhiloxRNGEngine.h): key = seed, counter = (offset lo,
