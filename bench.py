@@ -443,6 +443,8 @@ def bench_gpu(args):
         line["commit_layers"] = measure_commit_layers(args.commit_layers, passes[0], dev)
     if args.tree_build:
         line["tree_build"] = measure_tree_build(dev)
+    if args.dsd:
+        line["dsd"] = measure_dsd(dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, _ = run_cpu_baseline(works[0], args.mode)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
@@ -682,6 +684,58 @@ def measure_tree_build(dev, reps=20, replays=5):
                       "launches": 3, "nodes": int(moff[-1].item())}}
 
 
+def measure_dsd(dev, bss=(1, 4, 16, 64), max_k=8, replays=20):
+    """Offline goodput profile of this pass ("Hardware-aware dynamic
+    speculative decoding"): for each batch size, the sweep workload's chains
+    (prefix 4096, V = 32000, alpha = 0.3) cut to K + 1 nodes for K = 1..max_k;
+    each <tokens = B (K + 1), K> pass captured once in the graph cache and
+    replayed; ITL = the replay time (this library's verification pass:
+    mask, one attention layer, verification, commit); AL = emitted tokens per
+    request, averaged over the largest batch (acceptance is a property of the
+    draft/target pair, not of the batch size; one request alone is too few).
+    The table's optimal K per batch size comes from the library."""
+    import torch
+    import workloads as W
+    from tree_speculative_verification_spec_gb300.dynamic_k import DynamicK, GraphCache
+    from tree_speculative_verification_spec_gb300.pipeline import DeviceBatch, VerifyPass
+    ks = list(range(1, max_k + 1))
+    pol = DynamicK(bss, ks)
+    itl, al_big = {}, {}
+    for i, B in enumerate(bss):
+        full = W.config4(K=max_k, B=B, tree="chain", alpha=0.3)
+        made = {}
+
+        def make(tokens, K):
+            vp = VerifyPass(DeviceBatch.from_workload(W.chain_prefix(full, K + 1), device=dev))
+            made[(tokens, K)] = vp
+            return vp
+
+        cache = GraphCache(make)
+        for j, K in enumerate(ks):
+            key = (B * (K + 1), K)
+            vp = cache.replay(*key)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            stream = torch.cuda.current_stream(dev)
+            a.record(stream)
+            for _ in range(replays):
+                cache.replay(*key)
+            b.record(stream)
+            torch.cuda.synchronize()
+            itl[(i, j)] = a.elapsed_time(b) * 1e3 / replays
+            if B == max(bss):
+                al_big[j] = float(vp.n_emitted[:B].float().mean())
+        del cache, made, full
+        torch.cuda.empty_cache()
+    for (i, j), t in itl.items():
+        pol.record(i, j, al_big[j], t)
+    k_opt = pol.optimal_k()
+    return {"batch_sizes": list(bss), "k_values": ks, "al": [[round(x, 4) for x in r] for r in pol.al.tolist()],
+            "itl_us": [[round(x, 2) for x in r] for r in pol.itl.tolist()],
+            "goodput_tok_per_us": [[round(a / t, 5) for a, t in zip(ra, rt)] for ra, rt in zip(pol.al, pol.itl)],
+            "k_opt": k_opt.tolist(), "graphs_captured": len(bss) * len(ks)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -697,6 +751,7 @@ def main():
     ap.add_argument("--q-per-child", action="store_true",
                     help="read the draft rows per child (merged trees) instead of per parent")
     ap.add_argument("--tree-build", action="store_true", help="also time device tree construction")
+    ap.add_argument("--dsd", action="store_true", help="also profile goodput = AL / ITL per batch size and K")
     ap.add_argument("--commit-layers", type=int, default=0,
                     help="also time the commit of this many layers' caches in one launch (0: off)")
     args = ap.parse_args()

@@ -361,6 +361,39 @@ spec_status spec_tree_merge(const int32_t* seqs, const int32_t* lens, const int3
                             int32_t* node_of, int32_t* status, void* stream);
 
 /*
+ * Dynamic draft length ("Hardware-aware dynamic speculative decoding",
+ * "Dynamic speculative decoding" and "Compatibility with full CUDA Graph"):
+ * the scheduler picks, per step, the number of draft tokens K of highest
+ * goodput = AL / ITL (acceptance length over inter-token latency) for the
+ * current batch size, from a table profiled offline and refreshed with live
+ * statistics, and replays the full CUDA graph captured for <tokens, K>.
+ * HOST functions: every pointer is host memory; nothing is launched.
+ *
+ * spec_dsd_optimal_k: al, itl double [n_bs][n_k] (measured AL and ITL for the
+ *   draft lengths k_values[0..n_k-1] at each profiled batch size); a cell
+ *   counts when both are finite and itl > 0.  k_opt int32 [n_bs] out: the K
+ *   of the largest goodput in each row, the earliest column on ties; -1 when
+ *   no cell of the row counts.
+ * spec_dsd_select_k: bs_table int32 [n] strictly ascending (else
+ *   SPEC_ERR_INVALID_ARG), k_table int32 [n]; *k_out = the entry of the
+ *   largest bs_table[i] <= bs, or k_table[0] when bs < bs_table[0].
+ * spec_dsd_update: folds one live measurement into cell (bs_index, k_index):
+ *   x <- x + weight * (sample - x), weight in (0, 1]; a cell that is not
+ *   finite (unmeasured) takes the sample.  Samples must be finite.
+ * spec_dsd_graph_keys: every <tokens, K> with 1 <= tokens <= max_tokens and
+ *   1 <= K <= max_k such that tokens is divisible by K + 1 (every request of
+ *   the batch is then a decode request with K drafts), ordered by tokens
+ *   then K.  *count = their number; the first min(cap, count) are stored.
+ */
+spec_status spec_dsd_optimal_k(const double* al, const double* itl, int n_bs, int n_k, const int32_t* k_values,
+                               int32_t* k_opt);
+spec_status spec_dsd_select_k(const int32_t* bs_table, const int32_t* k_table, int n, int bs, int32_t* k_out);
+spec_status spec_dsd_update(double* al, double* itl, int n_bs, int n_k, int bs_index, int k_index, double al_sample,
+                            double itl_sample, double weight);
+spec_status spec_dsd_graph_keys(int max_tokens, int max_k, int32_t* tokens_out, int32_t* k_out, int cap,
+                                int32_t* count);
+
+/*
  * Diagnostic of the bounded device waits (no counterpart on the pages): one
  * small kernel waits on a barrier that nothing ever completes, with a limit of
  * `polls` polls (1 .. 2^20), the same wait the tensor-core attention roles use

@@ -470,6 +470,47 @@ def test_merge_parity(B, M, m, V):
         assert ref["status"][1] == S.SPEC_DEV_BAD_TREE and ref["status"][2] == S.SPEC_DEV_BAD_TOKEN
 
 
+# --------------------------------------------- graphs per <tokens, K> ----
+
+def test_graph_cache_per_tokens_and_k():
+    """Full graphs of the pass for the <tokens, K> keys with tokens divisible
+    by K + 1: each key's first use captures, a replay verifies its batch as
+    the oracle does, and new inputs copied into the same buffers replay
+    correctly as well."""
+    from tree_speculative_verification_spec_gb300.dynamic_k import GraphCache
+    keys = [key for key in S.spec_dsd_graph_keys(12, 3) if key[0] in (8, 12)]
+    assert keys == [(8, 1), (8, 3), (12, 1), (12, 2), (12, 3)]
+    works = {}
+
+    def make(tokens, K):
+        w = W.config4(K=K, B=tokens // (K + 1), tree="chain", alpha=0.3, seed=60, prefix=80, V=1000)
+        works[(tokens, K)] = w
+        return VerifyPass(DeviceBatch.from_workload(w))
+
+    cache = GraphCache(make)
+    for key in keys:
+        vp = cache.replay(*key)
+        torch.cuda.synchronize()
+        w = works[key]
+        ref = oracle_stochastic(w)
+        got = dict(path=vp.path.cpu().numpy(), accept_len=vp.accept_len.cpu().numpy(),
+                   emitted=vp.emitted.cpu().numpy(), n_emitted=vp.n_emitted.cpu().numpy(),
+                   status=vp.status.cpu().numpy())
+        _assert_verify_equal(got, ref, w.B)
+    assert cache.keys() == keys
+    # new inputs into the captured buffers of one key
+    key = (12, 2)
+    w2 = W.config4(K=2, B=4, tree="chain", alpha=0.3, seed=61, prefix=80, V=1000)
+    vp = cache.pass_for(*key)
+    for name in ("tokens", "p_logits", "q_probs", "uniforms", "q"):
+        getattr(vp.batch, name).copy_(getattr(w2, name))
+    vp = cache.replay(*key)
+    torch.cuda.synchronize()
+    ref = oracle_stochastic(w2)
+    assert np.array_equal(vp.emitted.cpu().numpy()[:4], ref["emitted"][:4])
+    assert np.array_equal(vp.accept_len.cpu().numpy()[:4], ref["accept_len"][:4])
+
+
 # ------------------------------------------------------------- attention ----
 
 def _gpu_attention(w, flags=S.SPEC_ATTN_AUTO, max_prefix=None):

@@ -36,6 +36,10 @@ SIGNATURES = {
     "spec_tree_init": ([_P, _I, _I, _P, _P, _P, _P], _I),
     "spec_tree_expand_level": ([_P, _I, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "spec_tree_merge": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
+    "spec_dsd_optimal_k": ([_P, _P, _I, _I, _P, _P], _I),
+    "spec_dsd_select_k": ([_P, _P, _I, _I, _P], _I),
+    "spec_dsd_update": ([_P, _P, _I, _I, _I, _I, ctypes.c_double, ctypes.c_double, ctypes.c_double], _I),
+    "spec_dsd_graph_keys": ([_I, _I, _P, _P, _I, _P], _I),
     "spec_tree_verify_stochastic": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
     "spec_kv_commit": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "spec_kv_commit_layers": ([_P, _P, _I, _P, _I, _I, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P],
@@ -173,6 +177,51 @@ def spec_tree_merge(seqs, lens, root_tok, B, M, m, V, tree_off, parent, tokens, 
     _check("spec_tree_merge", lib().spec_tree_merge(
         _ptr(seqs), _ptr(lens), _ptr(root_tok), B, M, m, V, _ptr(tree_off), _ptr(parent), _ptr(tokens), _ptr(src),
         _ptr(node_of), _ptr(status), _stream(stream)))
+
+
+def _hptr(a, dtype):
+    """Host (numpy) array argument: C-contiguous and of the C type, else an error."""
+    import numpy as np
+    if a is None:
+        return None
+    if not isinstance(a, np.ndarray) or a.dtype != dtype or not a.flags["C_CONTIGUOUS"]:
+        raise ValueError(f"host arguments must be C-contiguous numpy arrays of {np.dtype(dtype).name}")
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def spec_dsd_optimal_k(al, itl, k_values, k_opt):
+    """al, itl: float64 [n_bs, n_k]; k_values int32 [n_k]; k_opt int32 [n_bs] out (host arrays)."""
+    import numpy as np
+    n_bs, n_k = al.shape
+    _check("spec_dsd_optimal_k", lib().spec_dsd_optimal_k(_hptr(al, np.float64), _hptr(itl, np.float64), n_bs, n_k,
+                                                          _hptr(k_values, np.int32), _hptr(k_opt, np.int32)))
+
+
+def spec_dsd_select_k(bs_table, k_table, bs):
+    import numpy as np
+    out = np.zeros(1, np.int32)
+    _check("spec_dsd_select_k", lib().spec_dsd_select_k(_hptr(bs_table, np.int32), _hptr(k_table, np.int32),
+                                                        len(bs_table), int(bs), _hptr(out, np.int32)))
+    return int(out[0])
+
+
+def spec_dsd_update(al, itl, bs_index, k_index, al_sample, itl_sample, weight):
+    import numpy as np
+    n_bs, n_k = al.shape
+    _check("spec_dsd_update", lib().spec_dsd_update(_hptr(al, np.float64), _hptr(itl, np.float64), n_bs, n_k,
+                                                    bs_index, k_index, al_sample, itl_sample, weight))
+
+
+def spec_dsd_graph_keys(max_tokens, max_k):
+    """Returns [(tokens, K), ...]."""
+    import numpy as np
+    cnt = np.zeros(1, np.int32)
+    _check("spec_dsd_graph_keys", lib().spec_dsd_graph_keys(max_tokens, max_k, None, None, 0, _hptr(cnt, np.int32)))
+    n = int(cnt[0])
+    t, k = np.zeros(max(n, 1), np.int32), np.zeros(max(n, 1), np.int32)
+    _check("spec_dsd_graph_keys", lib().spec_dsd_graph_keys(max_tokens, max_k, _hptr(t, np.int32),
+                                                            _hptr(k, np.int32), n, _hptr(cnt, np.int32)))
+    return list(zip(t[:n].tolist(), k[:n].tolist()))
 
 
 def spec_kv_commit(k_cache, v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len, path, path_stride,

@@ -401,6 +401,22 @@ def config4(K=4, B=16, tree="chain", alpha=0.3, seed=1004, prefix=4096, V=32000,
                  meta=dict(K=K, tree=tree, alpha=alpha))
 
 
+def chain_prefix(w, n):
+    """The first n nodes of every request of a chain workload (a chain's
+    prefix is a chain): the same requests, prefixes and cache with K = n - 1
+    drafts."""
+    assert 1 <= n <= w.n_max and all(int(w.tree_off[b + 1] - w.tree_off[b]) == w.n_max for b in range(w.B))
+    rows = torch.cat([torch.arange(b * w.n_max, b * w.n_max + n) for b in range(w.B)])
+    meta = dict(w.meta, K=n - 1)
+    return Workload(name=w.name.replace(f"K={w.n_max - 1}", f"K={n - 1}"), B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D,
+                    dtype=w.dtype, V=w.V, n_max=n, block_size=w.block_size, parent=torch.cat([chain_tree(n)] * w.B),
+                    tree_off=torch.arange(0, w.B * n + 1, n, dtype=torch.int32), tokens=w.tokens[rows].contiguous(),
+                    prefix_len=w.prefix_len, block_table=w.block_table, num_blocks=w.num_blocks,
+                    q=w.q[rows].contiguous(), k_cache=w.k_cache, v_cache=w.v_cache,
+                    p_logits=w.p_logits[rows].contiguous(), q_probs=w.q_probs[rows].contiguous(),
+                    uniforms=w.uniforms[rows].contiguous(), meta=meta)
+
+
 def make_config(i, **kw):
     return [config0, config1, config2, config3, config4][i](**kw)
 
