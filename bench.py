@@ -421,6 +421,17 @@ def bench_gpu(args):
     launches_per_step = 4 + (1 if _attn_splits(passes[0]) > 1 else 0) + (1 if _verify_uses_stats(w0, args.mode) else 0)
     traffic = _profiled_traffic(dom, args.mode, args.workload)
 
+    # the dominant kernel's roof: tensor when its arithmetic intensity is above
+    # the ridge point of the measured peaks (attention over wide trees), else HBM
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind}
+    if dom == "attention" and t_attn > 0:
+        ridge = _bf16_peak() * 1e12 / (peak * 1e9)
+        if flops / algo["attention"] > ridge:
+            tf = kernels["attention"]["tflops"]
+            roofline = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": _bf16_peak(), "unit": "TFLOP/s",
+                        "frac": tf / _bf16_peak(), "traffic": traffic, "peak_source": peak_kind + " (bf16 burst)",
+                        "flop_per_byte": flops / algo["attention"], "ridge_flop_per_byte": ridge}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -436,8 +447,7 @@ def bench_gpu(args):
             "clocks": clk.summary(),
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
-            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind},
+            "roofline": roofline,
             "kernels": kernels}
     if args.commit_layers > 0:
         line["commit_layers"] = measure_commit_layers(args.commit_layers, passes[0], dev)
