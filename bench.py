@@ -694,7 +694,7 @@ def measure_tree_build(dev, reps=20, replays=5):
                       "launches": 3, "nodes": int(moff[-1].item())}}
 
 
-def measure_dsd(dev, bss=(1, 4, 16, 64), max_k=8, replays=20):
+def measure_dsd(dev, bss=(1, 4, 16, 64, 256), max_k=8, replays=20):
     """Offline goodput profile of this pass ("Hardware-aware dynamic
     speculative decoding"): for each batch size, the sweep workload's chains
     (prefix 4096, V = 32000, alpha = 0.3) cut to K + 1 nodes for K = 1..max_k;
@@ -703,7 +703,11 @@ def measure_dsd(dev, bss=(1, 4, 16, 64), max_k=8, replays=20):
     mask, one attention layer, verification, commit); AL = emitted tokens per
     request, averaged over the largest batch (acceptance is a property of the
     draft/target pair, not of the batch size; one request alone is too few).
-    The table's optimal K per batch size comes from the library."""
+    The table's optimal K per batch size comes from the library.  Beside the
+    measured AL: the closed form (1 - a^(K+1)) / (1 - a) of "Inference
+    Optimization Techniques" with a = the mean over the drafts of
+    sum_x min(p(x), q(x)) (the per-draft acceptance probability), computed on
+    the host from the largest batch's rows."""
     import torch
     import workloads as W
     from tree_speculative_verification_spec_gb300.dynamic_k import DynamicK, GraphCache
@@ -735,12 +739,21 @@ def measure_dsd(dev, bss=(1, 4, 16, 64), max_k=8, replays=20):
             itl[(i, j)] = a.elapsed_time(b) * 1e3 / replays
             if B == max(bss):
                 al_big[j] = float(vp.n_emitted[:B].float().mean())
+        if B == max(bss):
+            # per-draft acceptance: rows of the chains' parents (nodes 0 .. max_k - 1)
+            rows = torch.cat([torch.arange(b * (max_k + 1), b * (max_k + 1) + max_k) for b in range(B)])
+            p = torch.softmax(full.p_logits[rows].double(), -1)
+            a_hat = float(torch.minimum(p, full.q_probs[rows].double()).sum(-1).mean())
         del cache, made, full
         torch.cuda.empty_cache()
     for (i, j), t in itl.items():
         pol.record(i, j, al_big[j], t)
     k_opt = pol.optimal_k()
-    return {"batch_sizes": list(bss), "k_values": ks, "al": [[round(x, 4) for x in r] for r in pol.al.tolist()],
+    closed = [(1 - a_hat ** (K + 1)) / (1 - a_hat) for K in ks]
+    return {"batch_sizes": list(bss), "k_values": ks, "acceptance_a": a_hat,
+            "al_measured": [round(al_big[j], 4) for j in range(len(ks))],
+            "al_closed_form": [round(x, 4) for x in closed],
+            "al": [[round(x, 4) for x in r] for r in pol.al.tolist()],
             "itl_us": [[round(x, 2) for x in r] for r in pol.itl.tolist()],
             "goodput_tok_per_us": [[round(a / t, 5) for a, t in zip(ra, rt)] for ra, rt in zip(pol.al, pol.itl)],
             "k_opt": k_opt.tolist(), "graphs_captured": len(bss) * len(ks)}
