@@ -510,41 +510,77 @@ def _set_mb(w):
     return sum(t.numel() * t.element_size() for t in ts) / 1e6
 
 
+STEP_INPUTS = ("q", "parent", "tokens", "tree_off", "prefix_len", "p_logits", "q_probs", "uniforms")
+
+
 def run_e2e(args, works, sets, passes, stream, dev, n_sets):
+    """The pass through the C ABI with host buffers.  Every step copies its
+    inputs from pinned host memory into one of two device input slots (on a
+    copy stream) and reads its emitted tokens back; step i+1's copy overlaps
+    step i's compute.  The KV cache and block table are resident state, shared
+    by the slots of one input set."""
+    import dataclasses
     import torch
+    from tree_speculative_verification_spec_gb300.pipeline import VerifyPass
     steps = max(3, args.steps)
     host = []
     for w in works:
-        h = {k: getattr(w, k).pin_memory() for k in ("q", "parent", "tokens", "tree_off", "prefix_len", "p_logits",
-                                                      "q_probs", "uniforms")}
-        host.append(h)
-    out_tok = [torch.empty((p.batch.B, p.batch.n_max), dtype=torch.int32).pin_memory() for p in passes]
-    out_n = [torch.empty(p.batch.B, dtype=torch.int32).pin_memory() for p in passes]
+        host.append({k: getattr(w, k).pin_memory() for k in STEP_INPUTS})
+    # two device slots per input set: the set's own buffers, and a shadow
+    # with fresh per-step inputs and the same cache (and a pass of its own)
+    slots = []
+    for j in range(n_sets):
+        d = sets[j]
+        shadow = dataclasses.replace(d, **{k: torch.empty_like(getattr(d, k)) for k in STEP_INPUTS})
+        vp2 = VerifyPass(shadow)
+        vp2.inv_temp, vp2.q_layout = passes[j].inv_temp, passes[j].q_layout
+        slots.append([(d, passes[j]), (shadow, vp2)])
+    out_tok = [[torch.empty((p.batch.B, p.batch.n_max), dtype=torch.int32).pin_memory() for _ in range(2)]
+               for p in passes]
+    out_n = [[torch.empty(p.batch.B, dtype=torch.int32).pin_memory() for _ in range(2)] for p in passes]
     h2d = sum(t.numel() * t.element_size() for t in host[0].values())
-    d2h = out_tok[0].numel() * 4 + out_n[0].numel() * 4
+    d2h = out_tok[0][0].numel() * 4 + out_n[0][0].numel() * 4
+    copy_stream = torch.cuda.Stream(dev)
+    copied = [[torch.cuda.Event() for _ in range(2)] for _ in range(n_sets)]
+    consumed = [[torch.cuda.Event() for _ in range(2)] for _ in range(n_sets)]
+    used = [[False, False] for _ in range(n_sets)]
 
     def e2e_step(i):
-        j = i % n_sets
-        d, vp, h = sets[j], passes[j], host[j]
-        for k, t in h.items():
-            getattr(d, k).copy_(t, non_blocking=True)
+        j, k = i % n_sets, (i // n_sets) % 2
+        d, vp = slots[j][k]
+        h = host[j]
+        with torch.cuda.stream(copy_stream):
+            if used[j][k]:
+                copy_stream.wait_event(consumed[j][k])  # the slot's previous pass has read its inputs
+            for name, t in h.items():
+                getattr(d, name).copy_(t, non_blocking=True)
+            copied[j][k].record(copy_stream)
+        stream.wait_event(copied[j][k])
         vp.run(args.mode, args.attn_flags)
-        out_tok[j].copy_(vp.emitted, non_blocking=True)
-        out_n[j].copy_(vp.n_emitted, non_blocking=True)
+        consumed[j][k].record(stream)
+        used[j][k] = True
+        out_tok[j][k].copy_(vp.emitted, non_blocking=True)
+        out_n[j][k].copy_(vp.n_emitted, non_blocking=True)
+        return j, k
 
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
+    done = []
     for i in range(steps):
-        e2e_step(i)
+        done.append(e2e_step(i))
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
-    toks = sum(int(out_n[i % n_sets].sum()) for i in range(steps))
+    # every step's result was read back inside the timed region; a slot's
+    # inputs are the same at every step, so its last read-back counts for all
+    per_slot = {(j, k): int(out_n[j][k].sum()) for j in range(n_sets) for k in range(2)}
+    toks = sum(per_slot[jk] for jk in done)
     return {"value": toks / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms / steps}
+            "ms_per_step": ms / steps,
+            "overlap": "step i+1's host-to-device copy (copy stream) overlaps step i's pass; two input slots"}
 
 
 def measure_commit_layers(L, vp, dev, reps=20, replays=5):
