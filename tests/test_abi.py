@@ -99,6 +99,22 @@ def test_host_argument_checks_return_codes_without_launching(libpath):
     assert L.spec_kv_commit(None, None, None, 4, 12, 4, None, None, 4, None, 1, 2, 64, 1, None, None, None) == \
         S.SPEC_ERR_UNSUPPORTED
     assert L.spec_philox_uniforms(0, 0, None, -1, 4, None, None) == S.SPEC_ERR_INVALID_ARG
+    # layered commit: layers, page size, pool arguments given by halves
+    lc = [None, None, 0, None, 4, 16, 4, None, None, None, 4, None, 1, 2, 64, 1, None, None, 0, None, None, None]
+    assert L.spec_kv_commit_layers(*lc) == S.SPEC_ERR_INVALID_ARG  # no layers
+    lc[2] = 2
+    lc[5] = 12
+    assert L.spec_kv_commit_layers(*lc) == S.SPEC_ERR_UNSUPPORTED  # page size not a power of two
+    # tree construction: k above 32, a level past n_total, merge shapes past 1023 candidates
+    assert L.spec_tree_expand_level(None, 1, 1, 100, 33, 0, 64, None, None, None) == S.SPEC_ERR_UNSUPPORTED
+    assert L.spec_tree_expand_level(None, 1, 2, 100, 4, 0, 9, None, None, None) == S.SPEC_ERR_INVALID_ARG
+    assert L.spec_tree_expand_level(None, 1, 1, 100, 4, 0, 5, None, None, None) == S.SPEC_ERR_INVALID_ARG  # NULLs
+    assert L.spec_tree_init(None, 2, 0, None, None, None, None) == S.SPEC_ERR_INVALID_ARG
+    assert L.spec_tree_init(None, 2, 2000, None, None, None, None) == S.SPEC_ERR_UNSUPPORTED
+    assert L.spec_tree_merge(None, None, None, 1, 32, 32, 10, None, None, None, None, None, None, None) == \
+        S.SPEC_ERR_UNSUPPORTED
+    assert L.spec_tree_merge(None, None, None, 1, 4, 4, 10, None, None, None, None, None, None, None) == \
+        S.SPEC_ERR_INVALID_ARG
     assert L.spec_selftest_bounded_wait(None, 16, None) == S.SPEC_ERR_INVALID_ARG
     assert L.spec_selftest_bounded_wait(ctypes.c_void_p(16), 0, None) == S.SPEC_ERR_INVALID_ARG
 
