@@ -83,8 +83,12 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 /* Library version, (major << 16) | minor. */
 int spec_version(void);
 
-/* Human-readable name of a return code or of one SPEC_DEV_* bit. */
+/* Human-readable name of a return code (SPEC_OK, SPEC_ERR_*). */
 const char* spec_status_string(spec_status s);
+
+/* Human-readable name of one device status bit (SPEC_DEV_*); "unknown status
+ * bit" for anything else (0, several bits, or an undefined bit). */
+const char* spec_dev_status_string(int32_t bit);
 
 /*
  * Topology mask build.  "SpecInfer Guide", "The Topology-Aware 2D Causal Mask":

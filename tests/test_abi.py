@@ -58,6 +58,9 @@ def test_binding_covers_every_declared_symbol(libpath):
 def test_version_and_status_strings(libpath):
     assert S.version() >= 1
     assert S.status_string(0) == "ok"
+    assert S.spec_dev_status_string(S.SPEC_DEV_BAD_TEMP) == "bad inverse temperature"
+    assert S.spec_dev_status_string(3) == "unknown status bit"
+    assert S.dev_status_names(S.SPEC_DEV_BAD_TREE | S.SPEC_DEV_BAD_PATH) == ["bad tree", "bad commit path"]
     assert "workspace" in S.status_string(4)
 
 

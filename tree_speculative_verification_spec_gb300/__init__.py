@@ -12,4 +12,4 @@ from ._binding import (SPEC_ATTN_AUTO, SPEC_ATTN_CUDA_CORE, SPEC_ATTN_NOALLOC_BY
                        spec_philox_uniforms, spec_selftest_bounded_wait, spec_tree_attention, spec_tree_expand_level, spec_tree_init,
                        spec_tree_mask_build, spec_tree_merge, spec_tree_verify_greedy,
                        spec_tree_verify_stochastic, spec_tree_attention_noalloc,
-                       spec_verify_workspace_size, status_string, version)
+                       spec_verify_workspace_size, status_string, version, spec_dev_status_string, dev_status_names)

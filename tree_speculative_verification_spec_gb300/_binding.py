@@ -25,6 +25,7 @@ _P, _I, _U32, _U64, _SZ, _F = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, c
 SIGNATURES = {
     "spec_version": ([], _I),
     "spec_status_string": ([_I], ctypes.c_char_p),
+    "spec_dev_status_string": ([_I], ctypes.c_char_p),
     "spec_tree_mask_build": ([_P, _P, _I, _I, _P, _P, _P, _P], _I),
     "spec_attention_workspace_size": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
     "spec_tree_attention": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _SZ,
@@ -75,6 +76,15 @@ def lib():
 
 def status_string(code):
     return lib().spec_status_string(int(code)).decode()
+
+
+def spec_dev_status_string(bit):
+    return lib().spec_dev_status_string(int(bit)).decode()
+
+
+def dev_status_names(word):
+    """The names of the SPEC_DEV_* bits set in a status word."""
+    return [spec_dev_status_string(1 << i) for i in range(31) if int(word) >> i & 1]
 
 
 def version():

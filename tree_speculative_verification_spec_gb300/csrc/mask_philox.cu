@@ -101,6 +101,20 @@ const char* spec_status_string(spec_status s) {
   return "unknown status";
 }
 
+const char* spec_dev_status_string(int32_t bit) {
+  switch (bit) {
+    case SPEC_DEV_BAD_TREE: return "bad tree";
+    case SPEC_DEV_BAD_TOKEN: return "bad token";
+    case SPEC_DEV_CAPACITY: return "prefix beyond capacity";
+    case SPEC_DEV_TIMEOUT: return "device wait timed out";
+    case SPEC_DEV_BAD_BLOCK: return "bad block id";
+    case SPEC_DEV_BAD_PATH: return "bad commit path";
+    case SPEC_DEV_BAD_TEMP: return "bad inverse temperature";
+    default: break;
+  }
+  return "unknown status bit";
+}
+
 spec_status spec_tree_mask_build(const int32_t* parent, const int32_t* tree_off, int B, int n_max, uint64_t* mask,
                                  int32_t* depth, int32_t* status, void* stream) {
   if (B < 0 || n_max < 0) return SPEC_ERR_INVALID_ARG;
