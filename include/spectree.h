@@ -289,7 +289,8 @@ spec_status spec_kv_commit(void* k_cache, void* v_cache, const int32_t* block_ta
  *   free_pool   int32 [free_cap], free_count int32 [1]: device memory, in/out;
  *               both NULL: commit only, no release
  *   other arguments as in spec_kv_commit.  Two kernels: the commit (grid
- *   B x Hkv x 2*layers), then the release (one CTA).
+ *   B x Hkv x Z, each CTA moving the rows of every Z-th cache, Z chosen to
+ *   fill the GPU about once), then the release (one CTA).
  */
 spec_status spec_kv_commit_layers(void* const* k_caches, void* const* v_caches, int layers,
                                   int32_t* block_table, int max_blocks, int block_size, int num_blocks,
