@@ -504,11 +504,12 @@ __device__ void clear_request(const VerifyArgs& a, int b) {
 // over the whole GPU: for large batches the walk then enters an accepted node
 // with a few shared-memory reads instead of two passes over the node's row.
 // The same contract operations as the walk's own passes, so m and S are
-// bit-identical to what the walk would compute.  256 threads per CTA, so that
-// several rows are resident per SM and one row's loads overlap another's
-// arithmetic; the second pass reads the row again from L2.
+// bit-identical to what the walk would compute.  512 threads per CTA, each
+// issuing batches of four 16-byte loads before using any, so that a few rows
+// are resident per SM and one row's loads overlap another's arithmetic; the
+// second pass reads the row again from L2.
 // ---------------------------------------------------------------------------
-constexpr int kStatsThreads = 256;
+constexpr int kStatsThreads = 512;
 constexpr int kStatsWarps = kStatsThreads / 32;
 
 __global__ void __launch_bounds__(kStatsThreads) row_stats_kernel(VerifyArgs a, RowStats* stats) {
@@ -526,10 +527,17 @@ __global__ void __launch_bounds__(kStatsThreads) row_stats_kernel(VerifyArgs a, 
   const float4* r4 = reinterpret_cast<const float4*>(row);
   float lmax = -INFINITY;
   if (a.vec) {
-#pragma unroll 4
-    for (int j = threadIdx.x; j < (V >> 2); j += kStatsThreads) {
-      const float4 v = __ldg(r4 + j);
-      lmax = fmaxf(lmax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+    constexpr int kB = 4;  // 16-byte loads per thread issued before any is used
+    const int n4 = V >> 2;
+    for (int j0 = threadIdx.x; j0 < n4; j0 += kB * kStatsThreads) {
+      float4 v[kB];
+#pragma unroll
+      for (int q = 0; q < kB; ++q) {
+        const int j = j0 + q * kStatsThreads;
+        v[q] = j < n4 ? __ldg(r4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int q = 0; q < kB; ++q) lmax = fmaxf(lmax, fmaxf(fmaxf(v[q].x, v[q].y), fmaxf(v[q].z, v[q].w)));
     }
   } else {
     for (int j = threadIdx.x; j < V; j += kStatsThreads) lmax = fmaxf(lmax, __ldg(row + j));
@@ -543,13 +551,25 @@ __global__ void __launch_bounds__(kStatsThreads) row_stats_kernel(VerifyArgs a, 
   unsigned long long part;
   if (a.vec) {
     FxSum acc;
-    int it = 0;
-#pragma unroll 4
-    for (int j = threadIdx.x; j < (V >> 2); j += kStatsThreads) {
-      const float4 v = __ldg(r4 + j);
-      fx_add2(acc, canon_exp2(__fmul2_rn(__fadd2_rn(make_float2(v.x, v.y), f2(-m)), tau2)));
-      fx_add2(acc, canon_exp2(__fmul2_rn(__fadd2_rn(make_float2(v.z, v.w), f2(-m)), tau2)));
-      if ((++it & 63) == 0) acc.flush();  // 256 terms: A and B stay below 2^32
+    constexpr int kB = 4;
+    const int n4 = V >> 2;
+    for (int j0 = threadIdx.x; j0 < n4; j0 += kB * kStatsThreads) {
+      float4 v[kB];
+      bool in[kB];
+#pragma unroll
+      for (int q = 0; q < kB; ++q) {
+        const int j = j0 + q * kStatsThreads;
+        in[q] = j < n4;
+        v[q] = in[q] ? __ldg(r4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < kB; ++q) {
+        if (in[q]) {
+          fx_add2(acc, canon_exp2(__fmul2_rn(__fadd2_rn(make_float2(v[q].x, v[q].y), f2(-m)), tau2)));
+          fx_add2(acc, canon_exp2(__fmul2_rn(__fadd2_rn(make_float2(v[q].z, v[q].w), f2(-m)), tau2)));
+        }
+      }
+      acc.flush();  // 16 terms per batch: A and B stay below 2^32
     }
     part = acc.total();
   } else {
