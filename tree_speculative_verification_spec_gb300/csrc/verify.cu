@@ -697,15 +697,15 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         if (vec) {
           const float4* p4 = reinterpret_cast<const float4*>(prow);
           const int n4 = len >> 2;
-          for (int j = threadIdx.x; j < n4; j += 4 * kWalkThreads) {
-            float4 v[4];
+          for (int j = threadIdx.x; j < n4; j += 8 * kWalkThreads) {
+            float4 v[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 8; ++q) {
               const int jj = j + q * kWalkThreads;
               v[q] = jj < n4 ? __ldcg(p4 + jj) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 8; ++q) {
               const int x = x0 + ((j + q * kWalkThreads) << 2);
               if (v[q].x > bv) { bv = v[q].x; bi = x; }
               if (v[q].y > bv) { bv = v[q].y; bi = x + 1; }
