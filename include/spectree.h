@@ -278,7 +278,9 @@ spec_status spec_kv_commit(void* k_cache, void* v_cache, const int32_t* block_ta
  * ceil(new_len / block_size) .. ceil((prefix_len + n_b) / block_size) - 1 are
  * released: their block-table entries become -1 and their ids are appended to
  * free_pool after *free_count, in request order then page order, and
- * *free_count grows by their number.  Requests with a non-zero status after
+ * *free_count grows by their number.  The entries are taken as the table
+ * holds them (call once per pass: a second call over the same tree would
+ * append the -1 entries the first left).  Requests with a non-zero status after
  * the commit keep every page.  When the pool cannot take every page of the
  * call (*free_count + released > free_cap), none is released and each request
  * that had pages to release gets SPEC_DEV_CAPACITY.
