@@ -124,9 +124,14 @@ size_t spec_attention_workspace_size(int B, int T, int n_max, int max_prefix, in
  *   out      [T][Hq][D] dtype   out
  *   workspace   device scratch of spec_attention_workspace_size() bytes
  *   status   int32 [B]          in/out: or-ed with SPEC_DEV_CAPACITY / SPEC_DEV_BAD_BLOCK.
- *                               Requests whose status is non-zero on entry are skipped;
- *                               a flagged request's output rows are unspecified.
+ *                               A flagged request's output rows are unspecified (the
+ *                               CUDA-core path skips requests whose status is non-zero on
+ *                               entry; the tcgen05 path computes them).
  *   flags       SPEC_ATTN_*
+ * The tcgen05 kernel is launched as a programmatic dependent of the previous
+ * kernel in the stream: its set-up and K/V loads may overlap that kernel (the
+ * mask build ends by allowing it), and it reads the mask and the status word,
+ * and writes the status word, only after waiting for that kernel to finish.
  */
 spec_status spec_tree_attention(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int max_blocks, int block_size, int num_blocks,

@@ -315,9 +315,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = a.g;
   const int R = n * g;
   if (n <= 0 || n > a.n_max || mt * BM >= R || off < 0 || off + n > a.T) return;
-  if (*(volatile int32_t*)&a.status[b] != 0) return;
+  // The mask and the status word come from the previous kernel of the pass
+  // (launched as a programmatic dependent, this kernel may start before it
+  // ends): every read of either and every status write follows
+  // griddepcontrol.wait.  Rows of a request with a non-zero status are
+  // unspecified, so its work is not skipped early.
   if (P < 0 || P > a.max_prefix || (long long)P + n > (long long)a.max_blocks * a.block_size) {
-    if (threadIdx.x == 0 && mt == 0 && split == 0 && kvh == 0) atomicOr(&a.status[b], SPEC_DEV_CAPACITY);
+    if (threadIdx.x == 0 && mt == 0 && split == 0 && kvh == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      atomicOr(&a.status[b], SPEC_DEV_CAPACITY);
+    }
     return;
   }
   const int Lk = P + n;
@@ -491,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = mt * BM + r;
       const bool valid = row < R;
       const int t = valid ? off + row / g : off;
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the mask is the previous kernel's output
       const uint64_t* mrow = a.mask + (size_t)t * a.W;
       const float c2 = a.scale_log2;
       const float2 c22 = make_float2(c2, c2);
@@ -694,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // status writes follow the previous kernel's
     if (bad_block) atomicOr(&a.status[b], SPEC_DEV_BAD_BLOCK);
     if (abort_flag) atomicOr(&a.status[b], SPEC_DEV_TIMEOUT);
   }
@@ -794,7 +803,17 @@ static cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int rows_max = a.n_max * a.g;
   dim3 grid((rows_max + tc::BM - 1) / tc::BM, a.splits, a.B * a.Hkv);
-  kern<<<grid, tc::kThreads, dyn, stream>>>(mk, mv, mq, prm);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(tc::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kern, mk, mv, mq, prm);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,9 @@ __global__ void __launch_bounds__(256) mask_build_kernel(const int32_t* __restri
                                                          uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
                                                          int32_t* __restrict__ status) {
   __shared__ int32_t par[SPEC_MAX_NODES];
+  // the next kernel of the pass (attention) may start its set-up now; it
+  // waits for this grid before it reads the mask or the status word
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.x;
   const int off = tree_off[b];
   const int n = tree_off[b + 1] - off;
