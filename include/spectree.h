@@ -130,8 +130,12 @@ size_t spec_attention_workspace_size(int B, int T, int n_max, int max_prefix, in
  *   flags       SPEC_ATTN_*
  * The tcgen05 kernel is launched as a programmatic dependent of the previous
  * kernel in the stream: its set-up and K/V loads may overlap that kernel (the
- * mask build ends by allowing it), and it reads the mask and the status word,
- * and writes the status word, only after waiting for that kernel to finish.
+ * mask build allows this at its start), and it reads the mask and the status
+ * word, and writes the status word, only after waiting for that kernel to
+ * finish.  A kernel that allows programmatic dependents and sits right
+ * before this call must therefore not write q, the caches, block_table,
+ * prefix_len or tree_off; kernels that do not allow it (the usual case) are
+ * waited for in full, as with any launch.
  */
 spec_status spec_tree_attention(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int max_blocks, int block_size, int num_blocks,
