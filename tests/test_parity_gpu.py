@@ -652,6 +652,27 @@ def test_stochastic_with_and_without_row_statistics(tree):
         _assert_verify_equal(got, ref, w.B)
 
 
+def test_workspace_canary_changes_nothing(monkeypatch):
+    """With SPECTREE_WORKSPACE_CANARY=1 every workspace is filled with 0xFF
+    (NaN) before use: split-KV attention (long prefix, several key splits)
+    and stochastic verification with row statistics still equal the oracle,
+    so neither reads scratch it did not write."""
+    monkeypatch.setenv("SPECTREE_WORKSPACE_CANARY", "1")
+    B, nr, pr, Hq, Hkv, D, bs = TC_CASES[4]
+    w = W.small_random(sum(nr) + pr[1] + bs, B=B, n_range=nr, prefix_range=pr, Hq=Hq, Hkv=Hkv, D=D, dtype=W.BF16,
+                       V=16, block_size=bs)
+    d = DeviceBatch.from_workload(w)
+    assert S.spec_attention_workspace_size(d.B, d.T, d.n_max, d.max_prefix, d.Hq, d.Hkv, d.D) > 256  # splits
+    ref, _, _ = oracle_attention(w)
+    got, st = _gpu_attention(w, S.SPEC_ATTN_TCGEN05)
+    ref32 = (ref.astype(np.uint32) << 16).view(np.float32)
+    assert attn_tolerance_ok(got.reshape(ref32.shape), ref32, w.dtype).all() and (st[:w.B] == 0).all()
+    w2 = W.config4(K=6, B=80, tree="random", alpha=0.4, prefix=16)
+    ref2 = oracle_stochastic(w2)
+    got2 = _gpu_verify(w2, "stochastic")  # full workspace: row statistics
+    _assert_verify_equal(got2, ref2, w2.B)
+
+
 # ---------------------------------------------------------------- commit ----
 
 def _oracle_commit(w, ref_v):

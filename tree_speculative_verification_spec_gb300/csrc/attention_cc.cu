@@ -347,6 +347,7 @@ spec_status spec_tree_attention(const void* q, const void* k_cache, const void* 
                                 int max_prefix, int Hq, int Hkv, int D, spec_dtype dtype, float scale, void* out,
                                 void* workspace, size_t workspace_bytes, int32_t* status, uint32_t flags,
                                 void* stream) {
+  SPEC_NVTX_RANGE("spec_tree_attention");
   if (B < 0 || T < 0 || n_max < 0 || max_prefix < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
     return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
@@ -397,6 +398,7 @@ spec_status spec_tree_attention(const void* q, const void* k_cache, const void* 
   a.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t st = (cudaStream_t)stream;
+  if (need > 0) spec_workspace_canary(workspace, need, st);
   cudaError_t e;
   if (plan.use_tc) e = launch_attention_tc(a, st);
   else e = launch_attention_cc(a, dtype, plan.row_tile, st);
@@ -417,6 +419,7 @@ spec_status spec_tree_attention_noalloc(const void* q, const void* k_cache, cons
                                         int B, int T, int n_max, int max_prefix, int Hq, int Hkv, int D,
                                         spec_dtype dtype, float scale, void* out, int32_t* status, uint32_t flags,
                                         void* stream) {
+  SPEC_NVTX_RANGE("spec_tree_attention_noalloc");
   if (B < 0 || T < 0 || n_max < 0 || max_prefix < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
     return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;

@@ -5,6 +5,10 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <stdlib.h>
+
+#include <nvtx3/nvToolsExt.h>
+
 #include "spectree.h"
 
 #define SPEC_MAX_NODES 1024
@@ -47,6 +51,23 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 }  // namespace spectree
 
 // Host helpers.
+
+// An NVTX range around one C-ABI call (named after the call), for profilers
+// that show ranges; without a tool attached the calls cost a few nanoseconds.
+struct SpecNvtxRange {
+  explicit SpecNvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~SpecNvtxRange() { nvtxRangePop(); }
+};
+#define SPEC_NVTX_RANGE(name) SpecNvtxRange spec_nvtx_range_(name)
+
+// Debug switch: with SPECTREE_WORKSPACE_CANARY=1 in the environment, calls
+// that take a workspace first fill it with 0xFF bytes (NaN floats, all-ones
+// integers), so that a read of scratch the call did not write shows up in
+// the results.  Off by default; read at every call.
+inline void spec_workspace_canary(void* ws, size_t bytes, cudaStream_t stream) {
+  const char* e = getenv("SPECTREE_WORKSPACE_CANARY");
+  if (e && e[0] == '1' && ws && bytes) cudaMemsetAsync(ws, 0xFF, bytes, stream);
+}
 #define SPEC_LAUNCH_CHECK()                       \
   do {                                            \
     if (cudaGetLastError() != cudaSuccess)        \

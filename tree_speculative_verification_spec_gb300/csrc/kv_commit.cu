@@ -288,6 +288,7 @@ extern "C" spec_status spec_kv_commit(void* k_cache, void* v_cache, const int32_
                                       int block_size, int num_blocks, const int32_t* prefix_len, const int32_t* path,
                                       int path_stride, const int32_t* accept_len, int B, int Hkv, int D,
                                       spec_dtype dtype, int32_t* new_len, int32_t* status, void* stream) {
+  SPEC_NVTX_RANGE("spec_kv_commit");
   if (B < 0 || Hkv <= 0 || max_blocks <= 0 || num_blocks <= 0 || path_stride <= 0) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
@@ -311,6 +312,7 @@ extern "C" spec_status spec_kv_commit_layers(void* const* k_caches, void* const*
                                              int path_stride, const int32_t* accept_len, int B, int Hkv, int D,
                                              spec_dtype dtype, int32_t* new_len, int32_t* free_pool, int free_cap,
                                              int32_t* free_count, int32_t* status, void* stream) {
+  SPEC_NVTX_RANGE("spec_kv_commit_layers");
   if (B < 0 || layers <= 0 || Hkv <= 0 || max_blocks <= 0 || num_blocks <= 0 || path_stride <= 0 || free_cap < 0)
     return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;

@@ -120,6 +120,7 @@ const char* spec_dev_status_string(int32_t bit) {
 
 spec_status spec_tree_mask_build(const int32_t* parent, const int32_t* tree_off, int B, int n_max, uint64_t* mask,
                                  int32_t* depth, int32_t* status, void* stream) {
+  SPEC_NVTX_RANGE("spec_tree_mask_build");
   if (B < 0 || n_max < 0) return SPEC_ERR_INVALID_ARG;
   if (n_max > SPEC_MAX_NODES) return SPEC_ERR_UNSUPPORTED;
   if (B == 0) return SPEC_OK;
@@ -132,6 +133,7 @@ spec_status spec_tree_mask_build(const int32_t* parent, const int32_t* tree_off,
 
 spec_status spec_philox_uniforms(uint64_t seed, uint32_t round, const int32_t* tree_off, int B, int n_max,
                                  uint32_t* out, void* stream) {
+  SPEC_NVTX_RANGE("spec_philox_uniforms");
   if (B < 0 || n_max < 0) return SPEC_ERR_INVALID_ARG;
   if (B == 0 || n_max == 0) return SPEC_OK;
   if (!tree_off || !out) return SPEC_ERR_INVALID_ARG;

@@ -380,6 +380,7 @@ extern "C" {
 
 spec_status spec_tree_init(const int32_t* root_tok, int B, int n_total, int32_t* tree_off, int32_t* parent,
                            int32_t* tokens, void* stream) {
+  SPEC_NVTX_RANGE("spec_tree_init");
   if (B < 0 || n_total < 1) return SPEC_ERR_INVALID_ARG;
   if (n_total > SPEC_MAX_NODES || (long long)B * n_total >= (1LL << 31)) return SPEC_ERR_UNSUPPORTED;
   if (B == 0 && !tree_off) return SPEC_OK;
@@ -393,6 +394,7 @@ spec_status spec_tree_init(const int32_t* root_tok, int B, int n_total, int32_t*
 
 spec_status spec_tree_expand_level(const float* scores, int B, int F, int V, int k, int level_start, int n_total,
                                    int32_t* parent, int32_t* tokens, void* stream) {
+  SPEC_NVTX_RANGE("spec_tree_expand_level");
   if (B < 0 || F < 0 || V <= 0 || k < 0 || level_start < 0 || n_total < 1) return SPEC_ERR_INVALID_ARG;
   if (k > 32 || k > V || n_total > SPEC_MAX_NODES || (long long)B * n_total >= (1LL << 31))
     return SPEC_ERR_UNSUPPORTED;
@@ -422,6 +424,7 @@ spec_status spec_tree_expand_level(const float* scores, int B, int F, int V, int
 spec_status spec_tree_merge(const int32_t* seqs, const int32_t* lens, const int32_t* root_tok, int B, int M, int m,
                             int V, int32_t* tree_off, int32_t* parent, int32_t* tokens, int32_t* src,
                             int32_t* node_of, int32_t* status, void* stream) {
+  SPEC_NVTX_RANGE("spec_tree_merge");
   if (B < 0 || M < 0 || m < 0 || V <= 0) return SPEC_ERR_INVALID_ARG;
   if (M >= SPEC_MAX_NODES || (long long)M * m >= SPEC_MAX_NODES || V > (1 << 30) ||
       (long long)B * (1 + (long long)M * m) >= (1LL << 31) || B > (1 << 24))

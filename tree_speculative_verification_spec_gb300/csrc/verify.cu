@@ -1227,6 +1227,7 @@ inline int walk_cluster(int B, int V, int mode, bool allow16) {
 template <int MODE>
 spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   if (!workspace || ws_bytes < kVerifyWorkspace) return SPEC_ERR_WORKSPACE;
+  spec_workspace_canary(workspace, ws_bytes, stream);
   int C = walk_cluster(B, a.V, MODE, false);
   if (C == 8 && walk_cluster(B, a.V, MODE, true) == 16) {
     // only when every request's cluster is resident at once: a cluster that
@@ -1282,6 +1283,7 @@ spec_status spec_tree_verify_greedy(const float* p_logits, const int32_t* tokens
                                     const int32_t* tree_off, int B, int n_max, int V, int32_t* path,
                                     int32_t* accept_len, int32_t* emitted, int32_t* n_emitted, void* workspace,
                                     size_t workspace_bytes, int32_t* status, void* stream) {
+  SPEC_NVTX_RANGE("spec_tree_verify_greedy");
   spec_status s = verify_check(B, n_max, V);
   if (s != SPEC_OK) return s;
   if (B == 0 || n_max == 0) return SPEC_OK;
@@ -1307,6 +1309,7 @@ spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_pr
                                         const float* inv_temperature, int q_layout, int B, int n_max, int V,
                                         int32_t* path, int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
                                         void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+  SPEC_NVTX_RANGE("spec_tree_verify_stochastic");
   spec_status s = verify_check(B, n_max, V);
   if (s != SPEC_OK) return s;
   if (q_layout != SPEC_Q_PER_PARENT && q_layout != SPEC_Q_PER_CHILD) return SPEC_ERR_INVALID_ARG;
