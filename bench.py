@@ -263,7 +263,7 @@ def bench_reference(args):
     if rank != 0:
         return 0
     wl = WORKLOADS[args.workload]
-    w = make_workload(args.workload, 0, 0)
+    w = make_workload(args.workload, args.seed, 0)
     times, toks = [], 0
     for i in range(args.warmup + args.steps):
         v, sample, dt = run_cpu_baseline(w, args.mode)
@@ -317,7 +317,7 @@ def bench_gpu(args):
     n_sets = wl["sets"]
     sets, passes, works = [], [], []
     for i in range(n_sets):
-        w = make_workload(args.workload, 97 * rank, i)
+        w = make_workload(args.workload, args.seed + 97 * rank, i)
         works.append(w)
         d = DeviceBatch.from_workload(w, device=dev)
         sets.append(d)
@@ -805,6 +805,7 @@ def main():
     ap.add_argument("--workload", type=int, default=1, choices=sorted(WORKLOADS))
     ap.add_argument("--attn-flags", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0, help="offset added to the workload's input seeds")
     ap.add_argument("--temperature", type=float, default=None,
                     help="stochastic verification at this temperature for every request (default: none, T = 1)")
     ap.add_argument("--q-per-child", action="store_true",
