@@ -523,15 +523,17 @@ def run_e2e(args, works, sets, passes, stream, dev, n_sets):
     import torch
     from tree_speculative_verification_spec_gb300.pipeline import VerifyPass
     steps = max(3, args.steps)
+    # the step's inputs: greedy verification reads neither draft rows nor uniforms
+    names = [k for k in STEP_INPUTS if args.mode != "greedy" or k not in ("q_probs", "uniforms")]
     host = []
     for w in works:
-        host.append({k: getattr(w, k).pin_memory() for k in STEP_INPUTS})
+        host.append({k: getattr(w, k).pin_memory() for k in names})
     # two device slots per input set: the set's own buffers, and a shadow
     # with fresh per-step inputs and the same cache (and a pass of its own)
     slots = []
     for j in range(n_sets):
         d = sets[j]
-        shadow = dataclasses.replace(d, **{k: torch.empty_like(getattr(d, k)) for k in STEP_INPUTS})
+        shadow = dataclasses.replace(d, **{k: torch.empty_like(getattr(d, k)) for k in names})
         vp2 = VerifyPass(shadow)
         vp2.inv_temp, vp2.q_layout = passes[j].inv_temp, passes[j].q_layout
         slots.append([(d, passes[j]), (shadow, vp2)])
