@@ -580,6 +580,8 @@ def run_e2e(args, works, sets, passes, stream, dev, n_sets):
     # inputs are the same at every step, so its last read-back counts for all
     per_slot = {(j, k): int(out_n[j][k].sum()) for j in range(n_sets) for k in range(2)}
     toks = sum(per_slot[jk] for jk in done)
+    # whole job: the slowest rank's time, the tokens of all ranks (copies per rank)
+    ms, toks = aggregate_replicas(ms, float(toks), dev)
     return {"value": toks / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms / steps,
             "overlap": "step i+1's host-to-device copy (copy stream) overlaps step i's pass; two input slots"}
