@@ -582,7 +582,9 @@ def run_e2e(args, works, sets, passes, stream, dev, n_sets):
     toks = sum(per_slot[jk] for jk in done)
     # whole job: the slowest rank's time, the tokens of all ranks (copies per rank)
     ms, toks = aggregate_replicas(ms, float(toks), dev)
-    return {"value": toks / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+    world = _dist()[0]
+    return {"value": toks / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d * world,
+            "d2h_bytes_per_step": d2h * world,
             "ms_per_step": ms / steps,
             "overlap": "step i+1's host-to-device copy (copy stream) overlaps step i's pass; two input slots"}
 
