@@ -16,6 +16,9 @@
  *     Zero-Copy Pruning".
  *   "Inference Optimization Techniques: Speed and Efficiency": the accept rule
  *     and residual of the "Misconception" section, "Traced Example".
+ *   Around the pass: "Token Tree Construction: Expansion vs. Merge" (SpecInfer
+ *     guide) for the tree builders, and "Hardware-aware dynamic speculative
+ *     decoding" (Cohere) for the goodput table and the <tokens, K> graph keys.
  *
  * Conventions shared by every call
  *   - Every pointer argument is DEVICE memory owned by the caller, except where
