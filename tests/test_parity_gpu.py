@@ -315,6 +315,20 @@ def test_per_child_star_with_frozen_residuals(ws):
     _assert_verify_equal(got, ref, B)
 
 
+@pytest.mark.parametrize("which", [1, 2])
+def test_temperature_and_per_child_at_full_size(which):
+    """The decode-layer and ensemble workloads at full size, verified at
+    per-request temperatures and with per-child draft rows: bit-exact."""
+    w = _workload(which)
+    g = np.random.default_rng(which)
+    tau = g.choice(np.array([0.5, 0.8, 1.25, 2.0], np.float32), w.B)
+    for layout in (S.SPEC_Q_PER_PARENT, S.SPEC_Q_PER_CHILD):
+        ref = _oracle_opts(w, tau, layout == S.SPEC_Q_PER_CHILD)
+        got = _gpu_verify_opts(w, tau, layout)
+        _assert_verify_equal(got, ref, w.B)
+        assert (got["status"][:w.B] == 0).all()
+
+
 def test_bad_inverse_temperature_status():
     w = W.small_random(46, B=6, n_range=(2, 9), prefix_range=(0, 1), Hq=2, Hkv=1, D=64, V=1000, block_size=16)
     tau = np.array([0.0, -1.0, np.inf, np.nan, 1.0, 0.5], np.float32)
