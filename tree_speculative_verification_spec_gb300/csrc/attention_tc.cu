@@ -813,8 +813,8 @@ static cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, kern, mk, mv, mq, prm);
-  return cudaGetLastError();
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, mk, mv, mq, prm);
+  return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream) {
