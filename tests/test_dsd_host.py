@@ -91,3 +91,22 @@ def test_dynamic_k_table_selects_the_goodput_optimum():
     for _ in range(40):
         pol.record(0, 0, 1.8, 0.5, weight=0.25)
     assert pol.select(1) == 1
+
+
+def test_chain_prefix_keeps_each_requests_first_nodes():
+    """The dynamic-K profile cuts one set of chains to every K: a chain's
+    first K + 1 nodes, with the rows, tokens and uniforms of those nodes."""
+    import workloads as W
+    full = W.config4(K=4, B=3, tree="chain", alpha=0.3, prefix=32, V=500)
+    for n in (1, 2, 5):
+        w = W.chain_prefix(full, n)
+        assert w.n_max == n and w.tree_off.tolist() == list(range(0, 3 * n + 1, n))
+        assert w.parent.tolist() == ([-1] + list(range(n - 1))) * 3
+        for b in range(3):
+            src = slice(b * 5, b * 5 + n)
+            dst = slice(b * n, b * n + n)
+            assert np.array_equal(w.tokens[dst].numpy(), full.tokens[src].numpy())
+            assert np.array_equal(w.p_logits[dst].numpy(), full.p_logits[src].numpy())
+            assert np.array_equal(w.q_probs[dst].numpy(), full.q_probs[src].numpy())
+            assert np.array_equal(w.uniforms[dst].numpy(), full.uniforms[src].numpy())
+        assert w.k_cache is full.k_cache and w.meta["K"] == n - 1
