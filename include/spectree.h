@@ -163,6 +163,10 @@ spec_status spec_tree_attention(const void* q, const void* k_cache, const void* 
  *   otherwise SPEC_ERR_UNSUPPORTED and nothing is launched.
  *   Set-up: the first call on each device looks up the array's device address
  *   with that device current; make that first call before any stream capture.
+ *   The address is cached per device together with the current context: after
+ *   a reset of the device's primary context (cudaDeviceReset) the next call
+ *   looks it up again, so that call too belongs before any capture.  A failed
+ *   lookup returns SPEC_ERR_CUDA and leaves no pending runtime error.
  *   Sharing: every call uses the same array, which keeps the last call's
  *   contents.  Nothing in it must start at zero (a call writes every partial
  *   it reads back), but calls whose kernels overlap on the GPU race: serialise

@@ -5,10 +5,12 @@ once and must not pay cudaMalloc's device-wide synchronisation).  When the plan
 splits a long key range over several CTAs, the partial outputs of the splits
 go to a fixed scratch array inside the library, shared by every call.
 
-Two calls in a row, on different shapes that both split their keys (so the
+Two calls in a row, on different shapes whose plans split their keys (so the
 scratch really holds partials, and the second call starts from the first
-call's leftovers), must each match spec_tree_attention with a caller-allocated
-workspace within the attention tolerance of the other tests.  This file is
+call's leftovers), must each match the CPU oracle and spec_tree_attention with
+a caller-allocated workspace, within the attention tolerance of the other
+tests.  That the plan these calls take needs scratch is shown by the
+workspace entry point refusing to run without a workspace.  This file is
 collected last and passes alone or after the rest of the suite."""
 import numpy as np
 import pytest
@@ -17,7 +19,7 @@ import torch
 import workloads as W
 import tree_speculative_verification_spec_gb300 as S
 from tree_speculative_verification_spec_gb300.pipeline import DeviceBatch, VerifyPass
-from parity import attn_tolerance_ok
+from parity import attn_tolerance_ok, bf16_bits_to_f32, oracle_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +53,10 @@ def test_noalloc_attention_matches_workspace_attention_on_two_calls_in_a_row():
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
         out_ref, st_ref = torch.full_like(d.q, 7.0), torch.zeros(d.B, dtype=torch.int32, device="cuda")
         out_na, st_na = torch.full_like(d.q, -7.0), torch.zeros(d.B, dtype=torch.int32, device="cuda")
+        # the plan of this call (AUTO, bf16) needs scratch: without a workspace it is refused
+        with pytest.raises(S.SpecError) as e:
+            S.spec_tree_attention(*_args(d, vp.mask), out_ref, None, st_ref)
+        assert e.value.code == S.SPEC_ERR_WORKSPACE
         S.spec_tree_attention(*_args(d, vp.mask), out_ref, ws, st_ref)
         S.spec_tree_attention_noalloc(*_args(d, vp.mask), out_na, st_na)
         torch.cuda.synchronize()
@@ -59,6 +65,11 @@ def test_noalloc_attention_matches_workspace_attention_on_two_calls_in_a_row():
         got = out_na.float().cpu().numpy()
         assert np.isfinite(ref).all()
         assert attn_tolerance_ok(got, ref, w.dtype).all(), float(np.abs(got - ref).max())
+        # and directly against the oracle (fp64 attention rounded to bf16)
+        ora, _, s_ora = oracle_attention(w)
+        assert (s_ora == 0).all()
+        ora32 = bf16_bits_to_f32(ora).reshape(got.shape)
+        assert attn_tolerance_ok(got, ora32, w.dtype).all(), float(np.abs(got - ora32).max())
 
 
 def test_noalloc_attention_rejects_shapes_beyond_its_scratch():

@@ -8,6 +8,8 @@
 // K/V tile staged in shared memory serves every query head of the group.
 // Online softmax in the log2 domain; split-KV partials (unnormalised output,
 // running max, running sum) are merged by attn_combine_kernel.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "attention.cuh"
@@ -302,25 +304,74 @@ size_t attention_ws_bytes(const AttnPlan& p, int T, int Hq, int D) {
 // Scratch of spec_tree_attention_noalloc: one file-scope device array (every
 // GPU that loads the library holds it until the process exits).  In host code
 // the symbol names a host-side stand-in, so kernels get the device address,
-// looked up once per device with that device current.
+// looked up with the device current and cached per device together with the
+// context it was looked up in: after a reset of the device's primary context
+// the next call looks the address up again instead of using a stale one.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_attn_scratch[SPEC_ATTN_NOALLOC_BYTES];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+static CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 static std::mutex g_attn_scratch_mutex;
 static void* g_attn_scratch_ptr[128];
+static CUcontext g_attn_scratch_ctx[128];
 
 // Device address of the scratch array on the current device; NULL when the
-// lookup fails.
+// lookup fails (the runtime's error from the failed lookup is cleared, so a
+// later cudaGetLastError() does not report it).
 static void* attn_scratch() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  CUcontext ctx = nullptr;
+  if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_attn_scratch_mutex);
-  if (!g_attn_scratch_ptr[dev]) {
+  if (!g_attn_scratch_ptr[dev] || !ctx || g_attn_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      g_attn_scratch_ptr[dev] = nullptr;
+      return nullptr;
+    }
+    // the runtime creates the primary context on first use: read it again
+    if (!ctx && get_ctx && get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     g_attn_scratch_ptr[dev] = p;
+    g_attn_scratch_ctx[dev] = ctx;
   }
   return g_attn_scratch_ptr[dev];
+}
+
+// Argument checks shared by both attention entry points, made before the
+// plan is computed (the plan's row and chunk arithmetic assumes them).
+// SPEC_OK when the shape and scalar arguments are acceptable.
+static spec_status attention_shape_check(int B, int T, int n_max, int max_prefix, int Hq, int Hkv, int D,
+                                         spec_dtype dtype, int block_size, uint32_t flags) {
+  if (B < 0 || T < 0 || n_max < 0 || max_prefix < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (flags > SPEC_ATTN_TCGEN05) return SPEC_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
+  if (n_max > SPEC_MAX_NODES || B > 65535) return SPEC_ERR_UNSUPPORTED;
+  if (block_size < 8 || block_size > 65536 || (block_size & (block_size - 1))) return SPEC_ERR_UNSUPPORTED;
+  if (flags == SPEC_ATTN_TCGEN05 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if ((long long)B * Hkv > 65535 * 1024LL) return SPEC_ERR_UNSUPPORTED;
+  return SPEC_OK;
 }
 
 }  // namespace spectree
@@ -348,19 +399,12 @@ spec_status spec_tree_attention(const void* q, const void* k_cache, const void* 
                                 void* workspace, size_t workspace_bytes, int32_t* status, uint32_t flags,
                                 void* stream) {
   SPEC_NVTX_RANGE("spec_tree_attention");
-  if (B < 0 || T < 0 || n_max < 0 || max_prefix < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
-    return SPEC_ERR_INVALID_ARG;
-  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
-  if (flags > SPEC_ATTN_TCGEN05) return SPEC_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
-  if (n_max > SPEC_MAX_NODES || B > 65535) return SPEC_ERR_UNSUPPORTED;
-  if (block_size < 8 || block_size > 65536 || (block_size & (block_size - 1))) return SPEC_ERR_UNSUPPORTED;
-  if (flags == SPEC_ATTN_TCGEN05 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  const spec_status sc = attention_shape_check(B, T, n_max, max_prefix, Hq, Hkv, D, dtype, block_size, flags);
+  if (sc != SPEC_OK) return sc;
   if (B == 0 || T == 0 || n_max == 0) return SPEC_OK;
   if (!q || !k_cache || !v_cache || !block_table || !prefix_len || !tree_off || !mask || !out || !status ||
       max_blocks <= 0 || num_blocks <= 0)
     return SPEC_ERR_INVALID_ARG;
-  if ((long long)B * Hkv > 65535 * 1024LL) return SPEC_ERR_UNSUPPORTED;
 
   const AttnPlan plan = attention_plan(B, n_max, max_prefix, Hq, Hkv, D, dtype == SPEC_BF16, flags);
   const size_t need = attention_ws_bytes(plan, T, Hq, D);
@@ -411,8 +455,9 @@ spec_status spec_tree_attention(const void* q, const void* k_cache, const void* 
 }
 
 // Attention without a workspace argument: the split-KV partials live in the
-// library's fixed scratch array.  The shape checks the plan needs come first;
-// spec_tree_attention then checks everything else and launches.
+// library's fixed scratch array.  The same shape checks as spec_tree_attention
+// come first (the plan assumes them), then the scratch limit; the pointers are
+// checked by spec_tree_attention, which then launches.
 spec_status spec_tree_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                         const int32_t* block_table, int max_blocks, int block_size, int num_blocks,
                                         const int32_t* prefix_len, const int32_t* tree_off, const uint64_t* mask,
@@ -420,11 +465,9 @@ spec_status spec_tree_attention_noalloc(const void* q, const void* k_cache, cons
                                         spec_dtype dtype, float scale, void* out, int32_t* status, uint32_t flags,
                                         void* stream) {
   SPEC_NVTX_RANGE("spec_tree_attention_noalloc");
-  if (B < 0 || T < 0 || n_max < 0 || max_prefix < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
-    return SPEC_ERR_INVALID_ARG;
-  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
-  if (flags > SPEC_ATTN_TCGEN05) return SPEC_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
+  const spec_status sc = attention_shape_check(B, T, n_max, max_prefix, Hq, Hkv, D, dtype, block_size, flags);
+  if (sc != SPEC_OK) return sc;
+  if (B == 0 || T == 0 || n_max == 0) return SPEC_OK;
   const AttnPlan plan = attention_plan(B, n_max, max_prefix, Hq, Hkv, D, dtype == SPEC_BF16, flags);
   const size_t need = attention_ws_bytes(plan, T, Hq, D);
   if (need > (size_t)SPEC_ATTN_NOALLOC_BYTES) return SPEC_ERR_UNSUPPORTED;

@@ -203,6 +203,9 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_layers_kernel(
       }
       __syncthreads();
     }
+    // s_warp, s_src and s_dst are rewritten by the next batch: every thread has
+    // read them (also when this batch moved no row and the copy loop was empty)
+    __syncthreads();
   }
   if (writer && threadIdx.x == 0) new_len[b] = P + a;
 }
