@@ -425,6 +425,38 @@ spec_status spec_dsd_graph_keys(int max_tokens, int max_k, int32_t* tokens_out, 
  */
 spec_status spec_selftest_bounded_wait(int32_t* status, uint32_t polls, void* stream);
 
+/*
+ * Diagnostics of the stochastic verifier's arithmetic contract (no
+ * counterpart on the pages).  They run the very device functions the
+ * verifier uses (the exp E, the fixed-point weight FX and its two
+ * accumulators, the residual step) over arrays, so that a test can compare
+ * them bit for bit with an independent implementation of the contract
+ * described at spec_tree_verify_stochastic.  Device pointers, asynchronous on
+ * `stream`; SPEC_ERR_INVALID_ARG for a negative n, a bad segment or no output.
+ *
+ * spec_selftest_exp: x_i is the fp32 whose bit pattern is first_bits + i
+ *   (modulo 2^32), i < n.  exp_scalar[i] = E(x_i) by the scalar routine;
+ *   exp_pair[i] = E(x_i) by the two-lane routine, entries 2k and 2k+1 forming
+ *   one pair.  Either output may be NULL.
+ * spec_selftest_fx: v float [n] (the contract's domain is [0, 2)).
+ *   fx_out[i] = trunc(v[i] * 2^46); for each of the n / seg segments of seg
+ *   consecutive entries (1 <= seg <= 510, n a multiple of seg), seg_scalar[s]
+ *   = the fixed-point sum of the segment by the scalar accumulator and
+ *   seg_pair[s] = the same by the two-lane accumulator (seg even).  Any
+ *   output may be NULL (not all three).
+ * spec_selftest_resid: one residual step max(d / Z - q, 0) of the contract
+ *   per entry i < n, with Z = Zp[i / 2] (Zp holds ceil(n / 2) normalisers;
+ *   entries 2k and 2k+1 share one, as in the verifier's paired passes):
+ *   r_div by IEEE division, r_markstein by the scalar Markstein sequence the
+ *   residual passes use (y = RN(1/Z)), r_pair by its two-lane form.  Any
+ *   output may be NULL (not all three).
+ */
+spec_status spec_selftest_exp(uint32_t first_bits, long long n, float* exp_scalar, float* exp_pair, void* stream);
+spec_status spec_selftest_fx(const float* v, long long n, int seg, uint64_t* fx_out, uint64_t* seg_scalar,
+                             uint64_t* seg_pair, void* stream);
+spec_status spec_selftest_resid(const float* d, const float* q, const float* Zp, long long n, float* r_div,
+                                float* r_markstein, float* r_pair, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

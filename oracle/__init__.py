@@ -46,7 +46,9 @@ Pins (in tests/test_oracle_pins.py, all ``-m "not gpu"``):
     order, the emitted tokens follow p (Monte Carlo), and children whose
     rows copy their parent's reproduce the per-parent mode exactly;
   * canonical exp: <= 2 ulp from libm's fp64 exp;
-  * FX sums: equal to exact integer sums;
+  * FX sums: equal to exact integer sums; the array form equals the scalar;
+  * one residual step: the correctly rounded quotient d / Z, then the
+    correctly rounded difference with q, clamped at zero (exact rationals);
   * commit: invariants against a snapshot gather;
   * expansion: the page's schedule <3, 2, 1, 1> gives levels of 3, 6, 6, 6
     nodes; children are the top-k of their row in numpy's lexicographic
@@ -95,6 +97,8 @@ def lib():
         L.oracle_canon_exp.argtypes = [ctypes.c_float]
         L.oracle_canon_exp.restype = ctypes.c_float
         L.oracle_canon_exp_array.argtypes = [P, P, i64]
+        L.oracle_fx_array.argtypes = [P, P, i64]
+        L.oracle_resid_step_array.argtypes = [P, P, P, P, i64]
         L.oracle_fx.argtypes = [ctypes.c_float]
         L.oracle_fx.restype = u64
         L.oracle_f64_to_bf16.argtypes = [f64]
@@ -321,6 +325,23 @@ def canon_exp(x):
 
 def fx(v):
     return int(lib().oracle_fx(ctypes.c_float(v)))
+
+
+def fx_array(v):
+    """C3 weights trunc(v * 2^46) of a float32 array, as uint64."""
+    v = _c(v, np.float32)
+    out = np.empty(v.shape, np.uint64)
+    lib().oracle_fx_array(_p(v), _p(out), v.size)
+    return out
+
+
+def resid_step(d, q, Zp):
+    """One C5 residual step per entry: max(d / Z - q, 0), Z = Zp[i // 2]."""
+    d, q, Zp = _c(d, np.float32), _c(q, np.float32), _c(Zp, np.float32)
+    assert d.shape == q.shape and Zp.size >= (d.size + 1) // 2
+    out = np.empty_like(d)
+    lib().oracle_resid_step_array(_p(d), _p(q), _p(Zp), _p(out), d.size)
+    return out
 
 
 def f64_to_bf16_bits(x):

@@ -856,6 +856,24 @@ void oracle_canon_exp_array(const float *x, float *y, int64_t n)
     for (int64_t i = 0; i < n; i++) y[i] = oracle_canon_exp(x[i]);
 }
 
+/* Array helpers for the contract's pins: C3's weight of every entry, and one
+ * C5 residual step per entry as row_reject takes it (the previous target
+ * r = d / Z, then max(r - q, 0)), with Z = Zp[i / 2]: two neighbouring
+ * entries share one normaliser. */
+void oracle_fx_array(const float *v, uint64_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_fx(v[i]);
+}
+
+void oracle_resid_step_array(const float *d, const float *q, const float *Zp, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) {
+        float r = d[i] / Zp[i / 2];
+        float diff = r - q[i];
+        out[i] = diff > 0.0f ? diff : 0.0f;
+    }
+}
+
 
 /* ------------------------------------------------------------------ */
 /* Dynamic draft length (goodput tables)                               */

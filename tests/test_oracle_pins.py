@@ -694,6 +694,45 @@ def test_fx_is_exact_truncation():
     for v in vals:
         v32 = float(np.float32(v))
         assert o.fx(v32) == math.floor(Fraction(v32) * 2 ** 46)
+    arr = np.array(vals + [np.float32(2 ** -126), np.float32(1.4e-45)], np.float32)
+    got = o.fx_array(arr)
+    assert got.dtype == np.uint64
+    assert [int(x) for x in got] == [math.floor(Fraction(float(v)) * 2 ** 46) for v in arr]
+
+
+def _is_rn_f32(x, exact):
+    """x (fp32) is the round-to-nearest-even fp32 value of the rational `exact`."""
+    x = np.float32(x)
+    lo, hi = np.nextafter(x, np.float32(-np.inf)), np.nextafter(x, np.float32(np.inf))
+    e = abs(Fraction(float(x)) - exact)
+    for y in (lo, hi):
+        ey = abs(Fraction(float(y)) - exact)
+        if ey < e or (ey == e and int(np.float32(y).view(np.uint32)) % 2 == 0):
+            return False
+    return True
+
+
+def test_residual_step_is_rounded_quotient_then_rounded_difference():
+    """C5 one entry: r = RN(d / Z), then RN(r - q) clamped at zero, checked
+    against exact rationals (Z of the form fp32(S) * 2^-46 as the sums make
+    them, d and q probabilities, zeros)."""
+    import oracle as o
+    rng = np.random.default_rng(7)
+    n = 3000
+    d = (rng.random(n) ** 6).astype(np.float32)
+    d[::17] = 0.0
+    q = (rng.random(n) ** 3).astype(np.float32)
+    S = rng.integers(1, 2 ** 62, size=(n + 1) // 2, dtype=np.int64) >> rng.integers(0, 60, size=(n + 1) // 2)
+    Zp = (np.maximum(S, 1).astype(np.float32) * np.float32(2.0 ** -46)).astype(np.float32)
+    got = o.resid_step(d, q, Zp)
+    for i in range(n):
+        Z = Fraction(float(Zp[i // 2]))
+        r = np.float32(d[i]) / np.float32(Zp[i // 2])
+        assert _is_rn_f32(r, Fraction(float(d[i])) / Z)
+        diff = np.float32(r) - np.float32(q[i])
+        assert _is_rn_f32(diff, Fraction(float(r)) - Fraction(float(q[i])))
+        want = diff if diff > 0 else np.float32(0.0)
+        assert got[i].view(np.uint32) == np.float32(want).view(np.uint32), i
 
 
 # --------------------------------------------------------------- commit ----

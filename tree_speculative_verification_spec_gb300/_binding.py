@@ -47,6 +47,9 @@ SIGNATURES = {
                               _I),
     "spec_philox_uniforms": ([_U64, _U32, _P, _I, _I, _P, _P], _I),
     "spec_selftest_bounded_wait": ([_P, _U32, _P], _I),
+    "spec_selftest_exp": ([_U32, ctypes.c_longlong, _P, _P, _P], _I),
+    "spec_selftest_fx": ([_P, ctypes.c_longlong, _I, _P, _P, _P, _P], _I),
+    "spec_selftest_resid": ([_P, _P, _P, ctypes.c_longlong, _P, _P, _P, _P], _I),
 }
 
 _lib = None
@@ -263,3 +266,21 @@ def spec_philox_uniforms(seed, round_, tree_off, B, n_max, out, stream=None):
 def spec_selftest_bounded_wait(status, polls, stream=None):
     _check("spec_selftest_bounded_wait", lib().spec_selftest_bounded_wait(_ptr(status), ctypes.c_uint32(polls),
                                                                             _stream(stream)))
+
+
+def spec_selftest_exp(first_bits, n, exp_scalar=None, exp_pair=None, stream=None):
+    """exp_scalar / exp_pair: float32 CUDA tensors of n entries (or None)."""
+    _check("spec_selftest_exp", lib().spec_selftest_exp(ctypes.c_uint32(first_bits), n, _ptr(exp_scalar),
+                                                        _ptr(exp_pair), _stream(stream)))
+
+
+def spec_selftest_fx(v, seg, fx_out=None, seg_scalar=None, seg_pair=None, stream=None):
+    """v: float32 CUDA tensor; outputs: int64 CUDA tensors (raw uint64 bits) or None."""
+    _check("spec_selftest_fx", lib().spec_selftest_fx(_ptr(v), v.numel(), seg, _ptr(fx_out), _ptr(seg_scalar),
+                                                      _ptr(seg_pair), _stream(stream)))
+
+
+def spec_selftest_resid(d, q, Zp, r_div=None, r_markstein=None, r_pair=None, stream=None):
+    """d, q: float32 CUDA tensors of n entries; Zp: ceil(n / 2) normalisers."""
+    _check("spec_selftest_resid", lib().spec_selftest_resid(_ptr(d), _ptr(q), _ptr(Zp), d.numel(), _ptr(r_div),
+                                                            _ptr(r_markstein), _ptr(r_pair), _stream(stream)))

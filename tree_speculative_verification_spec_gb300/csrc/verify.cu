@@ -1261,6 +1261,97 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Diagnostics of the arithmetic contract: the device functions above, run over
+// arrays, so that a test can compare them bit for bit with an independent
+// implementation of the same contract.  Grid-stride loops; nothing else of the
+// verifier is involved.
+// ---------------------------------------------------------------------------
+constexpr int kSelftestThreads = 256;
+
+// x_i = the fp32 with bit pattern first_bits + i; pairs (2k, 2k+1) go through
+// the two-lane routine together.
+__global__ void __launch_bounds__(kSelftestThreads)
+    selftest_exp_kernel(uint32_t first_bits, long long n, float* __restrict__ e_scalar, float* __restrict__ e_pair) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; 2 * k < n; k += stride) {
+    const long long i = 2 * k;
+    const bool two = i + 1 < n;
+    const float x0 = __uint_as_float(first_bits + (uint32_t)i);
+    const float x1 = __uint_as_float(first_bits + (uint32_t)(i + 1));
+    if (e_scalar) {
+      e_scalar[i] = canon_exp(x0);
+      if (two) e_scalar[i + 1] = canon_exp(x1);
+    }
+    if (e_pair) {
+      const float2 e = canon_exp2(make_float2(x0, x1));
+      e_pair[i] = e.x;
+      if (two) e_pair[i + 1] = e.y;
+    }
+  }
+}
+
+// fx of every entry; per segment of `seg` entries the fixed-point sum by the
+// scalar accumulator and (seg even) by the two-lane accumulator.
+__global__ void __launch_bounds__(kSelftestThreads)
+    selftest_fx_kernel(const float* __restrict__ v, long long n, int seg, unsigned long long* __restrict__ fx_out,
+                       unsigned long long* __restrict__ seg_scalar, unsigned long long* __restrict__ seg_pair) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (fx_out)
+    for (long long i = tid; i < n; i += stride) fx_out[i] = fx(v[i]);
+  const long long nseg = n / seg;
+  for (long long sgi = tid; sgi < nseg; sgi += stride) {
+    const float* w = v + sgi * seg;
+    if (seg_scalar) {
+      FxSum acc;
+      for (int j = 0; j < seg; ++j) acc.add(w[j]);
+      seg_scalar[sgi] = acc.total();
+    }
+    if (seg_pair) {
+      FxSum acc;
+      for (int j = 0; j + 1 < seg; j += 2) fx_add2(acc, make_float2(w[j], w[j + 1]));
+      seg_pair[sgi] = acc.total();
+    }
+  }
+}
+
+// One residual step max(d / Z - q, 0) per entry: by the IEEE division, by
+// Markstein's sequence (scalar) and by the two-lane sequence; entries 2k and
+// 2k+1 share the normaliser Zp[k].
+__global__ void __launch_bounds__(kSelftestThreads)
+    selftest_resid_kernel(const float* __restrict__ d, const float* __restrict__ q, const float* __restrict__ Zp,
+                          long long n, float* __restrict__ r_div, float* __restrict__ r_mk,
+                          float* __restrict__ r_pair) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; 2 * k < n; k += stride) {
+    const long long i = 2 * k;
+    const bool two = i + 1 < n;
+    const float Z = Zp[k];
+    const float y = __frcp_rn(Z);
+    const float d0 = d[i], q0 = q[i];
+    const float d1 = two ? d[i + 1] : 0.0f, q1 = two ? q[i + 1] : 0.0f;
+    if (r_div) {
+      r_div[i] = resid(d0, Z, q0);
+      if (two) r_div[i + 1] = resid(d1, Z, q1);
+    }
+    if (r_mk) {
+      r_mk[i] = resid_y(d0, Z, y, q0);
+      if (two) r_mk[i + 1] = resid_y(d1, Z, y, q1);
+    }
+    if (r_pair) {
+      const float2 r = resid_y2(make_float2(d0, d1), Z, y, make_float2(q0, q1));
+      r_pair[i] = r.x;
+      if (two) r_pair[i + 1] = r.y;
+    }
+  }
+}
+
+inline unsigned selftest_grid(long long items) {
+  const long long b = (items + kSelftestThreads - 1) / kSelftestThreads;
+  return (unsigned)std::max(1LL, std::min(b, 152LL * 16));
+}
+
 }  // namespace spectree
 
 using namespace spectree;
@@ -1336,5 +1427,33 @@ spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_pr
   return verify_dispatch<1>(a, B, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
+spec_status spec_selftest_exp(uint32_t first_bits, long long n, float* exp_scalar, float* exp_pair, void* stream) {
+  if (n < 0 || (n > 0 && !exp_scalar && !exp_pair)) return SPEC_ERR_INVALID_ARG;
+  if (n == 0) return SPEC_OK;
+  selftest_exp_kernel<<<selftest_grid((n + 1) / 2), kSelftestThreads, 0, (cudaStream_t)stream>>>(
+      first_bits, n, exp_scalar, exp_pair);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_selftest_fx(const float* v, long long n, int seg, uint64_t* fx_out, uint64_t* seg_scalar,
+                             uint64_t* seg_pair, void* stream) {
+  if (n < 0 || seg < 1 || seg > 510 || (seg_pair && (seg & 1)) || n % seg != 0) return SPEC_ERR_INVALID_ARG;
+  if (n == 0) return SPEC_OK;
+  if (!v || (!fx_out && !seg_scalar && !seg_pair)) return SPEC_ERR_INVALID_ARG;
+  selftest_fx_kernel<<<selftest_grid(n), kSelftestThreads, 0, (cudaStream_t)stream>>>(
+      v, n, seg, reinterpret_cast<unsigned long long*>(fx_out), reinterpret_cast<unsigned long long*>(seg_scalar),
+      reinterpret_cast<unsigned long long*>(seg_pair));
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_selftest_resid(const float* d, const float* q, const float* Zp, long long n, float* r_div,
+                                float* r_markstein, float* r_pair, void* stream) {
+  if (n < 0) return SPEC_ERR_INVALID_ARG;
+  if (n == 0) return SPEC_OK;
+  if (!d || !q || !Zp || (!r_div && !r_markstein && !r_pair)) return SPEC_ERR_INVALID_ARG;
+  selftest_resid_kernel<<<selftest_grid((n + 1) / 2), kSelftestThreads, 0, (cudaStream_t)stream>>>(
+      d, q, Zp, n, r_div, r_markstein, r_pair);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
 
 }  // extern "C"
