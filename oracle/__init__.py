@@ -15,6 +15,8 @@ What each function follows (page title, section):
                          the accept / residual rule of "Inference Optimization
                          Techniques: Speed and Efficiency" (the
                          "Misconception" section and its traced example)
+  * kv_append         -- SpecInfer guide, "Depth-First Flattening and KV Cache
+                         Reuse" (tree K/V appended after the prefix)
   * kv_commit         -- SpecInfer guide, "Depth-First Flattening and KV Cache
                          Reuse" and "PagedKV Allocation with Zero-Copy Pruning"
   * tree_expand_level / tree_expand -- SpecInfer guide, "Method A:
@@ -49,6 +51,10 @@ Pins (in tests/test_oracle_pins.py, all ``-m "not gpu"``):
   * FX sums: equal to exact integer sums; the array form equals the scalar;
   * one residual step: the correctly rounded quotient d / Z, then the
     correctly rounded difference with q, clamped at zero (exact rationals);
+  * append: attention over the appended cache equals causal attention over
+    prefix + root path with the tree K/V taken straight from the caller's
+    rows; with one contiguous page the tree rows are a plain slice; nothing
+    else changes; bad requests are untouched;
   * commit: invariants against a snapshot gather;
   * expansion: the page's schedule <3, 2, 1, 1> gives levels of 3, 6, 6, 6
     nodes; children are the top-k of their row in numpy's lexicographic
@@ -84,6 +90,7 @@ def lib():
         L.oracle_verify_greedy.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P]
         L.oracle_verify_stochastic.argtypes = [P, P, P, P, P, P, i32, i32, i32, P, i32, P, P, P, P, P]
         L.oracle_kv_commit.argtypes = [P, P, i64, P, i32, i32, i32, P, P, i32, P, i32, i32, i32, i32, P, P]
+        L.oracle_kv_append.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, i32, i32, i32, i32, i32, P]
         L.oracle_kv_release.argtypes = [P, i32, i32, P, P, P, P, i32, P, i32, P]
         L.oracle_tree_expand_level.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P]
         L.oracle_tree_merge.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P]
@@ -195,6 +202,24 @@ def kv_commit(k_cache, v_cache, block_table, block_size, prefix_len, path, accep
                            _p(prefix_len), _p(path), path.shape[1], _p(accept_len), B, Hkv, D, dtype,
                            _p(new_len), _p(st))
     return k_new, v_new, new_len, st
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, block_table, block_size, prefix_len, tree_off, n_max, Hkv, D, dtype,
+              status):
+    """Tree K/V rows [T][Hkv][D] appended after each request's prefix.
+    Returns (k_cache_new, v_cache_new, status_out); the inputs are not modified."""
+    edt = np.float32 if dtype == F32 else np.uint16
+    k_out = np.array(k_cache, dtype=edt, copy=True, order="C")
+    v_out = np.array(v_cache, dtype=edt, copy=True, order="C")
+    k_new, v_new = _c(k_new, edt), _c(v_new, edt)
+    block_table, prefix_len, tree_off = _c(block_table, np.int32), _c(prefix_len, np.int32), _c(tree_off, np.int32)
+    st = np.array(status, dtype=np.int32, copy=True)
+    B = len(prefix_len)
+    assert k_new.size == v_new.size == int(tree_off[-1]) * Hkv * D
+    num_blocks = k_out.size // (Hkv * block_size * D)
+    lib().oracle_kv_append(_p(k_new), _p(v_new), _p(k_out), _p(v_out), _p(block_table), block_table.shape[1],
+                           block_size, num_blocks, _p(prefix_len), _p(tree_off), B, n_max, Hkv, D, dtype, _p(st))
+    return k_out, v_out, st
 
 
 def kv_release(block_table, block_size, prefix_len, tree_off, new_len, status, free_cap, free_count=0):

@@ -643,6 +643,55 @@ int oracle_kv_commit(void *k_cache, void *v_cache, int64_t cache_elems,
     return 0;
 }
 
+/* [SpecInfer guide] "Depth-First Flattening and KV Cache Reuse", step 1 of
+ * the verification pass: every tree token appends its computed key and
+ * value to the request's active cache, in the tree's flattened node order,
+ * right after the committed prefix.  Row h of node u of request b
+ * (k_new[tree_off[b] + u][h][0..D-1], likewise v_new) is written to slot
+ * P_b + u of kv-head h.  A request whose n_b lies outside [0, n_max] gets
+ * ORC_BAD_TREE; one whose prefix is negative or whose last tree slot lies
+ * beyond its block table gets ORC_CAPACITY; one whose pages covering
+ * [P_b, P_b + n_b) include an id outside [0, num_blocks) gets ORC_BAD_BLOCK.
+ * Such requests are left untouched.  status[b] is or-ed; nothing else of
+ * the cache changes. */
+int oracle_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                     const int32_t *block_table, int max_blocks, int block_size, int num_blocks,
+                     const int32_t *prefix_len, const int32_t *tree_off, int B, int n_max, int Hkv, int D,
+                     int dtype, int32_t *status)
+{
+    size_t es = dtype == ORC_F32 ? 4 : 2;
+    for (int b = 0; b < B; b++) {
+        int off = tree_off[b], n = tree_off[b + 1] - off, P = prefix_len[b];
+        if (n < 0 || n > n_max) {
+            status[b] |= ORC_BAD_TREE;
+            continue;
+        }
+        if (P < 0 || (long long)P + n > (long long)max_blocks * block_size) {
+            status[b] |= ORC_CAPACITY;
+            continue;
+        }
+        if (n == 0) continue;
+        const int32_t *bt_row = block_table + (size_t)b * max_blocks;
+        int bad = 0;
+        for (int s = P; s < P + n; s++) {
+            int blk = bt_row[s / block_size];
+            bad |= blk < 0 || blk >= num_blocks;
+        }
+        if (bad) {
+            status[b] |= ORC_BAD_BLOCK;
+            continue;
+        }
+        for (int u = 0; u < n; u++)
+            for (int h = 0; h < Hkv; h++) {
+                size_t dst = cache_index(bt_row, block_size, Hkv, D, h, P + u, 0);
+                size_t src = ((size_t)(off + u) * Hkv + h) * D;
+                memcpy((unsigned char *)k_cache + dst * es, (const unsigned char *)k_new + src * es, (size_t)D * es);
+                memcpy((unsigned char *)v_cache + dst * es, (const unsigned char *)v_new + src * es, (size_t)D * es);
+            }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------ */
 /* Multi-layer commit and page release                                 */
 /* "SpecInfer Guide", "PagedKV Allocation with Zero-Copy Pruning": the  */

@@ -737,6 +737,121 @@ def test_residual_step_is_rounded_quotient_then_rounded_difference():
 
 # --------------------------------------------------------------- commit ----
 
+def _elems(t, dtype):
+    return t.numpy() if dtype == W.F32 else t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _as_f64(a, dtype):
+    return a.astype(np.float64) if dtype == W.F32 else (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_append_then_attention_is_causal_attention_over_callers_rows(oracle, dtype):
+    """[SpecInfer guide] "Depth-First Flattening and KV Cache Reuse": the tree
+    tokens' keys and values are appended to the active cache after the
+    prefix, in node order.  After the append (over a cache whose tree slots
+    held garbage), the oracle's attention must equal causal attention over
+    prefix + root path where the prefix K/V come from the cache and the tree
+    K/V straight from the caller's [T][Hkv][D] rows (independent fp64)."""
+    w = W.small_random(21, B=3, n_range=(1, 11), prefix_range=(0, 30), Hq=4, Hkv=2, D=16, dtype=dtype, block_size=8)
+    g = np.random.default_rng(5)
+    tdt = w.torch_dtype
+    k_new = torch.from_numpy(g.standard_normal((w.T, w.Hkv, w.D))).to(tdt)
+    v_new = torch.from_numpy(g.standard_normal((w.T, w.Hkv, w.D))).to(tdt)
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    bt, bs = w.block_table.numpy(), w.block_size
+    for b in range(w.B):  # garbage in the tree slots
+        P, n = int(w.prefix_len[b]), int(w.tree_off[b + 1] - w.tree_off[b])
+        for s_ in range(P, P + n):
+            kc[bt[b, s_ // bs], :, s_ % bs] = 1e3
+            vc[bt[b, s_ // bs], :, s_ % bs] = -1e3
+    k_out, v_out, st = oracle.kv_append(_elems(k_new, dtype), _elems(v_new, dtype), _elems(kc, dtype),
+                                        _elems(vc, dtype), bt, bs, w.prefix_len.numpy(), w.tree_off.numpy(), w.n_max,
+                                        w.Hkv, w.D, dtype, np.zeros(w.B, np.int32))
+    assert st.tolist() == [0] * w.B
+    _, out64, status = oracle.tree_attention(_elems(w.q, dtype), k_out, v_out, bt, bs, w.prefix_len.numpy(),
+                                             w.tree_off.numpy(), w.parent.numpy(), w.n_max, w.Hq, w.Hkv, w.D, dtype,
+                                             w.scale, want_f64=True)
+    assert status.tolist() == [0] * w.B
+    kpre, vpre = kc.double().numpy(), vc.double().numpy()
+    kt, vt = k_new.double().numpy(), v_new.double().numpy()
+    q = w.q.double().numpy()
+    grp = w.Hq // w.Hkv
+    for b in range(w.B):
+        off, n, P = int(w.tree_off[b]), int(w.tree_off[b + 1] - w.tree_off[b]), int(w.prefix_len[b])
+        par = w.parent[off:off + n].numpy()
+        for u in range(n):
+            path, c = [], u
+            while c != -1:
+                path.append(c)
+                c = par[c]
+            path.reverse()
+            for h in range(w.Hq):
+                kvh = h // grp
+                Kp = np.array([kpre[bt[b, s_ // bs], kvh, s_ % bs] for s_ in range(P)]).reshape(P, w.D)
+                Vp = np.array([vpre[bt[b, s_ // bs], kvh, s_ % bs] for s_ in range(P)]).reshape(P, w.D)
+                K = np.concatenate([Kp, kt[off + np.array(path), kvh]])
+                V = np.concatenate([Vp, vt[off + np.array(path), kvh]])
+                sc = K @ q[off + u, h] * w.scale
+                p = np.exp(sc - sc.max())
+                np.testing.assert_allclose(out64[off + u, h], (p / p.sum()) @ V, rtol=0, atol=1e-12)
+
+
+def test_append_into_one_page_per_request_is_a_plain_slice(oracle):
+    """With one page per request (page b holds request b's slots), the tree
+    rows of kv-head h are exactly cache[b, h, P:P+n] and nothing else moves."""
+    B, Hkv, D, bs = 3, 2, 8, 64
+    g = np.random.default_rng(8)
+    n = np.array([5, 0, 17])
+    tree_off = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    P = np.array([10, 3, 47], np.int32)
+    T = int(tree_off[-1])
+    kc = g.standard_normal((B, Hkv, bs, D)).astype(np.float32)
+    vc = g.standard_normal((B, Hkv, bs, D)).astype(np.float32)
+    k_new = g.standard_normal((T, Hkv, D)).astype(np.float32)
+    v_new = g.standard_normal((T, Hkv, D)).astype(np.float32)
+    bt = np.arange(B, dtype=np.int32).reshape(B, 1)
+    k_out, v_out, st = oracle.kv_append(k_new, v_new, kc, vc, bt, bs, P, tree_off, 32, Hkv, D, W.F32,
+                                        np.zeros(B, np.int32))
+    assert st.tolist() == [0, 0, 0]
+    k_ref, v_ref = kc.copy(), vc.copy()
+    for b in range(B):
+        for h in range(Hkv):
+            k_ref[b, h, P[b]:P[b] + n[b]] = k_new[tree_off[b]:tree_off[b + 1], h]
+            v_ref[b, h, P[b]:P[b] + n[b]] = v_new[tree_off[b]:tree_off[b + 1], h]
+    assert np.array_equal(k_out, k_ref) and np.array_equal(v_out, v_ref)
+
+
+def test_append_keeps_other_slots_and_rejects_bad_requests(oracle):
+    w = W.small_random(22, B=5, n_range=(1, 9), prefix_range=(0, 40), Hq=4, Hkv=2, D=8, dtype=W.BF16, block_size=8)
+    g = np.random.default_rng(9)
+    k_new = g.integers(0, 2 ** 16, size=(w.T, w.Hkv, w.D), dtype=np.uint16)
+    v_new = g.integers(0, 2 ** 16, size=(w.T, w.Hkv, w.D), dtype=np.uint16)
+    bt = w.block_table.numpy().copy()
+    P = w.prefix_len.numpy().copy()
+    tree_off = w.tree_off.numpy()
+    P[1] = bt.shape[1] * 8 - int(tree_off[2] - tree_off[1]) + 1  # last tree slot past the table
+    bt[2, P[2] // 8] = w.num_blocks + 4                           # a bad id among the tree's pages
+    st_in = np.zeros(w.B, np.int32)
+    k0, v0 = _elems(w.k_cache, W.BF16), _elems(w.v_cache, W.BF16)
+    k_out, v_out, st = oracle.kv_append(k_new, v_new, k0, v0, bt, 8, P, tree_off, w.n_max, w.Hkv, w.D, W.BF16,
+                                        st_in)
+    assert st[1] == oracle.ST_CAPACITY and st[2] == oracle.ST_BAD_BLOCK and st[0] == st[3] == st[4] == 0
+    written = np.zeros(k0.shape[:3], bool)  # [block][head][row]
+    for b in (0, 3, 4):
+        for u in range(int(tree_off[b + 1] - tree_off[b])):
+            s_ = int(P[b]) + u
+            written[bt[b, s_ // 8], :, s_ % 8] = True
+            for h in range(w.Hkv):
+                assert np.array_equal(k_out[bt[b, s_ // 8], h, s_ % 8], k_new[tree_off[b] + u, h])
+                assert np.array_equal(v_out[bt[b, s_ // 8], h, s_ % 8], v_new[tree_off[b] + u, h])
+    assert np.array_equal(k_out[~written], k0[~written]) and np.array_equal(v_out[~written], v0[~written])
+    # a tree larger than n_max is flagged and nothing is written
+    _, _, st2 = oracle.kv_append(k_new, v_new, k0, v0, w.block_table.numpy(), 8, w.prefix_len.numpy(), tree_off, 1,
+                                 w.Hkv, w.D, W.BF16, np.zeros(w.B, np.int32))
+    assert all((st2[b] == oracle.ST_BAD_TREE) == (tree_off[b + 1] - tree_off[b] > 1) for b in range(w.B))
+
+
 def test_commit_moves_path_rows_and_keeps_the_rest(oracle):
     rng = np.random.default_rng(3)
     w = W.small_random(31, B=4, n_range=(3, 20), prefix_range=(0, 50), Hq=4, Hkv=2, D=8, dtype=W.BF16, block_size=4)
