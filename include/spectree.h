@@ -134,11 +134,14 @@ size_t spec_attention_workspace_size(int B, int T, int n_max, int max_prefix, in
  * The tcgen05 kernel is launched as a programmatic dependent of the previous
  * kernel in the stream: its set-up and K/V loads may overlap that kernel (the
  * mask build allows this at its start), and it reads the mask and the status
- * word, and writes the status word, only after waiting for that kernel to
- * finish.  A kernel that allows programmatic dependents and sits right
- * before this call must therefore not write q, the caches, block_table,
- * prefix_len or tree_off; kernels that do not allow it (the usual case) are
- * waited for in full, as with any launch.
+ * word, writes the status word, and loads any key tile that reaches the
+ * tree's own slots (prefix_len[b] and on) only after waiting for that kernel
+ * to finish; the grid does not complete before that kernel.  The tree K/V
+ * rows may therefore be written by the kernel right before this call
+ * (spec_kv_append).  A kernel that allows programmatic dependents and sits
+ * right before this call must not write q, the prefix slots of the caches,
+ * block_table, prefix_len or tree_off; kernels that do not allow it (the
+ * usual case) are waited for in full, as with any launch.
  */
 spec_status spec_tree_attention(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int max_blocks, int block_size, int num_blocks,
@@ -263,6 +266,34 @@ spec_status spec_tree_verify_stochastic(const float* p_logits, const float* q_pr
                                         const float* inv_temperature, int q_layout, int B, int n_max, int V,
                                         int32_t* path, int32_t* accept_len, int32_t* emitted, int32_t* n_emitted,
                                         void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Tree K/V append.  "SpecInfer Guide", "Depth-First Flattening and KV Cache
+ * Reuse", step 1 of the verification pass: every tree token appends the key
+ * and value the target model computed for it to the active cache, in the
+ * tree's node order, right after the committed prefix.  Row h of node u of
+ * request b, k_new[tree_off[b] + u][h][0..D-1] (likewise v_new), is written
+ * to slot prefix_len[b] + u of kv-head h through the block table; no other
+ * slot changes.  This is how the tree K/V reach the slots that
+ * spec_tree_attention reads.
+ *   k_new, v_new  [T][Hkv][D] dtype, T = tree_off[B]; 16-byte aligned, as are the caches
+ *                 (else SPEC_ERR_INVALID_ARG)
+ *   k_cache, v_cache, block_table, max_blocks, block_size, num_blocks  as for attention
+ *   prefix_len, tree_off  int32 [B], [B+1]
+ *   status   int32 [B] in/out, or-ed with SPEC_DEV_BAD_TREE (n_b outside [0, n_max]),
+ *            SPEC_DEV_CAPACITY (prefix_len < 0, or prefix_len + n_b beyond the block table)
+ *            or SPEC_DEV_BAD_BLOCK (an id outside [0, num_blocks) among the pages of slots
+ *            [prefix_len, prefix_len + n_b)); such a request is left untouched.  The
+ *            incoming status is not read: an upstream failure does not stop the append.
+ * Launched as a programmatic dependent of the previous kernel (the mask build
+ * allows it at its start): the copies may overlap that kernel, which must not
+ * write k_new, v_new or the tree slots; the status update and the end of the
+ * grid wait for it.  One launch, grid (B, parts).
+ */
+spec_status spec_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           const int32_t* block_table, int max_blocks, int block_size, int num_blocks,
+                           const int32_t* prefix_len, const int32_t* tree_off, int B, int n_max, int Hkv, int D,
+                           spec_dtype dtype, int32_t* status, void* stream);
 
 /*
  * KV commit / rollback.  "SpecInfer Guide", "Depth-First Flattening and KV

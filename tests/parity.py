@@ -72,15 +72,17 @@ def host_workers():
     return max(1, min(16, os.cpu_count() or 1))
 
 
-def oracle_attention_rows(w, rows, workers=None):
+def oracle_attention_rows(w, rows, workers=None, caches=None):
     """Oracle attention of the flat rows t * Hq + h listed in `rows` (sorted
     int64), computed in parallel: returns (out [len(rows)][D] in the oracle's
-    element type, status[B])."""
+    element type, status[B]).  caches: (k, v) oracle element arrays to use
+    instead of the workload's own."""
     import multiprocessing as mp
     import tempfile
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     workers = workers or host_workers()
-    arrays = dict(q=np_elems(w.q, w.dtype), k_cache=np_elems(w.k_cache, w.dtype), v_cache=np_elems(w.v_cache, w.dtype),
+    kc, vc = caches if caches is not None else (np_elems(w.k_cache, w.dtype), np_elems(w.v_cache, w.dtype))
+    arrays = dict(q=np_elems(w.q, w.dtype), k_cache=kc, v_cache=vc,
                   block_table=w.block_table.numpy(), prefix_len=w.prefix_len.numpy(), tree_off=w.tree_off.numpy(),
                   parent=w.parent.numpy())
     meta = dict(block_size=w.block_size, n_max=w.n_max, Hq=w.Hq, Hkv=w.Hkv, D=w.D, dtype=w.dtype, scale=w.scale)

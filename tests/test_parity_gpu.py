@@ -695,6 +695,89 @@ def test_workspace_canary_changes_nothing(monkeypatch):
     _assert_verify_equal(got2, ref2, w2.B)
 
 
+# ---------------------------------------------------------------- append ----
+
+def _oracle_append(w, k_new, v_new, status=None):
+    st = np.zeros(w.B, np.int32) if status is None else status
+    return O.kv_append(np_elems(k_new, w.dtype), np_elems(v_new, w.dtype), np_elems(w.k_cache, w.dtype),
+                       np_elems(w.v_cache, w.dtype), w.block_table.numpy(), w.block_size, w.prefix_len.numpy(),
+                       w.tree_off.numpy(), w.n_max, w.Hkv, w.D, w.dtype, st)
+
+
+@pytest.mark.parametrize("dtype,D,bs", [(W.BF16, 128, 16), (W.F32, 64, 8), (W.BF16, 64, 256), (W.F32, 128, 512)])
+def test_kv_append_parity(dtype, D, bs):
+    """Tree K/V rows into slots prefix + u, byte-exact against the oracle:
+    ragged and empty trees, a request past its block table, a bad block id
+    among a tree's pages."""
+    w = W.small_random(40 + bs, B=7, n_range=(0, 70), prefix_range=(0, 600), Hq=8, Hkv=2, D=D, dtype=dtype,
+                       block_size=bs, n_max=80)
+    k_new, v_new = W.tree_kv_rows(w, bs)
+    n = (w.tree_off[1:] - w.tree_off[:-1]).numpy()
+    big = [b for b in range(w.B) if n[b] > 0]
+    w.prefix_len[big[0]] = w.block_table.shape[1] * bs - int(n[big[0]]) + 1  # last tree slot past the table
+    b2 = big[1]
+    w.block_table[b2, (int(w.prefix_len[b2]) + int(n[b2]) - 1) // bs] = w.num_blocks + 3
+    k_ref, v_ref, st_ref = _oracle_append(w, k_new, v_new)
+    assert st_ref[big[0]] == O.ST_CAPACITY and st_ref[b2] == O.ST_BAD_BLOCK
+    d = DeviceBatch.from_workload(w)
+    vp = VerifyPass(d)
+    vp.status.zero_()
+    vp.append(k_new.cuda(), v_new.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(vp.status.cpu().numpy()[:w.B], st_ref)
+    assert np.array_equal(np_elems(d.k_cache, w.dtype), k_ref)
+    assert np.array_equal(np_elems(d.v_cache, w.dtype), v_ref)
+
+
+def test_kv_append_rejects_oversized_trees_and_bad_arguments():
+    w = W.small_random(47, B=3, n_range=(3, 9), prefix_range=(0, 40), Hq=4, Hkv=2, D=64, dtype=W.BF16, block_size=16)
+    k_new, v_new = W.tree_kv_rows(w, 1)
+    d = DeviceBatch.from_workload(w)
+    vp = VerifyPass(d)
+    vp.status.zero_()
+    k0 = d.k_cache.clone()
+    S.spec_kv_append(k_new.cuda(), v_new.cuda(), d.k_cache, d.v_cache, d.block_table, d.max_blocks, d.block_size,
+                     d.num_blocks, d.prefix_len, d.tree_off, d.B, 2, d.Hkv, d.D, vp.status)  # n_max 2 < n_b
+    torch.cuda.synchronize()
+    assert (vp.status.cpu().numpy()[:w.B] == S.SPEC_DEV_BAD_TREE).all()
+    assert torch.equal(d.k_cache, k0)
+    with pytest.raises(S.SpecError) as e:  # unaligned rows
+        S.spec_kv_append(k_new.cuda().view(-1)[1:1 + k_new.numel() - 8].view(-1), v_new.cuda(), d.k_cache, d.v_cache,
+                         d.block_table, d.max_blocks, d.block_size, d.num_blocks, d.prefix_len, d.tree_off, d.B,
+                         d.n_max, d.Hkv, d.D, vp.status)
+    assert e.value.code == S.SPEC_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("case", [TC_CASES[1], TC_CASES[4], TC_CASES[7]], ids=["paged16", "splits", "padded"])
+def test_mask_append_attention_chain(case):
+    """mask build -> append -> attention, each launched right after the other
+    (the append and the tensor-core attention start before their predecessor
+    ends): over a cache whose tree slots hold garbage, attention must see the
+    appended rows, as the oracle's append followed by its attention does."""
+    B, nr, pr, Hq, Hkv, D, bs = case
+    w = W.small_random(sum(nr) + pr[1] + bs + 7, B=B, n_range=nr, prefix_range=pr, Hq=Hq, Hkv=Hkv, D=D,
+                       dtype=W.BF16, V=16, block_size=bs)
+    k_new, v_new = W.tree_kv_rows(w, 77)
+    k_ref, v_ref, _ = _oracle_append(w, k_new, v_new)
+    ref, _, s_ref = O.tree_attention(np_elems(w.q, w.dtype), k_ref, v_ref, w.block_table.numpy(), w.block_size,
+                                     w.prefix_len.numpy(), w.tree_off.numpy(), w.parent.numpy(), w.n_max, w.Hq,
+                                     w.Hkv, w.D, w.dtype, w.scale)
+    d = DeviceBatch.from_workload(w)  # caches as generated: the tree slots hold other values
+    vp = VerifyPass(d)
+    kn, vn = k_new.cuda(), v_new.cuda()
+    torch.cuda.synchronize()
+    vp.mask_build()
+    vp.append(kn, vn)
+    vp.attention()
+    torch.cuda.synchronize()
+    assert (vp.status.cpu().numpy()[:w.B] == 0).all() and (s_ref == 0).all()
+    ref32 = bf16_bits_to_f32(ref).reshape(-1, w.D)
+    got = out_as_f32(vp.out, w.dtype).reshape(-1, w.D)
+    bad = ~attn_tolerance_ok(got, ref32, w.dtype)
+    assert not bad.any(), (int(bad.sum()), float(np.abs(got - ref32).max()))
+    assert np.array_equal(np_elems(d.k_cache, w.dtype), k_ref) and np.array_equal(np_elems(d.v_cache, w.dtype), v_ref)
+
+
 # ---------------------------------------------------------------- commit ----
 
 def _oracle_commit(w, ref_v):
@@ -870,6 +953,39 @@ def test_full_pass_workload3_greedy_then_commit():
     assert (ref_v["accept_len"] > 1).sum() > 0
     got = out_as_f32(vp.out, w.dtype).reshape(-1, w.D)[rows]
     assert attn_tolerance_ok(got, bf16_bits_to_f32(ref_a), w.dtype).all()
+    assert np.array_equal(np_elems(vp.batch.k_cache, w.dtype), k_ref)
+    assert np.array_equal(np_elems(vp.batch.v_cache, w.dtype), v_ref)
+    assert np.array_equal(vp.new_len.cpu().numpy(), nl_ref)
+    assert np.array_equal(vp.status.cpu().numpy()[:w.B], st_ref)
+
+
+def test_full_pass_workload3_with_tree_kv_append():
+    """The batched-serving pass starting from tree K/V handed over by the
+    caller: mask, append, attention, greedy verification, commit.  The caches
+    after the append and after the commit are byte-exact, verification exact,
+    attention on the first and last node of every request on every kv-head."""
+    w = _workload(3)
+    k_new, v_new = W.tree_kv_rows(w, 303)
+    k_app, v_app, st_app = _oracle_append(w, k_new, v_new)
+    assert (st_app == 0).all()
+    rows = rows_covering(w, 1024, 34)
+    ref_a, _ = oracle_attention_rows(w, rows, caches=(k_app, v_app))
+    ref_v = oracle_greedy(w)
+    k_ref, v_ref, nl_ref, st_ref = O.kv_commit(k_app, v_app, w.block_table.numpy(), w.block_size,
+                                               w.prefix_len.numpy(), ref_v["path"], ref_v["accept_len"], w.Hkv, w.D,
+                                               w.dtype, np.zeros(w.B, np.int32))
+    del k_app, v_app
+    vp = _pass(w)
+    vp.mask_build()
+    vp.append(k_new.cuda(), v_new.cuda())
+    vp.attention()
+    got = out_as_f32(vp.out, w.dtype).reshape(-1, w.D)[rows]  # synchronises
+    vp.verify("greedy")
+    vp.commit()
+    torch.cuda.synchronize()
+    assert attn_tolerance_ok(got, bf16_bits_to_f32(ref_a), w.dtype).all()
+    for k in ("path", "accept_len", "emitted", "n_emitted"):
+        assert np.array_equal(getattr(vp, k).cpu().numpy(), ref_v[k]), k
     assert np.array_equal(np_elems(vp.batch.k_cache, w.dtype), k_ref)
     assert np.array_equal(np_elems(vp.batch.v_cache, w.dtype), v_ref)
     assert np.array_equal(vp.new_len.cpu().numpy(), nl_ref)

@@ -42,6 +42,7 @@ SIGNATURES = {
     "spec_dsd_update": ([_P, _P, _I, _I, _I, _I, ctypes.c_double, ctypes.c_double, ctypes.c_double], _I),
     "spec_dsd_graph_keys": ([_I, _I, _P, _P, _I, _P], _I),
     "spec_tree_verify_stochastic": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P], _I),
+    "spec_kv_append": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "spec_kv_commit": ([_P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _P], _I),
     "spec_kv_commit_layers": ([_P, _P, _I, _P, _I, _I, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P],
                               _I),
@@ -235,6 +236,17 @@ def spec_dsd_graph_keys(max_tokens, max_k):
     _check("spec_dsd_graph_keys", lib().spec_dsd_graph_keys(max_tokens, max_k, _hptr(t, np.int32),
                                                             _hptr(k, np.int32), n, _hptr(cnt, np.int32)))
     return list(zip(t[:n].tolist(), k[:n].tolist()))
+
+
+def spec_kv_append(k_new, v_new, k_cache, v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len,
+                   tree_off, B, n_max, Hkv, D, status, stream=None):
+    """k_new / v_new: [T][Hkv][D] CUDA tensors of the caches' dtype."""
+    if k_new.dtype != k_cache.dtype or v_new.dtype != k_cache.dtype:
+        raise ValueError("k_new / v_new must have the caches' dtype")
+    _check("spec_kv_append", lib().spec_kv_append(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_blocks, block_size,
+        num_blocks, _ptr(prefix_len), _ptr(tree_off), B, n_max, Hkv, D, _dtype_code(k_cache), _ptr(status),
+        _stream(stream)))
 
 
 def spec_kv_commit(k_cache, v_cache, block_table, max_blocks, block_size, num_blocks, prefix_len, path, path_stride,

@@ -231,20 +231,28 @@ __device__ __forceinline__ int kv_box_row(const TcParams& prm, const int32_t* bt
 // between a stage becoming free and its copy going out.
 template <int D, int NST>
 __device__ __forceinline__ void produce_ring(uint32_t ring, const CUtensorMap* map, const TcParams& prm, int b, int kvh,
-                                             int k_begin, int Lk, int ntiles, uint64_t* full, uint64_t* empty,
-                                             int* bad_block, volatile int* abort_flag) {
+                                             int k_begin, int Lk, int tree_lo, int ntiles, uint64_t* full,
+                                             uint64_t* empty, int* bad_block, volatile int* abort_flag) {
   const AttnArgs& a = prm.a;
   const int lane = threadIdx.x & 31;
   const int br = prm.box_rows, nb = BN / br;  // boxes per tile (1 .. 16)
   const int32_t* bt = a.block_table + (size_t)b * a.max_blocks;
   int y_next = lane < nb ? kv_box_row(prm, bt, kvh, k_begin + lane * br, Lk, bad_block) : 0;
   int issued = 0;
+  bool waited = false;
   for (int j = 0; j < ntiles; ++j) {
     const int st = j % NST;
     const int y = y_next;
     if (j + 1 < ntiles && lane < nb) y_next = kv_box_row(prm, bt, kvh, k_begin + (j + 1) * BN + lane * br, Lk, bad_block);
     bool go = true;
     if (lane == 0 && j >= NST) go = mbar_wait(&empty[st], (j / NST - 1) & 1, abort_flag);
+    // The tree's own K/V rows (slots from the prefix length on) may come from
+    // the previous kernel of the stream (the tree K/V append): a tile that
+    // reaches them is loaded only after that kernel has finished.
+    if (!waited && k_begin + (j + 1) * BN > tree_lo) {
+      if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
+    }
     go = __shfl_sync(0xffffffffu, go, 0);
     if (!go) break;
     if (lane == 0) mbar_expect_tx(&full[st], Layout<D>::kKV);
@@ -314,7 +322,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int P = a.prefix_len[b];
   const int g = a.g;
   const int R = n * g;
-  if (n <= 0 || n > a.n_max || mt * BM >= R || off < 0 || off + n > a.T) return;
+  // The grid never completes before the previous kernel of the stream (its
+  // programmatic predecessor): the first CTA waits for it on every early
+  // exit (the others wait on their normal path), so kernels after this one
+  // find that kernel's results too.
+  const bool first_cta = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  auto leave_early = [&]() {
+    if (first_cta && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  };
+  if (n <= 0 || n > a.n_max || mt * BM >= R || off < 0 || off + n > a.T) {
+    leave_early();
+    return;
+  }
   // The mask and the status word come from the previous kernel of the pass
   // (launched as a programmatic dependent, this kernel may start before it
   // ends): every read of either and every status write follows
@@ -325,12 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("griddepcontrol.wait;" ::: "memory");
       atomicOr(&a.status[b], SPEC_DEV_CAPACITY);
     }
+    leave_early();
     return;
   }
   const int Lk = P + n;
   const int k_begin = split * a.chunk;
   const int k_end = min(Lk, k_begin + a.chunk);
-  if (k_begin >= k_end) return;
+  if (k_begin >= k_end) {
+    leave_early();
+    return;
+  }
   const int ntiles = (k_end - k_begin + BN - 1) / BN;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -384,12 +407,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
     }
-    produce_ring<D, KST>(sbase + L_::kOffK, &tmap_k, prm, b, kvh, k_begin, Lk, ntiles, k_full, k_empty, &bad_block,
+    produce_ring<D, KST>(sbase + L_::kOffK, &tmap_k, prm, b, kvh, k_begin, Lk, P, ntiles, k_full, k_empty, &bad_block,
                          &abort_flag);
     if (lane == 0 && prm.q_tma) mbar_wait(&q_full, 0, &abort_flag);  // the Q copy has landed before any exit
   } else if (warp == 2) {
     // ---------------------------------------------------------- V producer
-    produce_ring<D, VST>(sbase + L_::kOffV, &tmap_v, prm, b, kvh, k_begin, Lk, ntiles, v_full, v_empty, &bad_block,
+    produce_ring<D, VST>(sbase + L_::kOffV, &tmap_v, prm, b, kvh, k_begin, Lk, P, ntiles, v_full, v_empty, &bad_block,
                          &abort_flag);
   } else if (warp == 1) {
     // --------------------------------------------------------- QK issuer

@@ -283,6 +283,62 @@ __global__ void __launch_bounds__(kReleaseThreads) kv_release_kernel(
   if (threadIdx.x == 0) *free_count = (int32_t)base;
 }
 
+// "SpecInfer Guide", "Depth-First Flattening and KV Cache Reuse", step 1 of
+// the verification pass: the tree tokens' keys and values are appended to
+// the active cache in node order after the prefix.  Row h of node u of
+// request b (k_new[tree_off[b] + u][h], likewise v_new) goes to slot
+// prefix_len[b] + u of kv-head h.  Grid (request, part): the parts of one
+// request stride over its (node, head, 16-byte vector) triples, K and V in
+// the same pass.  Every CTA checks its whole request first, so a bad request
+// is left untouched by all of them.  The kernel may start before the previous
+// kernel of the stream ends (programmatic dependent of the mask build): its
+// copies read nothing that kernel writes, and its end waits for it.
+constexpr int kAppendThreads = 256;
+__global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, char* __restrict__ k_cache,
+    char* __restrict__ v_cache, const int32_t* __restrict__ block_table, int max_blocks, int bs, int num_blocks,
+    const int32_t* __restrict__ prefix_len, const int32_t* __restrict__ tree_off, int n_max, int Hkv, int row_bytes,
+    int32_t* __restrict__ status) {
+  const int b = blockIdx.x;
+  const int off = tree_off[b];
+  const int n = tree_off[b + 1] - off;
+  const int P = prefix_len[b];
+  int bad = 0;
+  if (n < 0 || n > n_max) bad = SPEC_DEV_BAD_TREE;
+  else if (P < 0 || (long long)P + n > (long long)max_blocks * bs) bad = SPEC_DEV_CAPACITY;
+  const int32_t* bt = block_table + (size_t)b * max_blocks;
+  if (!bad && n > 0) {
+    int bb = 0;
+    for (int pg = P / bs + threadIdx.x; pg <= (P + n - 1) / bs; pg += blockDim.x) bb |= bt[pg] < 0 || bt[pg] >= num_blocks;
+    if (__syncthreads_or(bb)) bad = SPEC_DEV_BAD_BLOCK;
+  }
+  if (!bad && n > 0) {
+    const int vpr = row_bytes / 16;
+    const long long per = (long long)n * Hkv * vpr;  // vectors of K (and of V)
+    const long long step = (long long)gridDim.y * blockDim.x;
+    for (long long j = (long long)blockIdx.y * blockDim.x + threadIdx.x; j < per; j += step) {
+      const int u = (int)(j / ((long long)Hkv * vpr));
+      const int rem = (int)(j - (long long)u * Hkv * vpr);
+      const int h = rem / vpr, c = rem - h * vpr;
+      const int s = P + u;
+      const long long dst = (((long long)bt[s / bs] * Hkv + h) * bs + s % bs) * row_bytes + c * 16;
+      const long long src = ((long long)(off + u) * Hkv + h) * vpr + c;
+      const uint4 kv = __ldg(k_new + src), vv = __ldg(v_new + src);
+      *reinterpret_cast<uint4*>(k_cache + dst) = kv;
+      *reinterpret_cast<uint4*>(v_cache + dst) = vv;
+    }
+  }
+  // Every CTA waits for the previous kernel before it exits, so this grid
+  // completes only after that kernel has: a kernel launched after this one
+  // (tree attention, which waits for its own predecessor before it reads the
+  // mask) then also finds the mask build's results.  The status update
+  // follows the mask build, which writes the status word.
+  if (threadIdx.x == 0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (bad && blockIdx.y == 0) atomicOr(&status[b], bad);
+  }
+}
+
 }  // namespace spectree
 
 using namespace spectree;
@@ -347,5 +403,42 @@ extern "C" spec_status spec_kv_commit_layers(void* const* k_caches, void* const*
         status);
     SPEC_LAUNCH_CHECK();
   }
+  return SPEC_OK;
+}
+
+extern "C" spec_status spec_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                      const int32_t* block_table, int max_blocks, int block_size, int num_blocks,
+                                      const int32_t* prefix_len, const int32_t* tree_off, int B, int n_max, int Hkv,
+                                      int D, spec_dtype dtype, int32_t* status, void* stream) {
+  SPEC_NVTX_RANGE("spec_kv_append");
+  if (B < 0 || n_max < 0 || Hkv <= 0 || max_blocks <= 0 || num_blocks <= 0) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return SPEC_ERR_UNSUPPORTED;
+  if (block_size < 8 || block_size > 65536 || (block_size & (block_size - 1))) return SPEC_ERR_UNSUPPORTED;
+  if (n_max > SPEC_MAX_NODES || B > 65535 || Hkv > 65535) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0 || n_max == 0) return SPEC_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !prefix_len || !tree_off || !status)
+    return SPEC_ERR_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+        reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15) != 0)
+    return SPEC_ERR_INVALID_ARG;
+  const int row_bytes = D * (dtype == SPEC_F32 ? 4 : 2);
+  // about four CTAs' worth of 16-byte vectors per thread at the largest tree
+  const long long per_req = (long long)n_max * Hkv * (row_bytes / 16);
+  const int parts = (int)std::max(1LL, std::min(65535LL, (per_req + 4LL * kAppendThreads - 1) / (4LL * kAppendThreads)));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B, parts, 1);
+  cfg.blockDim = dim3(kAppendThreads, 1, 1);
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<const uint4*>(k_new),
+                                           static_cast<const uint4*>(v_new), static_cast<char*>(k_cache),
+                                           static_cast<char*>(v_cache), block_table, max_blocks, block_size,
+                                           num_blocks, prefix_len, tree_off, n_max, Hkv, row_bytes, status);
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }

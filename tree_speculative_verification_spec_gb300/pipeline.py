@@ -2,8 +2,8 @@
 
 VerifyPass owns the device outputs and workspaces of one batch shape and
 enqueues, on one stream and with no host synchronisation:
-  spec_tree_mask_build -> spec_tree_attention -> spec_tree_verify_{greedy,
-  stochastic} -> spec_kv_commit.
+  spec_tree_mask_build -> [spec_kv_append] -> spec_tree_attention ->
+  spec_tree_verify_{greedy, stochastic} -> spec_kv_commit.
 Allocation happens once, in the constructor; run() only launches.
 """
 from dataclasses import dataclass
@@ -86,6 +86,12 @@ class VerifyPass:
         b = self.batch
         S.spec_tree_mask_build(b.parent, b.tree_off, b.B, b.n_max, self.mask, self.depth, self.status, stream)
 
+    def append(self, k_new, v_new, stream=None):
+        """Tree K/V rows [T][Hkv][D] into slots prefix_len + u (before attention)."""
+        b = self.batch
+        S.spec_kv_append(k_new, v_new, b.k_cache, b.v_cache, b.block_table, b.max_blocks, b.block_size,
+                         b.num_blocks, b.prefix_len, b.tree_off, b.B, b.n_max, b.Hkv, b.D, self.status, stream)
+
     def attention(self, flags=S.SPEC_ATTN_AUTO, stream=None):
         b = self.batch
         S.spec_tree_attention(b.q, b.k_cache, b.v_cache, b.block_table, b.max_blocks, b.block_size, b.num_blocks,
@@ -110,8 +116,12 @@ class VerifyPass:
                          b.prefix_len, self.path, b.n_max, self.accept_len, b.B, b.Hkv, b.D, self.new_len,
                          self.status, stream)
 
-    def run(self, mode="stochastic", attn_flags=S.SPEC_ATTN_AUTO, commit=True, stream=None):
+    def run(self, mode="stochastic", attn_flags=S.SPEC_ATTN_AUTO, commit=True, stream=None, tree_kv=None):
+        """tree_kv: (k_new, v_new) rows appended before attention, or None when
+        the tree K/V are already in the cache."""
         self.mask_build(stream)
+        if tree_kv is not None:
+            self.append(*tree_kv, stream=stream)
         self.attention(attn_flags, stream)
         self.verify(mode, stream)
         if commit:

@@ -421,6 +421,15 @@ def make_config(i, **kw):
     return [config0, config1, config2, config3, config4][i](**kw)
 
 
+def tree_kv_rows(w, seed):
+    """Keys and values of the tree tokens as the target model would hand them
+    over: [T][Hkv][D] ~ N(0, 1) in the workload's dtype, one pair per seed."""
+    g = _rng(seed)
+    k = _normal(g, (w.T, w.Hkv, w.D), 1.0, w.torch_dtype)
+    v = _normal(g, (w.T, w.Hkv, w.D), 1.0, w.torch_dtype)
+    return k, v
+
+
 def small_random(seed, B=3, n_range=(1, 40), prefix_range=(0, 300), Hq=8, Hkv=2, D=64, dtype=BF16, V=97,
                  block_size=16, n_max=None):
     """Small ragged case for parity tests: several tiles, ragged tails."""
