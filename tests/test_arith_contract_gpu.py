@@ -16,9 +16,9 @@ verifier's own device code) and every result is compared:
   * one residual step max(d / Z - q, 0) by IEEE division and by the
     Markstein sequences (scalar and two-lane) on 16.7M random entries of the
     verifier's domain (d in [0, 1], Z = fp32(S) * 2^-46).
-The device outputs are compared with the oracle on the host; where a second
-device output must equal a first one already compared, the equality is
-checked on the device (bitwise), which keeps the copies to one per chunk."""
+The device outputs are compared with the oracle on the host (for FX, the two
+accumulators are compared on the device with the FX values already checked
+against the oracle, which keeps the copies to one per chunk)."""
 import ctypes
 from concurrent.futures import ThreadPoolExecutor
 
@@ -72,16 +72,16 @@ def _exp_range(first, count):
         es = torch.empty(n, dtype=torch.float32, device="cuda")
         ep = torch.empty(n, dtype=torch.float32, device="cuda")
         S.spec_selftest_exp(start, n, es, ep)
-        # the two-lane routine equals the scalar one, bit for bit (on the device)
-        assert torch.equal(es.view(torch.int32), ep.view(torch.int32)), start
-        got = es.cpu().numpy().view(np.uint32)
         if start + n <= 1 << 32:
             bits = np.arange(start, start + n, dtype=np.uint32)
         else:  # the patterns wrap modulo 2^32
             bits = (np.arange(n, dtype=np.uint64) + np.uint64(start)).astype(np.uint32)
         ref = _oracle_parallel(O.canon_exp, bits.view(np.float32), out_dtype=np.float32).view(np.uint32)
-        bad = np.flatnonzero(got != ref)
-        assert bad.size == 0, [(hex(int(bits[i])), hex(int(got[i])), hex(int(ref[i]))) for i in bad[:5]]
+        for name, t in (("scalar", es), ("two-lane", ep)):
+            got = t.cpu().numpy().view(np.uint32)
+            bad = np.flatnonzero(got != ref)
+            assert bad.size == 0, (name, int(bad.size), [(hex(int(bits[i])), float(bits[i:i + 1].view(np.float32)[0]),
+                                                         hex(int(got[i])), hex(int(ref[i]))) for i in bad[:6]])
         done += n
 
 

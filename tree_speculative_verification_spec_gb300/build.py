@@ -22,6 +22,10 @@ LIB = os.path.join(PKG, "libspectree.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", INCLUDE, "-I", CSRC]
+# The verifier's arithmetic must be bit-reproducible: no multiply and add is
+# ever contracted into a fused multiply-add there (its fused operations are
+# explicit), and division and denormals stay IEEE.
+FILE_FLAGS = {"verify.cu": ["--fmad=false", "-prec-div=true", "-ftz=false"]}
 
 
 def _nvcc():
@@ -59,7 +63,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *FILE_FLAGS.get(os.path.basename(src), []), "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -150,9 +150,13 @@ __device__ __forceinline__ float resid_y(float d, float Z, float y, float q) {
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 __device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
 
+// The rint step takes scalar operations: a paired multiply whose only use is a
+// paired add can be fused into one f32x2 fused multiply-add (rint of the
+// unrounded product, which differs where the rounded product x log2 e is a
+// half-integer), while the scalar _rn operations are never fused.
 __device__ __forceinline__ float2 canon_exp2(float2 x) {
-  const float2 t = __fmul2_rn(x, f2(0x1.715476p+0f));
-  const float2 big = __fadd2_rn(t, f2(12582912.0f));
+  const float2 big = make_float2(__fadd_rn(__fmul_rn(x.x, 0x1.715476p+0f), 12582912.0f),
+                                 __fadd_rn(__fmul_rn(x.y, 0x1.715476p+0f), 12582912.0f));
   const float2 n = __fadd2_rn(big, f2(-12582912.0f));
   const int nx = __float_as_int(big.x) - 0x4B400000, ny = __float_as_int(big.y) - 0x4B400000;
   const float2 nn = neg2(n);
