@@ -1,13 +1,18 @@
-"""Benchmark: one tree-verification pass per step on the Llama-style decode
-layer workload (B=8, 32/8 heads, D=128, bf16, prefix 2048, 64-node expansion
-trees, V=32000, stochastic verification, then KV commit).
+"""Benchmark: one tree-verification pass per step.  The default workload is
+batched serving (B=64, 32/8 heads, D=128, bf16, 16-token pages with a random
+block table, prefixes U[256, 16384], trees of U[8, 64] nodes, V=32000, greedy
+verification, then KV commit), the largest single-GPU configuration and the
+one whose attention is bound by HBM.
 
-A step = spec_tree_mask_build + spec_tree_attention + spec_tree_verify_stochastic
-+ spec_kv_commit over one batch whose inputs are already in HBM.  Three input
-sets rotate between steps (each ~205 MB, together far above the 129 MB L2),
-so every step reads its inputs from DRAM.
+A step = spec_tree_mask_build + spec_tree_attention + spec_tree_verify_{greedy,
+stochastic} + spec_kv_commit over one batch whose inputs are already in HBM
+(the tree K/V resident in their slots).  Inputs larger than L2 (one 2.2 GB
+set for batched serving; three rotating ~205 MB sets for the decode layer and
+the ensemble) make every step read from DRAM.  The e2e figure adds, every
+step, the host-to-device copy of the step's inputs including the tree K/V
+rows, their spec_kv_append, and the read-back of the emitted tokens.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload 1|2|3|4]
 
 Prints one JSON line.  Metric: tree-verify tokens/s = tokens emitted by the
 verifier per second of pass time.  For N > 1 (torchrun) every rank runs an
@@ -26,8 +31,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tree-verify tokens/s"
 UNIT = "tokens/s"
-# --workload: 1 is the default line; the others give the same contract line for
-# the wide-ensemble tree, the batched-serving and one linear-vs-tree sweep point
+# --workload: 3 (batched serving) is the default line; the others give the same
+# contract line for the decode layer, the wide-ensemble tree and one
+# linear-vs-tree sweep point
 WORKLOADS = {
     1: dict(desc="Llama-style decode layer: B=8, 32 query / 8 KV heads, head_dim 128, bf16, prefix 2048, 64-node "
                  "expansion trees (4,2,2,1,1,1,1,1) per request, V=32000, stochastic verification, KV commit",
@@ -211,13 +217,25 @@ class ClockSampler:
                 except (ValueError, IndexError):
                     continue
 
+    def mark_timed_end(self):
+        """Record where the timed region's samples end (the sampler keeps going)."""
+        self.timed_n = len(self.samples)
+
     def summary(self):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         reasons = sorted({name for _, _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
-        return {"sm_mhz": statistics.median(x[0] for x in self.samples),
-                "sm_max_mhz": max(x[1] for x in self.samples), "reasons": reasons, "samples": len(self.samples),
-                "source": "nvml" if self.thread is not None else "nvidia-smi"}
+        out = {"sm_mhz": statistics.median(x[0] for x in self.samples),
+               "sm_max_mhz": max(x[1] for x in self.samples), "reasons": reasons, "samples": len(self.samples),
+               "source": "nvml" if self.thread is not None else "nvidia-smi"}
+        tn = getattr(self, "timed_n", None)
+        if tn is not None:
+            timed = self.samples[:tn]
+            out["window"] = ("the timed region and the kernel-timing replays right after it (same kernels, same "
+                             "inputs)")
+            out["timed_region_samples"] = len(timed)
+            out["timed_region_sm_mhz"] = statistics.median(x[0] for x in timed) if timed else None
+        return out
 
 
 def _oracle_request(item):
@@ -421,13 +439,22 @@ def bench_gpu(args):
         return a.elapsed_time(b)
 
     graphs = capture()
+    # The clock sampler runs through the timed region and the kernel-timing
+    # legs right after it (hundreds of replays of the same kernels), so that
+    # the clock record spans more than the K timed steps.
     with ClockSampler(local) as clk:
         elapsed_ms = timed(graphs)
-    # per-kernel launch durations: the same K steps without that kernel, timed
-    # the same way right after; duration = (full - without) / K
-    stage = {}
-    for k in stages:
-        stage[k] = max(0.0, (elapsed_ms - timed(capture(skip=k))) / args.steps)
+        clk.mark_timed_end()
+        # per-kernel launch durations: the same K steps without that kernel,
+        # timed the same way right after; duration = (full - without) / K
+        stage = {}
+        for k in stages:
+            stage[k] = max(0.0, (elapsed_ms - timed(capture(skip=k))) / args.steps)
+        # each kernel alone: one graph per stage of input set 0, replayed with
+        # an L2 flush (a write of twice the L2 size) before every replay, each
+        # replay bracketed by its own CUDA events
+        tree_kv = [t.to(dev) for t in W.tree_kv_rows(works[0], 11)]
+        iso = isolated_times(passes[0], args, dev, stream, tree_kv)
     dom = max(("attention", "verify"), key=lambda k: stage[k])
 
     # emitted tokens per step (verify inputs do not change between steps of one set)
@@ -450,6 +477,12 @@ def bench_gpu(args):
     avg = stage
     kernels = {k: {"ms": avg[k], "bytes": algo[k], "gbs": algo[k] / (avg[k] * 1e-3) / 1e9 if avg[k] > 0 else None,
                    "frac_hbm": algo[k] / (avg[k] * 1e-3) / 1e9 / peak if avg[k] > 0 else None} for k in avg}
+    for k, ms in iso.items():
+        kernels.setdefault(k, {"bytes": algo.get(k)})
+        kernels[k]["isolated_ms"] = ms
+        if kernels[k].get("bytes") and ms > 0:
+            kernels[k]["gbs_isolated"] = kernels[k]["bytes"] / (ms * 1e-3) / 1e9
+            kernels[k]["frac_hbm_isolated"] = kernels[k]["gbs_isolated"] / peak
     # the pages' per-unit formulas for the two big kernels: attention flops
     # (unmasked keys only) and the verifier's full-row byte count
     flops = attention_flops(w0)
@@ -462,6 +495,12 @@ def bench_gpu(args):
     full_rows = 4 * w0.V * (w0.T + (n_int if args.mode == "stochastic" else 0))
     kernels["verify"]["bytes_all_rows"] = full_rows
     kernels["verify"]["gbs_all_rows"] = full_rows / (avg["verify"] * 1e-3) / 1e9 if avg["verify"] > 0 else None
+    # the walk is sequential in depth: its time per level of the deepest walk
+    levels = max(1, int(passes[0].accept_len[:w0.B].max()))
+    kernels["verify"]["levels"] = levels
+    kernels["verify"]["us_per_level"] = 1e3 * avg["verify"] / levels
+    if "isolated_ms" in kernels["verify"]:
+        kernels["verify"]["us_per_level_isolated"] = 1e3 * kernels["verify"]["isolated_ms"] / levels
     achieved = kernels[dom]["gbs"]
     launches_per_step = 4 + (1 if _attn_splits(passes[0]) > 1 else 0) + (1 if _verify_uses_stats(w0, args.mode) else 0)
     traffic = _profiled_traffic(dom, args.mode, args.workload)
@@ -485,8 +524,10 @@ def bench_gpu(args):
                        "l2": (f"{n_sets} rotating input sets of {_set_mb(works[0]):.0f} MB each (inputs larger than L2)"
                               if n_sets > 1 else f"one input set of {_set_mb(works[0]):.0f} MB (larger than L2)"),
                        "launch": "one CUDA graph per step (the C-ABI calls of the pass captured, no event nodes)",
-                       "kernel_timing": "per kernel: (K timed steps - the same K steps without that kernel) / K, "
-                                        "each run bracketed by CUDA events on the replay stream",
+                       "kernel_timing": "per kernel: ms = (K timed steps - the same K steps without that kernel) "
+                                        "/ K, each run bracketed by CUDA events on the replay stream; isolated_ms = "
+                                        "the kernel's call alone in a graph, L2 flushed before each replay, mean of "
+                                        f"{ISO_REPLAYS} event-bracketed replays",
                        "tokens_per_step": tokens / args.steps / max(world, 1), "status_ok": status_ok,
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "clocks": clk.summary(),
@@ -515,22 +556,65 @@ def bench_gpu(args):
     return 0
 
 
-def _profiled_traffic(kernel, mode, workload=1):
+def _profiled_traffic(kernel, mode, workload=3):
     """DRAM bytes per launch (read + write) of the dominant kernel from the
-    committed ncu summary, or None when the summary is missing or the kernel
-    source changed since the capture."""
+    committed ncu figures (profiles/traffic.json), or None when there is no
+    entry for this kernel, workload and mode, or the kernel source changed
+    since the capture (the entry records the source's sha256 prefix)."""
     import hashlib
     src = {"attention": "attention_tc.cu", "verify": "verify.cu"}[kernel]
     path = os.path.join(ROOT, "tree_speculative_verification_spec_gb300", "csrc", src)
     try:
         digest = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
-        for line in open(os.path.join(ROOT, "profiles", "traffic.md")):
-            f = [x.strip() for x in line.strip().strip("|").split("|")]
-            if len(f) >= 5 and f[0] == kernel and f[1] == str(workload) and f[2] == mode and f[3] == digest:
-                return float(f[4])
-    except (OSError, ValueError):
-        pass
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entries = json.load(f)["entries"]
+    except (OSError, ValueError, KeyError):
+        return None
+    for e in entries:
+        if (e.get("kernel") == kernel and e.get("workload") == workload and e.get("mode") == mode
+                and e.get("source_digest") == digest):
+            return float(e["dram_bytes_per_launch"])
     return None
+
+
+ISO_REPLAYS = 30
+
+
+def isolated_times(vp, args, dev, stream, tree_kv):
+    """Each call of one pass alone (input set 0): captured in its own graph,
+    replayed ISO_REPLAYS times after 3 warm-up replays, with a write of twice
+    the L2 size before every replay and CUDA events on the replay stream
+    around the replay only.  Returns the mean milliseconds per call, by stage
+    (attention includes its split-KV combine; stochastic verification its
+    row statistics when it uses them; append is the tree K/V append)."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(1, 2 * l2 // 4), dtype=torch.int32, device=dev)
+    calls = {"mask": vp.mask_build, "append": lambda: vp.append(*tree_kv),
+             "attention": lambda: vp.attention(args.attn_flags), "verify": lambda: vp.verify(args.mode),
+             "commit": vp.commit}
+    cap = torch.cuda.Stream(dev)
+    out = {}
+    for name, fn in calls.items():
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+        torch.cuda.synchronize()
+        for i in range(3):
+            flush.fill_(i)
+            g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ISO_REPLAYS)]
+        for i, (a, b) in enumerate(ev):
+            flush.fill_(i)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        out[name] = sum(a.elapsed_time(b) for a, b in ev) / ISO_REPLAYS
+        del g
+    return out
 
 
 def _verify_uses_stats(w, mode):
@@ -565,19 +649,25 @@ STEP_INPUTS = ("q", "parent", "tokens", "tree_off", "prefix_len", "p_logits", "q
 
 def run_e2e(args, works, sets, passes, stream, dev, n_sets):
     """The pass through the C ABI with host buffers.  Every step copies its
-    inputs from pinned host memory into one of two device input slots (on a
-    copy stream) and reads its emitted tokens back; step i+1's copy overlaps
-    step i's compute.  The KV cache and block table are resident state, shared
-    by the slots of one input set."""
+    inputs (queries, tree arrays, the rows verification reads, and the tree's
+    K/V rows) from pinned host memory into one of two device input slots (on a
+    copy stream), appends the tree K/V after the prefix, runs the pass and
+    reads its emitted tokens back; step i+1's copy overlaps step i's compute.
+    The KV cache and block table are resident state, shared by the slots of
+    one input set."""
     import dataclasses
     import torch
     from tree_speculative_verification_spec_gb300.pipeline import VerifyPass
     steps = max(3, args.steps)
     # the step's inputs: greedy verification reads neither draft rows nor uniforms
     names = [k for k in STEP_INPUTS if args.mode != "greedy" or k not in ("q_probs", "uniforms")]
-    host = []
-    for w in works:
+    import workloads as W
+    host, tree_host = [], []
+    for j, w in enumerate(works):
         host.append({k: getattr(w, k).pin_memory() for k in names})
+        # the tree's keys and values as the caller computes them: copied in and
+        # appended after the prefix every step
+        tree_host.append([t.pin_memory() for t in W.tree_kv_rows(w, 500 + j)])
     # two device slots per input set: the set's own buffers, and a shadow
     # with fresh per-step inputs and the same cache (and a pass of its own)
     slots = []
@@ -586,11 +676,13 @@ def run_e2e(args, works, sets, passes, stream, dev, n_sets):
         shadow = dataclasses.replace(d, **{k: torch.empty_like(getattr(d, k)) for k in names})
         vp2 = VerifyPass(shadow)
         vp2.inv_temp, vp2.q_layout = passes[j].inv_temp, passes[j].q_layout
-        slots.append([(d, passes[j]), (shadow, vp2)])
+        kv = [[torch.empty_like(t, device=dev) for t in tree_host[j]] for _ in range(2)]
+        slots.append([(d, passes[j], kv[0]), (shadow, vp2, kv[1])])
     out_tok = [[torch.empty((p.batch.B, p.batch.n_max), dtype=torch.int32).pin_memory() for _ in range(2)]
                for p in passes]
     out_n = [[torch.empty(p.batch.B, dtype=torch.int32).pin_memory() for _ in range(2)] for p in passes]
     h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    h2d += sum(t.numel() * t.element_size() for t in tree_host[0])
     d2h = out_tok[0][0].numel() * 4 + out_n[0][0].numel() * 4
     copy_stream = torch.cuda.Stream(dev)
     copied = [[torch.cuda.Event() for _ in range(2)] for _ in range(n_sets)]
@@ -599,16 +691,18 @@ def run_e2e(args, works, sets, passes, stream, dev, n_sets):
 
     def e2e_step(i):
         j, k = i % n_sets, (i // n_sets) % 2
-        d, vp = slots[j][k]
+        d, vp, kv = slots[j][k]
         h = host[j]
         with torch.cuda.stream(copy_stream):
             if used[j][k]:
                 copy_stream.wait_event(consumed[j][k])  # the slot's previous pass has read its inputs
             for name, t in h.items():
                 getattr(d, name).copy_(t, non_blocking=True)
+            for dst, src in zip(kv, tree_host[j]):
+                dst.copy_(src, non_blocking=True)
             copied[j][k].record(copy_stream)
         stream.wait_event(copied[j][k])
-        vp.run(args.mode, args.attn_flags)
+        vp.run(args.mode, args.attn_flags, tree_kv=kv)
         consumed[j][k].record(stream)
         used[j][k] = True
         out_tok[j][k].copy_(vp.emitted, non_blocking=True)
@@ -636,7 +730,8 @@ def run_e2e(args, works, sets, passes, stream, dev, n_sets):
     return {"value": toks / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d * world,
             "d2h_bytes_per_step": d2h * world,
             "ms_per_step": ms / steps,
-            "overlap": "step i+1's host-to-device copy (copy stream) overlaps step i's pass; two input slots"}
+            "overlap": "step i+1's host-to-device copy (copy stream) overlaps step i's pass; two input slots",
+            "pass": "mask build, tree K/V append (rows copied from the host), attention, verification, commit"}
 
 
 def measure_commit_layers(L, vp, dev, reps=20, replays=5):
@@ -858,7 +953,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--mode", default=None, choices=["stochastic", "greedy"])
-    ap.add_argument("--workload", type=int, default=1, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", type=int, default=3, choices=sorted(WORKLOADS))
     ap.add_argument("--attn-flags", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0, help="offset added to the workload's input seeds")
