@@ -214,6 +214,14 @@ size_t spec_verify_workspace_size(int B, int n_max, int V);
  *                              n_b outside [0, n_max]) and SPEC_DEV_BAD_TOKEN; a request whose
  *                              status is non-zero after the call has accept_len = n_emitted = 0
  *                              and -1 rows.
+ * Both verifiers are launched as programmatic dependents of the previous
+ * kernel in the stream (tree attention lets them launch once its CTAs have
+ * issued their last MMA): their prologue (input checks, the root row's
+ * copy) may overlap that kernel, and they read the status word only after
+ * waiting for it to finish.  A kernel that allows programmatic dependents and
+ * sits right before a verify call must therefore not write p_logits,
+ * q_probs, tokens, parent, tree_off, uniforms or inv_temperature; kernels
+ * that do not allow it are waited for in full.
  */
 spec_status spec_tree_verify_greedy(const float* p_logits, const int32_t* tokens, const int32_t* parent,
                                     const int32_t* tree_off, int B, int n_max, int V,

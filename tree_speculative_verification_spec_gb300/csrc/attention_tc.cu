@@ -507,6 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&pv_done[j & 1]);
           umma_commit(&v_empty[j % VST]);
         }
+        // the CTA's last MMA is out: kernels launched as programmatic
+        // dependents (the verifier) may start their prologue
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         umma_commit(&drain);
         mbar_wait(&drain, 0, &abort_flag);
       }

@@ -519,6 +519,14 @@ constexpr int kStatsWarps = kStatsThreads / 32;
 __global__ void __launch_bounds__(kStatsThreads) row_stats_kernel(VerifyArgs a, RowStats* stats) {
   __shared__ float smax[kStatsWarps];
   __shared__ unsigned long long ssum[kStatsWarps];
+  // Launched as a programmatic dependent of the previous kernel (whose
+  // outputs it does not read): every CTA waits for that kernel before it
+  // exits, so the walk after this grid finds that kernel's results too.
+  struct WaitOnExit {
+    __device__ ~WaitOnExit() {
+      if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+  } wait_on_exit;
   const int b = blockIdx.x / a.n_max, u = blockIdx.x % a.n_max;
   const int off = a.tree_off[b];
   const int n = a.tree_off[b + 1] - off;
@@ -615,10 +623,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
   const bool vec = a.vec != 0;
   int32_t* status = &a.status[b];
   int xk = 0;  // exchange counter
-  const int st_in = *(volatile int32_t*)status;
   constexpr int kOwnBits = SPEC_DEV_BAD_TOKEN | SPEC_DEV_BAD_TREE | SPEC_DEV_BAD_TEMP;
   const float tau = MODE == 1 ? request_tau(a, b) : 1.0f;
-  const bool may_run = n >= 1 && n <= a.n_max && (st_in & ~kOwnBits) == 0 && tau_ok(tau);
+  // The status word comes from the kernels before this one (this kernel is
+  // launched as their programmatic dependent and may start before the last
+  // of them ends): it is read only after griddepcontrol.wait below.  Until
+  // then the walk's own inputs are checked and the root's slice copied.
+  const bool may_run = n >= 1 && n <= a.n_max && tau_ok(tau);
 
   // stochastic: the root's target slice is copied while the inputs are checked
   float* D = reinterpret_cast<float*>(dyn_smem);  // current weights of this CTA's slice
@@ -645,9 +656,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
   // inputs; the only status bits this kernel sets are those checks' (by rank
   // 0, when every CTA of the cluster skips the walk), so ignoring them in the
   // incoming status keeps the decision uniform.
-  int bad = 0;
-  bool skip = (st_in & ~kOwnBits) != 0;
-  if (!skip) {
+  int bad;
+  {
     const int nc = min(max(n, 0), a.n_max);  // nodes whose entries are checked
     bool bt = false, bp = n < 0 || n > a.n_max;
     for (int i = threadIdx.x; i < nc; i += kWalkThreads) {
@@ -659,8 +669,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
     }
     bad = (__syncthreads_or(bt) ? SPEC_DEV_BAD_TOKEN : 0) | (__syncthreads_or(bp) ? SPEC_DEV_BAD_TREE : 0) |
           (tau_ok(tau) ? 0 : SPEC_DEV_BAD_TEMP);
-    skip = bad != 0 || n == 0;
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int st_in = *(volatile int32_t*)status;
+  // a request flagged upstream is skipped without this kernel's own checks
+  if ((st_in & ~kOwnBits) != 0) bad = 0;
+  const bool skip = (st_in & ~kOwnBits) != 0 || bad != 0 || n == 0;
   if constexpr (C > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   __syncthreads();
   if (skip) {
@@ -1173,13 +1187,18 @@ cudaError_t launch_walk(const VerifyArgs& a, int B, cudaStream_t stream) {
   cfg.blockDim = dim3(kWalkThreads, 1, 1);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  // a programmatic dependent of the previous kernel (tree attention lets it
+  // launch as its CTAs finish their last tile): the prologue overlaps that
+  // kernel's tail, and the status word is read after griddepcontrol.wait
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = C > 1 ? 1 : 0;
+  cfg.numAttrs = C > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
@@ -1249,8 +1268,17 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
     RowStats* st = static_cast<RowStats*>(workspace);
     const long long ctas = (long long)B * a.n_max;
     if (ctas > 0 && ctas < (1LL << 31)) {
-      row_stats_kernel<<<(unsigned)ctas, kStatsThreads, 0, stream>>>(a, st);
-      if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+      cfg.blockDim = dim3(kStatsThreads, 1, 1);
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, row_stats_kernel, a, st) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+        return SPEC_ERR_CUDA;
       a.stats = st;
     }
   }
