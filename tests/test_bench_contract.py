@@ -50,3 +50,28 @@ def test_algorithmic_formulas_on_a_small_workload():
     kv = sum(2 * w.Hkv * w.D * 2 * (int(w.prefix_len[b]) + int(n[b])) for b in range(w.B))
     qo = sum(2 * int(n[b]) * w.Hq * w.D * 2 for b in range(w.B))
     assert ab["attention"] == kv + qo + sum(8 * int(n[b]) * W_ for b in range(w.B))
+
+
+def test_traffic_lookup_matches_kernel_workload_mode_and_source_digest(tmp_path, monkeypatch):
+    """bench.py reports DRAM traffic only from an entry of profiles/traffic.json
+    whose kernel, workload, mode and source digest all match the current
+    source; anything else gives None (the figure is then unmeasured)."""
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    src = os.path.join(ROOT, "tree_speculative_verification_spec_gb300", "csrc", "attention_tc.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    root = tmp_path / "repo"
+    (root / "profiles").mkdir(parents=True)
+    (root / "tree_speculative_verification_spec_gb300" / "csrc").mkdir(parents=True)
+    (root / "tree_speculative_verification_spec_gb300" / "csrc" / "attention_tc.cu").write_bytes(open(src, "rb").read())
+    entries = [dict(kernel="attention", workload=3, mode="greedy", source_digest=digest, dram_bytes_per_launch=123.0),
+               dict(kernel="attention", workload=1, mode="greedy", source_digest="0" * 16, dram_bytes_per_launch=9.0)]
+    (root / "profiles" / "traffic.json").write_text(json.dumps({"entries": entries}))
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench._profiled_traffic("attention", "greedy", 3) == 123.0
+    assert bench._profiled_traffic("attention", "stochastic", 3) is None  # other mode
+    assert bench._profiled_traffic("attention", "greedy", 4) is None      # other workload
+    assert bench._profiled_traffic("attention", "greedy", 1) is None      # stale digest
+    (root / "profiles" / "traffic.json").write_text("not json")
+    assert bench._profiled_traffic("attention", "greedy", 3) is None
