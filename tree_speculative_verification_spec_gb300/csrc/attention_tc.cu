@@ -280,18 +280,35 @@ __device__ __forceinline__ void produce_ring(uint32_t ring, const CUtensorMap* m
 // comparisons on a shared copy); batches above kOrderMax keep their order.
 constexpr int kOrderMax = 256;
 // `len` is scratch shared memory of kOrderMax ints (the first bytes of the
-// K ring, which no copy has reached yet).
-__device__ __forceinline__ int request_by_length(const AttnArgs& a, int slot, int* len) {
-  if (a.B < 2 || a.B > kOrderMax) return slot;
-  __shared__ int pick;
-  for (int i = threadIdx.x; i < a.B; i += blockDim.x) len[i] = a.prefix_len[i] + (a.tree_off[i + 1] - a.tree_off[i]);
-  if (threadIdx.x == 0) pick = slot;
+// K ring, which no copy has reached yet).  Thread c ranks candidate c and,
+// if c is the slot's request, hands over the offset, node count and prefix
+// length it already loaded: a CTA without rows then leaves right after the
+// ranking, and no dependent global load follows it.
+struct Request {
+  int b, off, n, P;
+};
+static_assert(kThreads >= kOrderMax, "one ranking thread per candidate");
+__device__ __forceinline__ Request request_by_length(const AttnArgs& a, int slot, int* len) {
+  if (a.B < 2 || a.B > kOrderMax) {
+    const int off = a.tree_off[slot];
+    return Request{slot, off, a.tree_off[slot + 1] - off, a.prefix_len[slot]};
+  }
+  __shared__ Request pick;
+  const int c = threadIdx.x;
+  int off = 0, n = 0, P = 0;
+  if (c < a.B) {
+    off = a.tree_off[c];
+    n = a.tree_off[c + 1] - off;
+    P = a.prefix_len[c];
+    len[c] = P + n;
+  }
+  if (threadIdx.x == 0) pick = Request{slot, 0, 0, 0};  // replaced below: the ranks are a permutation
   __syncthreads();
-  for (int c = threadIdx.x; c < a.B; c += blockDim.x) {
+  if (c < a.B) {
     const int L = len[c];
     int rank = 0;
     for (int j = 0; j < a.B; ++j) rank += (len[j] > L) || (len[j] == L && j < c);
-    if (rank == slot) pick = c;
+    if (rank == slot) pick = Request{c, off, n, P};
   }
   // the ring's TMA writes (async proxy) come after these generic accesses
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -323,10 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 1024-byte aligned dynamic shared memory (128-byte swizzle atoms)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
-  const int b = request_by_length(a, blockIdx.z / a.Hkv, reinterpret_cast<int*>(smem + L_::kOffK));
-  const int off = a.tree_off[b];
-  const int n = a.tree_off[b + 1] - off;
-  const int P = a.prefix_len[b];
+  const Request rq = request_by_length(a, blockIdx.z / a.Hkv, reinterpret_cast<int*>(smem + L_::kOffK));
+  const int b = rq.b, off = rq.off, n = rq.n, P = rq.P;
   const int g = a.g;
   const int R = n * g;
   // The grid never completes before the previous kernel of the stream (its
