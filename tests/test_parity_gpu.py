@@ -571,6 +571,10 @@ TC_CASES = [  # (B, n_range, prefix_range, Hq, Hkv, D, block_size)
     (2, (5, 90), (200, 700), 16, 4, 64, 16),
     (1, (128, 128), (127, 127), 4, 1, 64, 512),
     (4, (1, 3), (1, 2000), 32, 8, 128, 128),        # few rows: padded 128-row tile
+    # more CTAs than SMs (the multi-wave instantiation): D 64 with Q by TMA,
+    # and g = 3 (Q staged by the threads)
+    (64, (20, 60), (50, 300), 16, 4, 64, 16),
+    (48, (10, 40), (30, 200), 12, 4, 128, 16),
 ]
 
 
@@ -605,6 +609,29 @@ def test_attention_capacity_and_bad_blocks():
     got, st = _gpu_attention(w, max_prefix=int(w.prefix_len.max()))
     assert st[0] & S.SPEC_DEV_CAPACITY and st[1] & S.SPEC_DEV_BAD_BLOCK and st[2] == 0
     assert s_ref[0] & O.ST_CAPACITY and s_ref[1] & O.ST_BAD_BLOCK
+
+
+def test_attention_capacity_and_bad_blocks_multi_wave():
+    # 200 requests x 2 kv-heads: more CTAs than SMs
+    w = W.small_random(10, B=200, n_range=(2, 6), prefix_range=(10, 60), Hq=4, Hkv=2, D=128, dtype=W.BF16, V=16,
+                       block_size=16)
+    w.prefix_len[7] = w.block_table.shape[1] * 16  # beyond the block table
+    w.block_table[150, 0] = w.num_blocks + 5       # bad block id
+    ref, _, s_ref = oracle_attention(w)
+    got, st = _gpu_attention(w, S.SPEC_ATTN_TCGEN05, max_prefix=int(w.prefix_len.max()))
+    flagged = {7: S.SPEC_DEV_CAPACITY, 150: S.SPEC_DEV_BAD_BLOCK}
+    for b in range(w.B):
+        assert st[b] == flagged.get(b, 0), (b, int(st[b]))
+    assert s_ref[7] & O.ST_CAPACITY and s_ref[150] & O.ST_BAD_BLOCK
+    # rows of the other requests match the oracle
+    ref32 = (ref.astype(np.uint32) << 16).view(np.float32)
+    g = got.reshape(ref32.shape)
+    to = w.tree_off.numpy()
+    keep = np.ones(w.T, bool)
+    for b in flagged:
+        keep[to[b]:to[b + 1]] = False
+    bad = ~attn_tolerance_ok(g[keep], ref32[keep], w.dtype)
+    assert not bad.any(), int(bad.sum())
 
 
 def _sampled_rows(w, k, seed):
