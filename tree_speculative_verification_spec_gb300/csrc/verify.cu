@@ -10,8 +10,9 @@
 //
 // The C CTAs of a cluster split the vocabulary into C slices.  Each row
 // reduction (max, argmax, fixed-point sums, the exclusive prefix of the final
-// sample) is a block reduction followed by one cluster barrier and reads of
-// the peers' exchange slots in distributed shared memory.  Every CTA takes
+// sample) is a block reduction followed by one push of the CTA's value into
+// every peer's shared memory (st.async, completing on the peer's mbarrier):
+// one one-way trip, no cluster barrier.  Every CTA takes
 // the same decisions: they depend only on cluster-reduced values and on
 // single entries (a child's logit and draft probability) that each CTA reads
 // and evaluates itself.  While a node is processed, the row slices its
