@@ -316,10 +316,11 @@ __device__ __forceinline__ Request request_by_length(const AttnArgs& a, int slot
   return pick;
 }
 
-// STAGGER: the grid is one wave (at most one CTA per SM), and the K and V
-// rings fill tile by tile (see produce_ring).  A separate instantiation, so
-// that multi-wave launches run code without it.
-template <int D, bool STAGGER>
+// ONE_WAVE: the grid is one wave (at most one CTA per SM, all starting at
+// once).  Its K and V rings fill tile by tile (see produce_ring), and one lane
+// per softmax warp polls the barriers.  A separate instantiation, so that
+// multi-wave launches run code without either.
+template <int D, bool ONE_WAVE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                    const __grid_constant__ CUtensorMap tmap_q, const TcParams prm) {
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], kSoftmaxThreads);
+      mbar_init(&p_full[i], kSoftmaxThreads / 32);  // one arrival per softmax warp
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(&q_full, prm.q_tma ? 1 : kThreads - 96);
@@ -429,12 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
     }
-    produce_ring<D, KST, STAGGER>(sbase + L_::kOffK, &tmap_k, prm, b, kvh, k_begin, Lk, P, ntiles, k_full, k_empty,
+    produce_ring<D, KST, ONE_WAVE>(sbase + L_::kOffK, &tmap_k, prm, b, kvh, k_begin, Lk, P, ntiles, k_full, k_empty,
                                   &bad_block, &abort_flag);
     if (lane == 0 && prm.q_tma) mbar_wait(&q_full, 0, &abort_flag);  // the Q copy has landed before any exit
   } else if (warp == 2) {
     // ---------------------------------------------------------- V producer
-    produce_ring<D, VST, STAGGER>(sbase + L_::kOffV, &tmap_v, prm, b, kvh, k_begin, Lk, P, ntiles, v_full, v_empty,
+    produce_ring<D, VST, ONE_WAVE>(sbase + L_::kOffV, &tmap_v, prm, b, kvh, k_begin, Lk, P, ntiles, v_full, v_empty,
                                   &bad_block, &abort_flag);
   } else if (warp == 1) {
     // --------------------------------------------------------- QK issuer
@@ -553,8 +554,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY;
       float2 lacc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
       bool ok = true;
-      // tcgen05.ld / st are warp-collective: every decision before one is warp-uniform
+      // tcgen05.ld / st are warp-collective: every decision before one is
+      // warp-uniform.  In a one-wave grid one lane per warp polls and the warp
+      // follows it (fewer shared-memory polls beside the MMAs' operand reads:
+      // wide ensemble 63.6 -> 61.0 us); in multi-wave grids every lane polls
+      // (batched serving measured 398 -> 404 us with one).
       auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (ONE_WAVE) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(bar, parity, &abort_flag);
+          __syncwarp();
+          return __shfl_sync(0xffffffffu, w, 0);
+        }
         const bool w = mbar_wait(bar, parity, &abort_flag);
         return __all_sync(0xffffffffu, w);
       };
@@ -681,7 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(sl + lane_off, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full[j & 1]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[j & 1]);
       }
       // epilogue: merge the halves; this thread writes output columns
       // half*D/2 .. half*D/2 + D/2 - 1 of its row
