@@ -575,6 +575,7 @@ TC_CASES = [  # (B, n_range, prefix_range, Hq, Hkv, D, block_size)
     # and g = 3 (Q staged by the threads)
     (64, (20, 60), (50, 300), 16, 4, 64, 16),
     (48, (10, 40), (30, 200), 12, 4, 128, 16),
+    (2, (5, 40), (50, 300), 6, 2, 128, 16),          # one wave, g = 3 (Q staged by the threads)
 ]
 
 
@@ -609,6 +610,23 @@ def test_attention_capacity_and_bad_blocks():
     got, st = _gpu_attention(w, max_prefix=int(w.prefix_len.max()))
     assert st[0] & S.SPEC_DEV_CAPACITY and st[1] & S.SPEC_DEV_BAD_BLOCK and st[2] == 0
     assert s_ref[0] & O.ST_CAPACITY and s_ref[1] & O.ST_BAD_BLOCK
+
+
+@pytest.mark.parametrize("extra", [0, 1])
+def test_attention_one_wave_boundary(extra):
+    # exactly one CTA per SM (the one-wave instantiation), then one more (the
+    # multi-wave one): one kv-head and at most 128 rows per request, so the
+    # grid has B CTAs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    w = W.small_random(40 + extra, B=sms + extra, n_range=(1, 32), prefix_range=(1, 200), Hq=4, Hkv=1, D=128,
+                       dtype=W.BF16, V=16, block_size=16)
+    ref, _, s_ref = oracle_attention(w)
+    got, st = _gpu_attention(w, S.SPEC_ATTN_TCGEN05)
+    assert (st[:w.B] == 0).all() and (s_ref == 0).all()
+    ref32 = (ref.astype(np.uint32) << 16).view(np.float32)
+    g = got.reshape(ref32.shape)
+    bad = ~attn_tolerance_ok(g, ref32, w.dtype)
+    assert not bad.any(), (int(bad.sum()), float(np.abs(g - ref32).max()))
 
 
 def test_attention_capacity_and_bad_blocks_multi_wave():
