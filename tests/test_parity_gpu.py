@@ -114,7 +114,8 @@ def _assert_verify_equal(got, ref, B):
 SMALL_VERIFY = [dict(seed=s, B=B, n_range=nr, V=V) for s, B, nr, V in [
     (1, 4, (1, 12), 2), (2, 6, (1, 40), 7), (3, 5, (0, 64), 64), (4, 3, (1, 300), 513), (5, 2, (60, 90), 1000),
     (6, 8, (1, 30), 4099), (7, 2, (10, 30), 32000), (8, 1, (5, 9), 40000), (9, 2, (3, 20), 128256),
-    (10, 1, (3, 12), 131072)]]  # the largest vocabulary the library takes
+    (10, 1, (3, 12), 131072),  # the largest vocabulary the library takes
+    (11, 12, (1, 40), 32000), (12, 7, (2, 20), 131072)]]  # 12-CTA clusters (5 to 12 requests)
 
 
 @pytest.mark.parametrize("cfg", SMALL_VERIFY, ids=lambda c: f"V{c['V']}_s{c['seed']}")

@@ -1203,31 +1203,33 @@ cudaError_t launch_walk(const VerifyArgs& a, int B, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// How many 16-CTA clusters of the walk can be resident at once on the
-// current device (queried once per device and mode; 0 if none).
-template <int MODE>
-int clusters16(size_t dyn) {
+// How many CS-CTA clusters of the walk can be resident at once on the
+// current device (queried once per device, mode and size; 0 if none).
+// CS > 8 needs the non-portable cluster size.
+template <int MODE, int CS>
+int resident_clusters(size_t dyn) {
   static int cache[2][128];
   static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return false;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
   std::lock_guard<std::mutex> lock(mu);
   int& c = cache[MODE][dev];
   if (c == 0) {
-    auto kern = verify_walk_kernel<MODE, 16>;
+    auto kern = verify_walk_kernel<MODE, CS>;
     int n = 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(16, 1, 1);
+    cfg.gridDim = dim3(CS, 1, 1);
     cfg.blockDim = dim3(kWalkThreads, 1, 1);
     cfg.dynamicSmemBytes = dyn;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.x = CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+    const bool ok = (CS <= 8 || cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                                    cudaSuccess) &&
                     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) ==
                         cudaSuccess &&
                     cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1;
@@ -1253,11 +1255,19 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
   if (!workspace || ws_bytes < kVerifyWorkspace) return SPEC_ERR_WORKSPACE;
   spec_workspace_canary(workspace, ws_bytes, stream);
   int C = walk_cluster(B, a.V, MODE, false);
-  if (C == 8 && walk_cluster(B, a.V, MODE, true) == 16) {
-    // only when every request's cluster is resident at once: a cluster that
-    // waits for another to finish costs more than the wider slices save
-    const int s16 = (((a.V + 15) / 16) + 3) & ~3;
-    if (clusters16<MODE>(MODE == 1 ? 3 * (size_t)s16 * sizeof(float) : 0) >= B) C = 16;
+  if (C == 8) {
+    // wider clusters only when every request's cluster is resident at once: a
+    // cluster that waits for another to finish costs more than the shorter
+    // slices save.  16 CTAs for at most 4 requests, else 12 while B * 12 CTAs
+    // fit one per SM (decode layer, 8 requests: 22.9 -> 21.9 us against 8;
+    // 16 there leaves one of the 8 clusters waiting: 28.2 us)
+    const int s16 = (((a.V + 15) / 16) + 3) & ~3, s12 = (((a.V + 11) / 12) + 3) & ~3;
+    if (walk_cluster(B, a.V, MODE, true) == 16 &&
+        resident_clusters<MODE, 16>(MODE == 1 ? 3 * (size_t)s16 * sizeof(float) : 0) >= B)
+      C = 16;
+    else if ((long long)B * 12 <= kTargetCtas &&
+             resident_clusters<MODE, 12>(MODE == 1 ? 3 * (size_t)s12 * sizeof(float) : 0) >= B)
+      C = 12;
   }
   a.slice = (((a.V + C - 1) / C) + 3) & ~3;
   if (MODE == 1 && a.slice > kMaxSlice) return SPEC_ERR_UNSUPPORTED;
@@ -1289,6 +1299,7 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
     case 2: e = launch_walk<MODE, 2>(a, B, stream); break;
     case 4: e = launch_walk<MODE, 4>(a, B, stream); break;
     case 8: e = launch_walk<MODE, 8>(a, B, stream); break;
+    case 12: e = launch_walk<MODE, 12>(a, B, stream); break;
     default: e = launch_walk<MODE, 16>(a, B, stream); break;
   }
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
