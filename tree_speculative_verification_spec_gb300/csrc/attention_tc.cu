@@ -859,10 +859,10 @@ static cudaError_t launch_tc_d(const AttnArgs& a, cudaStream_t stream) {
   if (!prm.q_tma) mq = mk;  // unused
   const int rows_max = a.n_max * a.g;
   dim3 grid((rows_max + tc::BM - 1) / tc::BM, a.splits, a.B * a.Hkv);
-  // Tile-by-tile ring fills only when every CTA starts at once (one CTA per
-  // SM).  Measured: decode layer 22.8 -> 22.1 us, wide ensemble 64.2 -> 63.9
-  // us; the same rule on the first wave of a multi-wave grid cost batched
-  // serving 398 -> 412 us.
+  // The one-wave instantiation when every CTA starts at once (one CTA per
+  // SM): tile-by-tile ring fills (decode layer 22.8 -> 22.1 us, wide ensemble
+  // 64.2 -> 63.9 us; on the first wave of a multi-wave grid they cost batched
+  // serving 398 -> 412 us) and one poller per softmax warp (see wait_warp).
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
