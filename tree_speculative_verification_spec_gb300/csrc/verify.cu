@@ -609,7 +609,12 @@ __global__ void __launch_bounds__(kStatsThreads) row_stats_kernel(VerifyArgs a, 
 // The walk
 // ---------------------------------------------------------------------------
 
-template <int MODE, int C>
+// LEAN: a stochastic walk without row statistics and with per-parent draft
+// rows, its most common form, compiled without the code of the other two
+// (one launch runs each code region only a few times, so instruction fetch
+// shows: decode layer 22.0 -> 21.1 us, wide ensemble 38.7 -> 37.4 us).  The
+// greedy walk has one form.
+template <int MODE, int C, bool LEAN>
 __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs a) {
   extern __shared__ float4 dyn_smem[];
   __shared__ WalkShared sh;
@@ -803,8 +808,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
     // their order does not matter; only the final sample scans in index order.
     float4* D4 = reinterpret_cast<float4*>(D);
     const int len4 = len >> 2;
-    const bool use_stats = a.stats != nullptr;
-    const bool per_child = a.q_per_child != 0;
+    const bool use_stats = !LEAN && a.stats != nullptr;
+    const bool per_child = !LEAN && a.q_per_child != 0;
     // the draft slice is copied on demand (at a rejection, into buffer 0)
     // with row statistics or per-child rows; otherwise at node entry
     const bool q_lazy = use_stats || per_child;
@@ -1171,7 +1176,8 @@ constexpr int kStatsMaxCluster = 2;
 
 template <int MODE, int C>
 cudaError_t launch_walk(const VerifyArgs& a, int B, cudaStream_t stream) {
-  auto kern = verify_walk_kernel<MODE, C>;
+  const bool lean = MODE == 0 || (a.stats == nullptr && a.q_per_child == 0);
+  auto kern = lean ? verify_walk_kernel<MODE, C, true> : verify_walk_kernel<MODE, C, MODE == 0>;
   // stochastic: the target slice and two draft buffers; with row statistics
   // the second draft buffer's room also holds 6 words per node
   size_t words = MODE == 1 ? 3 * (size_t)a.slice : 0;
@@ -1215,7 +1221,7 @@ int resident_clusters(size_t dyn) {
   std::lock_guard<std::mutex> lock(mu);
   int& c = cache[MODE][dev];
   if (c == 0) {
-    auto kern = verify_walk_kernel<MODE, CS>;
+    auto kern = verify_walk_kernel<MODE, CS, true>;
     int n = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CS, 1, 1);
