@@ -404,6 +404,7 @@ struct VerifyArgs {
   const RowStats* stats;  // stochastic: every node's row statistics, or null (the walk computes them)
   const float* inv_temp;  // stochastic: per-request inverse temperature, or null (1)
   int q_per_child;        // stochastic: q_probs row c is child c's own draft row (else row u serves u's children)
+  int ahead;              // stochastic without statistics: a fourth slice receives the first child's target slice
 };
 
 // A request's inverse temperature tau (1 without an array); usable iff
@@ -415,6 +416,7 @@ struct WalkShared {
   Red red;
   Exch ex;
   uint64_t dbar, qbar[2];       // stochastic: slice copies of the target and draft rows
+  uint64_t nbar;                // stochastic: the copy of the first child's target slice
   int32_t par[SPEC_MAX_NODES];  // the request's parent array
   int32_t tok[SPEC_MAX_NODES];  // the request's tokens
   int32_t aux[SPEC_MAX_NODES];  // greedy: argmax of frontier nodes; stochastic: the path
@@ -649,6 +651,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.dbar)) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.qbar[0])) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.qbar[1])) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.nbar)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (root_copy) start_copy(D, a.p_logits + (size_t)off * V + x0, (uint32_t)len * 4, &sh.dbar);
     else if (MODE == 0 && may_run && vec) prefetch_l2(a.p_logits + (size_t)off * V + x0, (uint32_t)len * 4);
@@ -809,6 +812,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
     float4* D4 = reinterpret_cast<float4*>(D);
     const int len4 = len >> 2;
     const bool use_stats = !LEAN && a.stats != nullptr;
+    // the copy ahead: at each node the first child's target slice goes into a
+    // spare buffer while the node is decided; accepting that child swaps the
+    // buffers instead of copying its slice after the decision
+    const bool ahead = !use_stats && a.ahead != 0 && vec && len > 0;
+    float* Dn = Qb + 2 * a.slice;  // the spare buffer (the fourth slice)
+    uint32_t nphase = 0;
+    bool npend = false;  // a copy into Dn is in flight (or landed and not yet waited for)
     const bool per_child = !LEAN && a.q_per_child != 0;
     // the draft slice is copied on demand (at a rejection, into buffer 0)
     // with row statistics or per-child rows; otherwise at node entry
@@ -885,6 +895,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
           }
         }
         if (threadIdx.x == 0) uterm = a.uniforms[off + u].y;
+        if (ahead && k > 0) {  // Dn's last readers finished before the barrier that ended the previous node
+          if (threadIdx.x == 0)
+            start_copy(Dn, a.p_logits + (size_t)(off + sh.s.kids[0]) * V + x0, (uint32_t)len * 4, &sh.nbar);
+          npend = true;
+        }
         if (!q_lazy) {
           if (qpend & (1u << qb)) wait_draft(sh, qb, qphase, qpend, status);
           if (k > 0 && vec && len > 0) {
@@ -1079,8 +1094,22 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
         u = accepted;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();  // D and Q are no longer read before the copies overwrite them
-        if (use_stats) loaded = false;
-        else load_target(u);
+        if (use_stats) {
+          loaded = false;
+        } else if (npend) {
+          wait_copy(&sh.nbar, nphase, status);
+          npend = false;
+          if (u == sh.s.kids[0]) {  // the slice is there: the buffers trade places
+            float* t = D;
+            D = Dn;
+            Dn = t;
+            D4 = reinterpret_cast<float4*>(D);
+          } else {
+            load_target(u);
+          }
+        } else {
+          load_target(u);
+        }
         continue;
       }
 
@@ -1141,6 +1170,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyArgs
       break;
     }
     // no copy may land after the CTA has left
+    if (npend) wait_copy(&sh.nbar, nphase, status);
     if (qpend & 1u) wait_draft(sh, 0, qphase, qpend, status);
     if (qpend & 2u) wait_draft(sh, 1, qphase, qpend, status);
     // path, emitted tokens of the accepted nodes, lengths, -1 tails
@@ -1178,9 +1208,10 @@ template <int MODE, int C>
 cudaError_t launch_walk(const VerifyArgs& a, int B, cudaStream_t stream) {
   const bool lean = MODE == 0 || (a.stats == nullptr && a.q_per_child == 0);
   auto kern = lean ? verify_walk_kernel<MODE, C, true> : verify_walk_kernel<MODE, C, MODE == 0>;
-  // stochastic: the target slice and two draft buffers; with row statistics
-  // the second draft buffer's room also holds 6 words per node
-  size_t words = MODE == 1 ? 3 * (size_t)a.slice : 0;
+  // stochastic: the target slice and two draft buffers (and the spare target
+  // buffer of the copy ahead); with row statistics the second draft buffer's
+  // room also holds 6 words per node
+  size_t words = MODE == 1 ? (a.ahead ? 4 : 3) * (size_t)a.slice : 0;
   if (MODE == 1 && a.stats) words = std::max(words, 2 * (size_t)a.slice + 6 * (size_t)a.n_max);
   const size_t dyn = words * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
@@ -1280,6 +1311,7 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
   a.vec = (a.V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.p_logits) & 15) == 0 &&
           (MODE == 0 || (reinterpret_cast<uintptr_t>(a.q_probs) & 15) == 0);
   a.stats = nullptr;
+  a.ahead = 0;
   if (MODE == 1 && C <= kStatsMaxCluster && ws_bytes >= stats_bytes(B, a.n_max) &&
       (reinterpret_cast<uintptr_t>(workspace) & 15) == 0) {
     RowStats* st = static_cast<RowStats*>(workspace);
@@ -1299,6 +1331,8 @@ spec_status verify_dispatch(VerifyArgs a, int B, void* workspace, size_t ws_byte
       a.stats = st;
     }
   }
+  // the copy ahead when four slices fit in the room of three of the longest
+  if (MODE == 1 && !a.stats && a.vec && 4 * a.slice <= 3 * kMaxSlice) a.ahead = 1;
   cudaError_t e;
   switch (C) {
     case 1: e = launch_walk<MODE, 1>(a, B, stream); break;
