@@ -89,7 +89,9 @@ def algorithmic_bytes(w, stats, mode="stochastic"):
     verify = 4 * w.V * (stats["walk_rows"] + (stats["rejecting_nodes"] if mode == "stochastic" else 0))
     mask = 4 * w.T + 12 * w.T + 8 * w.T * Wd
     commit = 2 * 2 * w.Hkv * w.D * s * stats["moved_rows"]
-    return dict(mask=mask, attention=attn, verify=verify, commit=commit)
+    # the tree's K and V rows: read from the caller's arrays, written to their slots
+    append = 2 * 2 * w.T * w.Hkv * w.D * s
+    return dict(mask=mask, attention=attn, verify=verify, commit=commit, append=append)
 
 
 def attention_flops(w):
